@@ -1,0 +1,175 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 (sm_103a) paged-attention library.
+ *
+ * The library computes, per query head, softmax(q . K^T * scale) . V over a KV
+ * cache cut into fixed-size physical pages that each sequence reaches through
+ * its own block table.  It is the full-attention decode path of a hybrid
+ * Gated-DeltaNet/attention model (24 query heads on 4 KV heads, head_dim 256,
+ * pages of 784 or 832 tokens; dense models use 16-token pages).
+ *
+ * Sources (web pages; cited by title and section):
+ *   "DCU page832 attention" (luanjiahao.me), Sec.1 block-table address math,
+ *     Sec.4 cache shape, Sec.5 tiled loop with online softmax, Sec.6 the
+ *     varlen interface (q, k, v, seqused_k, block_table, max_seqlen_k, causal),
+ *     Sec.7 page-contiguous decode loop.
+ *   "Hybrid SSM decode rate on dual Radeon under vLLM" (cadamcat.github.io),
+ *     section on the upstream split-KV fix: the KV range of one (sequence,
+ *     KV head) is cut across many workgroups, then reduced.
+ *   "Qwen3.8 on MI350P" (flozi.net), Lektion 3: several verify rows share each
+ *     K/V tile, with a causal mask per row and merged softmax statistics.
+ *   "Qwen3.5-27B 6x faster on one RTX 3090" (coreui.cn): new K/V rows are
+ *     written into the cache by a copy (ggml_cpy) before attention reads them.
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA device addresses owned by the caller; the library
+ *     never allocates, frees or synchronises.  Calls are asynchronous on the
+ *     given stream (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *   - Tensors are dense row-major (C order).  bf16 data is IEEE bfloat16.
+ *     Every data pointer must be 16-byte aligned.
+ *   - Host-detectable errors are returned synchronously as a pa_status; nothing
+ *     is launched in that case.  A failed launch returns PA_ERR_CUDA.
+ *   - Device-side errors (which the host cannot see: seq_lens and block tables
+ *     live in device memory) are OR-ed as PA_DEV_* bits into *device_status if
+ *     that pointer is non-NULL.  Kernels never trap; the affected output rows
+ *     are written as zeros.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, inconsistent or negative sizes */
+    PA_ERR_UNSUPPORTED = 2,  /* valid request outside the compiled kernel set */
+    PA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than pa_workspace_bytes() */
+    PA_ERR_CUDA = 4          /* a CUDA runtime/driver call or a launch failed */
+} pa_status;
+
+/* Output element type. */
+typedef enum { PA_OUT_F32 = 0, PA_OUT_BF16 = 1 } pa_out_dtype;
+
+/* Bits OR-ed into *device_status by the kernels. */
+#define PA_DEV_BAD_SEQLEN 1  /* seq_lens[b] < 0, > max_seq_len, or (verify) < q_len */
+#define PA_DEV_BAD_PAGE 2    /* a block_table entry that is read lies outside [0, num_pages) */
+#define PA_DEV_BAD_SLOT 4    /* reshape_and_cache: slot >= num_pages * block_size */
+#define PA_DEV_TIMEOUT 8     /* a bounded wait inside a kernel gave up (never expected) */
+
+/* Shape and launch description of one attention call.
+ *   num_seqs          B, number of sequences (>= 0; 0 is a no-op)
+ *   q_len             query rows per sequence: 1 for decode, > 1 for verify
+ *   num_q_heads       Hq;  num_kv_heads Hkv; Hq % Hkv == 0, G = Hq / Hkv
+ *   head_dim          D (128 or 256)
+ *   block_size        BS, tokens per physical page (a multiple of 16: 16, 784, 832 ...)
+ *   max_pages_per_seq columns of block_table
+ *   max_seq_len       host-side upper bound of seq_lens (plans the split count,
+ *                     like max_seqlen_k of the varlen interface)
+ *   num_pages         P, physical pages in each cache tensor
+ *   scale             softmax scale (1/sqrt(D) for the models here)
+ *   out_dtype         pa_out_dtype
+ *   num_splits        0 = automatic; > 0 forces the split count (benchmarks, tests)
+ *   num_sms           0 = query the current device; > 0 plans for that SM count
+ */
+typedef struct {
+    int32_t num_seqs;
+    int32_t q_len;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t max_pages_per_seq;
+    int32_t max_seq_len;
+    int64_t num_pages;
+    float scale;
+    int32_t out_dtype;
+    int32_t num_splits;
+    int32_t num_sms;
+} pa_attn_desc;
+
+/* What the last successful attention call on this host thread ran: the path
+ * marker the tests and benchmarks record. */
+typedef struct {
+    int32_t path_id;           /* PA_PATH_* */
+    int32_t num_splits;        /* splits of the context per (sequence, KV head) */
+    int32_t chunks_per_split;  /* 16-token chunks per split */
+    int32_t grid_ctas;         /* CTAs of the main kernel */
+    int32_t block_size;
+    int32_t reduce_launched;   /* 1 if the partition-reduce kernel ran */
+} pa_plan_info;
+
+#define PA_PATH_DECODE_CUDA_CORE 1  /* split-KV decode, CUDA cores, TMA-staged chunks */
+#define PA_PATH_VERIFY_MMA 2        /* multi-row verify, tensor-core mma.sync */
+#define PA_PATH_VERIFY_TCGEN05 3    /* multi-row verify, tcgen05 + TMEM */
+
+/* Bytes of device workspace an attention call with this description needs
+ * (split partials: out vectors, max and sum per split).  0 when the plan does
+ * not split.  Returns (size_t)-1 if the description is invalid.  Host only;
+ * queries the device SM count unless desc->num_sms > 0. */
+size_t pa_workspace_bytes(const pa_attn_desc *desc);
+
+/* reshape_and_cache -- write new K/V rows into their page slots.
+ * For every new token i with slot s = slot_mapping[i]:
+ *     k_cache[s / BS, s % BS, h, :] = k_new[i, h, :]   (and the same for V)
+ * with the page/offset split of the block-table address math.  s < 0 marks a
+ * padding token and is skipped; s >= num_pages * BS sets PA_DEV_BAD_SLOT and is
+ * skipped.  The copy is bit-exact.
+ *   k_new, v_new   device bf16 [num_tokens, num_kv_heads, head_dim]
+ *   k_cache,
+ *   v_cache        device bf16 [num_pages, block_size, num_kv_heads, head_dim], written in place
+ *   slot_mapping   device int64 [num_tokens]
+ * head_dim * 2 bytes must be a multiple of 16. */
+pa_status pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                               const int64_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int64_t num_pages,
+                               int32_t *device_status, void *stream);
+
+/* paged_attention_decode -- one query row per sequence (desc->q_len == 1).
+ * out[b, h, :] = sum_{t < L_b} softmax_t(scale * q[b, h, :] . K_t) V_t
+ * with K_t, V_t the rows of token t of KV head h / G, found at
+ * (block_table[b, t / BS], t % BS).  L_b = seq_lens[b] counts every cached
+ * token, including the one just written.  L_b == 0 gives a zero row.
+ * The context is cut into desc-planned splits per (sequence, KV head); each
+ * split runs on its own CTA and a log-sum-exp reduce merges them.
+ *   q            device bf16 [B, Hq, D]
+ *   k_cache,
+ *   v_cache      device bf16 [P, BS, Hkv, D]
+ *   block_table  device int32 [B, max_pages_per_seq]; entries past the last
+ *                page a sequence uses are never read
+ *   seq_lens     device int32 [B]
+ *   out          device [B, Hq, D] of desc->out_dtype
+ *   workspace    device, >= pa_workspace_bytes(desc) bytes (may be NULL if 0)
+ *   device_status nullable device int32, PA_DEV_* bits are OR-ed in */
+pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_table, const int32_t *seq_lens,
+                                    const pa_attn_desc *desc, void *out, void *workspace,
+                                    size_t workspace_bytes, int32_t *device_status, void *stream);
+
+/* paged_attention_verify -- desc->q_len > 1 new rows per sequence, causal among
+ * them (speculative verify).  Rows are ordered (sequence, new row): q and out
+ * are [B * q_len, Hq, D].  Row r (0-based) of sequence b attends to keys
+ * 0 .. L_b - q_len + r inclusive; the q_len new rows must already be in the
+ * cache (L_b >= q_len, else PA_DEV_BAD_SEQLEN and zero rows).  All G * q_len
+ * rows of one KV head share every K/V tile on the tensor cores.  Supported:
+ * G * q_len <= 128.  Other arguments as for decode. */
+pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_table, const int32_t *seq_lens,
+                                    const pa_attn_desc *desc, void *out, void *workspace,
+                                    size_t workspace_bytes, int32_t *device_status, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *pa_status_string(pa_status status);
+
+/* Copies the plan of the last successful attention call made on this host
+ * thread.  PA_ERR_INVALID_ARG if info is NULL or no call was made yet. */
+pa_status pa_last_plan(pa_plan_info *info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,331 @@
+/*
+ * pa_oracle.c -- plain, slow, obviously-correct CPU oracle for paged attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * execute this file.  Its only users are the test suite, the smoke check in
+ * __graft_entry__.py, and the CPU-baseline leg of bench.py.  It shares no code,
+ * header, table or helper with the CUDA kernels of paged_attention_decode_split_gb300.
+ *
+ * Everything is computed in IEEE double precision.  bf16 inputs are widened to
+ * double exactly (a bf16 value is the top 16 bits of an IEEE binary32 value).
+ *
+ * Sources (web pages this library restates; cited by title and section):
+ *   [DCU-832]  "DCU page832 attention" (luanjiahao.me, 2026-07-17):
+ *              Sec.1 block-table address math; Sec.4 K/V cache shape
+ *              [num_physical_pages, BLOCK_SIZE, kv_heads, head_size] after unbind;
+ *              Sec.5 per-tile loop score = dot(Q,K)*scale + online softmax;
+ *              Sec.7 page-contiguous decode loop ("no logical page is skipped,
+ *              the causal range is unchanged").
+ *   [RADEON]   "Hybrid SSM decode rate on dual Radeon under vLLM"
+ *              (cadamcat.github.io, hybrid-ssm-collapse), section on the
+ *              upstream fix vllm#45916: the KV range is cut across many
+ *              workgroups and the pieces are reduced afterwards.
+ *   [MI350P]   "Qwen3.8 on MI350P: kernels, errors and measurements"
+ *              (flozi.net), Lektion 3: verify rows share K/V tiles, a causal
+ *              mask is applied per row, partial softmax statistics are merged.
+ *
+ * Readings where the pages are silent (each is listed in the design doc):
+ *   - query head h reads KV head h / (num_q_heads / num_kv_heads)  (contiguous GQA);
+ *   - seq_lens[b] counts every cached token of sequence b, including the q_len
+ *     rows just written; row r (0-based) of a q_len-row block sees keys
+ *     0 .. seq_lens[b] - q_len + r inclusive;
+ *   - plain softmax: no sliding window, ALiBi, sinks or soft-cap (the DCU page
+ *     lists those as excluded conditions, Sec.6);
+ *   - a row that sees no key returns zeros;
+ *   - a negative slot in reshape_and_cache is a padding slot and is skipped.
+ *
+ * Return codes: 0 ok, -1 bad argument, -2 an index (page, slot) out of range.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Exact widening of a bf16 bit pattern. */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* [DCU-832] Sec.1: logical_page = t // BLOCK_SIZE, page_offset = t % BLOCK_SIZE,
+ * physical_page = block_table[logical_page]; then the cache strides over
+ * (page, offset, kv_head, dim) of a [num_pages, BLOCK_SIZE, kv_heads, head_dim]
+ * tensor (Sec.4) give the element offset of the row.  Returns -1 when the
+ * table entry is outside [0, num_pages). */
+static int64_t row_offset(const int32_t *block_table_row, int64_t t, int block_size,
+                          int num_kv_heads, int head_dim, int kv_head, int64_t num_pages)
+{
+    int64_t logical_page = t / block_size;
+    int64_t page_offset = t % block_size;
+    int64_t physical_page = block_table_row[logical_page];
+    if (physical_page < 0 || physical_page >= num_pages)
+        return -1;
+    return ((physical_page * block_size + page_offset) * num_kv_heads + kv_head) * (int64_t)head_dim;
+}
+
+/* ------------------------------------------------------------------------ */
+/* reshape_and_cache: k_cache[s / BS, s % BS, h, :] = k_new[i, h, :] for the
+ * slot s = slot_mapping[i] of every new token i (same for V).  Bit copy. */
+int oracle_reshape_and_cache(const uint16_t *k_new, const uint16_t *v_new,
+                             uint16_t *k_cache, uint16_t *v_cache,
+                             const int64_t *slot_mapping, int64_t num_tokens,
+                             int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_pages)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_pages < 0)
+        return -1;
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0)
+            continue; /* padding slot */
+        if (s >= num_pages * block_size)
+            return -2;
+        int64_t page = s / block_size;
+        int64_t off = s % block_size;
+        int64_t dst = (page * block_size + off) * row;
+        memcpy(k_cache + dst, k_new + i * row, (size_t)row * sizeof(uint16_t));
+        memcpy(v_cache + dst, v_new + i * row, (size_t)row * sizeof(uint16_t));
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Problem description shared by the attention entry points. */
+typedef struct {
+    const uint16_t *q;          /* [num_seqs*q_len, num_q_heads, head_dim] bf16 bits */
+    const uint16_t *k_cache;    /* [num_pages, block_size, num_kv_heads, head_dim]  */
+    const uint16_t *v_cache;
+    const int32_t *block_table; /* [num_seqs, max_pages_per_seq] */
+    const int32_t *seq_lens;    /* [num_seqs] */
+    int num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_pages_per_seq;
+    int64_t num_pages;
+    double scale;
+} problem;
+
+/* Number of keys query row r of sequence b may attend to (causal rule). */
+static int64_t visible_keys(const problem *p, int b, int r)
+{
+    int64_t n = (int64_t)p->seq_lens[b] - p->q_len + r + 1;
+    return n < 0 ? 0 : n;
+}
+
+/* Softmax attention of one (row, query head) over keys [t_begin, t_end) of its
+ * sequence, clipped to the visible range.  Returns the normalised output o
+ * (head_dim doubles), the maximum logit m and the sum l of exp(s_t - m).
+ * An empty range gives o = 0, m = -inf, l = 0.  Scores are summed over d in
+ * index order and the softmax sums run over t in logical token order.
+ * scratch holds at least (t_end - t_begin) doubles. */
+static int attend_range(const problem *p, int64_t row, int h, int64_t t_begin, int64_t t_end,
+                        double *o, double *m_out, double *l_out, double *scratch)
+{
+    int D = p->head_dim;
+    int b = (int)(row / p->q_len);
+    int r = (int)(row % p->q_len);
+    int group = p->num_q_heads / p->num_kv_heads;
+    int kv_head = h / group;
+    const int32_t *bt = p->block_table + (int64_t)b * p->max_pages_per_seq;
+    const uint16_t *qv = p->q + (row * p->num_q_heads + h) * (int64_t)D;
+
+    int64_t n = visible_keys(p, b, r);
+    if (t_end > n)
+        t_end = n;
+    if (t_begin < 0)
+        t_begin = 0;
+    for (int d = 0; d < D; ++d)
+        o[d] = 0.0;
+    if (t_begin >= t_end) {
+        *m_out = -INFINITY;
+        *l_out = 0.0;
+        return 0;
+    }
+
+    /* scores s_t = scale * sum_d q_d k_{t,d}   ([DCU-832] Sec.5) */
+    double m = -INFINITY;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t off = row_offset(bt, t, p->block_size, p->num_kv_heads, D, kv_head, p->num_pages);
+        if (off < 0)
+            return -2;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += bf16_to_double(qv[d]) * bf16_to_double(p->k_cache[off + d]);
+        double s = p->scale * dot;
+        scratch[t - t_begin] = s;
+        if (s > m)
+            m = s;
+    }
+    /* max-subtracted exponentials, their sum, and the weighted sum of V rows */
+    double l = 0.0;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t off = row_offset(bt, t, p->block_size, p->num_kv_heads, D, kv_head, p->num_pages);
+        double w = exp(scratch[t - t_begin] - m);
+        l += w;
+        for (int d = 0; d < D; ++d)
+            o[d] += w * bf16_to_double(p->v_cache[off + d]);
+    }
+    for (int d = 0; d < D; ++d)
+        o[d] /= l;
+    *m_out = m;
+    *l_out = l;
+    return 0;
+}
+
+static int check_problem(const problem *p)
+{
+    if (!p->q || !p->k_cache || !p->v_cache || !p->block_table || !p->seq_lens)
+        return -1;
+    if (p->num_seqs < 0 || p->q_len <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
+        p->head_dim <= 0 || p->block_size <= 0 || p->max_pages_per_seq < 0 || p->num_pages < 0)
+        return -1;
+    if (p->num_q_heads % p->num_kv_heads != 0)
+        return -1;
+    for (int b = 0; b < p->num_seqs; ++b) {
+        int64_t L = p->seq_lens[b];
+        if (L < 0 || (L + p->block_size - 1) / p->block_size > p->max_pages_per_seq)
+            return -1;
+    }
+    return 0;
+}
+
+typedef struct {
+    const problem *p;
+    double *out;
+    int64_t first_item, item_stride, num_items;
+    int status;
+} worker_arg;
+
+static void *attention_worker(void *varg)
+{
+    worker_arg *a = (worker_arg *)varg;
+    const problem *p = a->p;
+    int64_t max_keys = 1;
+    for (int b = 0; b < p->num_seqs; ++b)
+        if (p->seq_lens[b] > max_keys)
+            max_keys = p->seq_lens[b];
+    double *scratch = (double *)malloc((size_t)max_keys * sizeof(double));
+    if (!scratch) {
+        a->status = -1;
+        return NULL;
+    }
+    a->status = 0;
+    for (int64_t item = a->first_item; item < a->num_items; item += a->item_stride) {
+        int64_t row = item / p->num_q_heads;
+        int h = (int)(item % p->num_q_heads);
+        double m, l;
+        double *o = a->out + item * p->head_dim; /* out[row, h, :] */
+        int rc = attend_range(p, row, h, 0, INT64_MAX, o, &m, &l, scratch);
+        if (rc != 0) {
+            a->status = rc;
+            break;
+        }
+    }
+    free(scratch);
+    return NULL;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Full paged attention: out[row, h, :] = sum_t softmax_t(scale q.K_t) V_t over
+ * the keys the row may see.  Rows are ordered (sequence, new-row), i.e. row =
+ * b * q_len + r.  q_len == 1 is plain decode; q_len > 1 is the verify variant.
+ * Work is spread over num_threads POSIX threads by (row, head) item. */
+int oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, int max_pages_per_seq,
+                           int64_t num_pages, double scale, double *out, int num_threads)
+{
+    problem p = {q, k_cache, v_cache, block_table, seq_lens, num_seqs, q_len, num_q_heads,
+                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale};
+    if (!out || check_problem(&p) != 0)
+        return -1;
+    if (num_threads < 1)
+        num_threads = 1;
+    int64_t num_items = (int64_t)num_seqs * q_len * num_q_heads;
+    if (num_threads > num_items)
+        num_threads = num_items > 0 ? (int)num_items : 1;
+
+    pthread_t *tids = (pthread_t *)calloc((size_t)num_threads, sizeof(pthread_t));
+    worker_arg *args = (worker_arg *)calloc((size_t)num_threads, sizeof(worker_arg));
+    if (!tids || !args) {
+        free(tids);
+        free(args);
+        return -1;
+    }
+    int rc = 0;
+    for (int i = 0; i < num_threads; ++i) {
+        args[i] = (worker_arg){&p, out, i, num_threads, num_items, 0};
+        if (num_threads == 1)
+            attention_worker(&args[i]);
+        else if (pthread_create(&tids[i], NULL, attention_worker, &args[i]) != 0)
+            rc = -1;
+    }
+    if (num_threads > 1)
+        for (int i = 0; i < num_threads; ++i)
+            pthread_join(tids[i], NULL);
+    for (int i = 0; i < num_threads && rc == 0; ++i)
+        rc = args[i].status;
+    free(tids);
+    free(args);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* One split of the method ([RADEON], split-KV fix): attention of one (row, head)
+ * restricted to keys [t_begin, t_end).  Gives the split's normalised output
+ * o (head_dim doubles), its max logit m and its exponential sum l. */
+int oracle_attention_partial(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                             const int32_t *block_table, const int32_t *seq_lens,
+                             int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                             int head_dim, int block_size, int max_pages_per_seq,
+                             int64_t num_pages, double scale, int64_t row, int head,
+                             int64_t t_begin, int64_t t_end, double *o, double *m, double *l)
+{
+    problem p = {q, k_cache, v_cache, block_table, seq_lens, num_seqs, q_len, num_q_heads,
+                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale};
+    if (!o || !m || !l || check_problem(&p) != 0)
+        return -1;
+    if (row < 0 || row >= (int64_t)num_seqs * q_len || head < 0 || head >= num_q_heads)
+        return -1;
+    int64_t span = t_end - t_begin;
+    double *scratch = (double *)malloc((size_t)(span > 1 ? span : 1) * sizeof(double));
+    if (!scratch)
+        return -1;
+    int rc = attend_range(&p, row, head, t_begin, t_end, o, m, l, scratch);
+    free(scratch);
+    return rc;
+}
+
+/* The reduce step of the split method: given n split results (o_i, m_i, l_i),
+ * M = max_i m_i, w_i = l_i exp(m_i - M), out = sum_i w_i o_i / sum_i w_i.
+ * Splits with l_i == 0 (no keys) carry no weight; if every split is empty the
+ * output is zero. */
+int oracle_lse_combine(const double *o_parts, const double *m_parts, const double *l_parts,
+                       int n, int head_dim, double *out)
+{
+    if (n < 0 || head_dim <= 0 || !out)
+        return -1;
+    double M = -INFINITY;
+    for (int i = 0; i < n; ++i)
+        if (l_parts[i] > 0.0 && m_parts[i] > M)
+            M = m_parts[i];
+    for (int d = 0; d < head_dim; ++d)
+        out[d] = 0.0;
+    if (M == -INFINITY)
+        return 0;
+    double wsum = 0.0;
+    for (int i = 0; i < n; ++i) {
+        if (l_parts[i] <= 0.0)
+            continue;
+        double w = l_parts[i] * exp(m_parts[i] - M);
+        wsum += w;
+        for (int d = 0; d < head_dim; ++d)
+            out[d] += w * o_parts[(int64_t)i * head_dim + d];
+    }
+    for (int d = 0; d < head_dim; ++d)
+        out[d] /= wsum;
+    return 0;
+}
