@@ -1,0 +1,421 @@
+"""Benchmark: paged-attention decode, µs per call and achieved KV-read HBM GB/s.
+
+Workload (one "step"): the decode step of the hybrid model's 16 full-attention
+layers -- per layer, reshape_and_cache of the new token's K/V, then split-KV
+paged-attention decode: batch 1, 24 query / 4 KV heads, head_dim 256, bf16
+N(0,1) data, context 32768, 784-token pages scattered at random through a
+pool 1.1x the context.  Every layer has its own 128 MiB cache (2 GiB per
+step, far larger than the 129 MB L2), so no L2 flush is needed between steps.
+
+`value` is whole-job KV-read GB/s (algorithmic bytes: 4096 B per context token
+per layer) with all inputs resident in HBM; the step runs as a CUDA graph and
+is timed with CUDA events on the launching stream.  `e2e` is the same metric
+through the Python binding with the step's inputs copied from pinned host
+memory and its outputs copied back inside the timed region.  `roofline`
+covers the decode kernel (main + reduce launch per layer call), timed with
+CUDA events around every layer call inside the timed region.
+
+`--impl reference` times the CPU fp64 oracle on the host cores instead (a
+bounded sample of the same workload) and prints the same line shape.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "hybrid_step_l32768_bs784_x16"
+METRIC = "paged-attn decode µs/call & achieved KV-read HBM GB/s vs context length"
+KV_BYTES_PER_TOKEN_LAYER = 4096  # 2 (K, V) x 4 KV heads x 256 dims x 2 bytes
+FALLBACK_HBM_GBS = 6800.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_attention_decode_split_gb300", "csrc")
+    for name in ("pa_device.cuh", "decode_split.cuh", "decode_launch.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """DRAM bytes per decode call from the committed ncu summary, if it was
+    taken on the current decode kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_l32768_bs784_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    return rec.get("dram_bytes_per_call")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.result = None
+        if self.proc is None:
+            return False
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return False
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        loaded = [v for v in sm if smax and v > 0.5 * max(smax)] or sm
+        self.result = {"sm_mhz": statistics.median(loaded) if loaded else None,
+                       "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+        return False
+
+
+def dist_setup(n_gpus):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(world, value: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------
+
+def _bits(t):
+    """bf16 tensor -> uint16 numpy bit patterns on the host (the oracle's input form)."""
+    import numpy as np
+    import torch
+    return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def run_oracle_sample(layers, block_table, seq_lens, scale, budget_s: float):
+    """Times the oracle over whole layers of the workload until about budget_s
+    seconds of CPU work; returns (seconds, layers, threads)."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    done, t_total = 0, 0.0
+    for q, kc, vc in layers:
+        t0 = time.perf_counter()
+        oracle.paged_attention(q, kc, vc, block_table, seq_lens, scale, num_threads=threads)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total >= budget_s:
+            break
+    return t_total, done, threads
+
+
+def bench_reference(args, world, rank):
+    """The oracle as the reference arm: one layer per step on the host cores."""
+    import torch
+    from paged_attention_decode_split_gb300.inputs import WORKLOADS, make_problem
+    if rank != 0:
+        return
+    spec = dict(WORKLOADS[WORKLOAD])
+    spec["num_layers"] = 1
+    prob = make_problem(1002, **spec)
+    layers = [(_bits(prob.q[0]), _bits(prob.k_cache[0]), _bits(prob.v_cache[0]))]
+    L = int(prob.seq_lens[0])
+    bytes_layer = L * KV_BYTES_PER_TOKEN_LAYER
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    times = []
+    t_start = time.perf_counter()
+    warm = min(args.warmup, 1)
+    for i in range(warm + args.steps):
+        q, kc, vc = layers[0]
+        t0 = time.perf_counter()
+        oracle.paged_attention(q, kc, vc, prob.block_table.numpy(), prob.seq_lens.numpy(), prob.scale,
+                               num_threads=threads)
+        dt = time.perf_counter() - t0
+        if i >= warm:
+            times.append(dt)
+        if time.perf_counter() - t_start > args.reference_budget and times:
+            break  # keep the reference arm within a few minutes
+    per_layer = sum(times) / len(times)
+    gbs = bytes_layer / per_layer / 1e9
+    sample = (f"one of the 16 layers per step (batch 1, 24 heads, context {L}, block 784), fp64 oracle; "
+              f"ms_per_step extrapolates x16 layers")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": len(times), "steps_requested": args.steps, "warmup": warm, "ms_per_step": per_layer * 16 * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers_timed_per_step": 1, "context": L, "batch": 1,
+                   "block_size": 784, "q_heads": 24, "kv_heads": 4, "head_dim": 256},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def bench_gpu(args, world, rank, local):
+    import torch
+    import paged_attention_decode_split_gb300 as pa
+    from paged_attention_decode_split_gb300 import _build
+    from paged_attention_decode_split_gb300.inputs import WORKLOADS, make_new_tokens, make_problem
+
+    _build.build()
+    pa.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    spec = dict(WORKLOADS[WORKLOAD])
+    prob = make_problem(1002 + rank, **spec, device="cuda")
+    n_layers = prob.num_layers
+    L = int(prob.seq_lens[0])
+    B = prob.num_seqs
+    bt = prob.block_table.to(dev)
+    sl = prob.seq_lens.to(dev)
+    desc = pa.make_desc(num_seqs=B, num_q_heads=24, num_kv_heads=4, head_dim=256, block_size=prob.block_size,
+                        max_pages_per_seq=prob.max_pages_per_seq, max_seq_len=L, num_pages=prob.num_pages,
+                        scale=prob.scale)
+    ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    k_new, v_new = make_new_tokens(77 + rank, n_layers * B, 4, 256, device="cuda")
+    k_new = k_new.view(n_layers, B, 4, 256)
+    v_new = v_new.view(n_layers, B, 4, 256)
+    slots = prob.new_token_slots().to(dev)
+    out = torch.empty((n_layers, B, 24, 256), dtype=torch.float32, device=dev)
+
+    def layer_call(l):
+        pa.reshape_and_cache(k_new[l], v_new[l], prob.k_cache[l], prob.v_cache[l], slots, status=status)
+        pa.paged_attention_decode(prob.q[l], prob.k_cache[l], prob.v_cache[l], bt, sl, desc, out[l], ws,
+                                  status=status)
+
+    stream = torch.cuda.Stream(device=dev)
+    # eager warm-up (sets kernel attributes, loads modules) outside any capture
+    with torch.cuda.stream(stream):
+        for l in range(n_layers):
+            layer_call(l)
+    torch.cuda.synchronize()
+    plan = pa.last_plan()
+
+    try:
+        ev_pairs = [(torch.cuda.Event(enable_timing=True, external=True),
+                     torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_layers)]
+    except TypeError:
+        ev_pairs = None
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for l in range(n_layers):
+            pa.reshape_and_cache(k_new[l], v_new[l], prob.k_cache[l], prob.v_cache[l], slots, status=status)
+            if ev_pairs:
+                ev_pairs[l][0].record()
+            pa.paged_attention_decode(prob.q[l], prob.k_cache[l], prob.v_cache[l], bt, sl, desc, out[l], ws,
+                                      status=status)
+            if ev_pairs:
+                ev_pairs[l][1].record()
+    torch.cuda.synchronize()
+    launches_per_step = n_layers * (2 + (1 if plan["reduce_launched"] else 0))
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
+    barrier(world)
+
+    step_events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        with torch.cuda.stream(stream):
+            step_events[0].record()
+            for k in range(args.steps):
+                graph.replay()
+                step_events[k + 1].record()
+        torch.cuda.synchronize()
+        barrier(world)
+    per_step_ms = [step_events[k].elapsed_time(step_events[k + 1]) for k in range(args.steps)]
+    total_ms = step_events[0].elapsed_time(step_events[-1])
+    total_ms = max_over_ranks(world, total_ms)
+    ms_per_step = total_ms / args.steps
+    if ev_pairs:
+        call_us = [a.elapsed_time(b) * 1e3 for a, b in ev_pairs]  # last timed step, every layer
+    else:
+        call_us = None
+
+    bytes_step = n_layers * B * L * KV_BYTES_PER_TOKEN_LAYER
+    value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    if call_us:
+        avg_call_us = sum(call_us) / len(call_us)
+    else:
+        avg_call_us = ms_per_step * 1e3 / n_layers
+    achieved = (B * L * KV_BYTES_PER_TOKEN_LAYER) / (avg_call_us * 1e-6) / 1e9
+    st = int(status.item())
+
+    # ---- end to end through the binding with host buffers ----
+    q_host = torch.stack([q for q in prob.q]).cpu().pin_memory()          # [16, B, 24, 256] bf16
+    kn_host = k_new.cpu().pin_memory()
+    vn_host = v_new.cpu().pin_memory()
+    slots_host = slots.cpu().pin_memory()
+    sl_host = prob.seq_lens.cpu().pin_memory()
+    bt_host = prob.block_table.cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_dev = torch.empty_like(q_host, device=dev)
+    kn_dev, vn_dev = torch.empty_like(kn_host, device=dev), torch.empty_like(vn_host, device=dev)
+    slots_dev, sl_dev, bt_dev = (torch.empty_like(slots_host, device=dev), torch.empty_like(sl_host, device=dev),
+                                 torch.empty_like(bt_host, device=dev))
+    h2d = sum(t.numel() * t.element_size() for t in (q_host, kn_host, vn_host, slots_host, sl_host, bt_host))
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for src, dst in ((q_host, q_dev), (kn_host, kn_dev), (vn_host, vn_dev), (slots_host, slots_dev),
+                         (sl_host, sl_dev), (bt_host, bt_dev)):
+            dst.copy_(src, non_blocking=True)
+        for l in range(n_layers):
+            pa.reshape_and_cache(kn_dev[l], vn_dev[l], prob.k_cache[l], prob.v_cache[l], slots_dev, status=status)
+            pa.paged_attention_decode(q_dev[l], prob.k_cache[l], prob.v_cache[l], bt_dev, sl_dev, desc, out[l],
+                                      ws, status=status)
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_steps = max(5, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+            torch.cuda.current_stream().synchronize()  # the result is on the host each step
+        e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(world, e2e_s)
+    e2e_value = world * bytes_step * e2e_steps / e2e_s / 1e9
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        layer_cpu = ((_bits(prob.q[l]), _bits(prob.k_cache[l]), _bits(prob.v_cache[l])) for l in range(n_layers))
+        secs, layers_done, threads = run_oracle_sample(layer_cpu, prob.block_table.numpy(),
+                                                       prob.seq_lens.numpy(), prob.scale, args.cpu_budget)
+        cpu = {"value": layers_done * B * L * KV_BYTES_PER_TOKEN_LAYER / secs / 1e9, "unit": "GB/s",
+               "cores": threads, "kind": "oracle",
+               "sample": f"{layers_done} of the 16 layers (all 24 heads, context {L}), fp64, "
+                         f"{secs:.1f} s on {threads} host threads"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "accum_dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": n_layers, "batch": B, "context": L, "block_size": prob.block_size,
+                   "q_heads": 24, "kv_heads": 4, "head_dim": 256, "num_pages_per_layer": prob.num_pages,
+                   "l2": "no flush: 16 distinct 128 MiB layer caches (2 GiB per step) exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world}", "plan": plan},
+        "us_per_call": ms_per_step * 1e3 / n_layers,
+        "us_per_context_token": ms_per_step * 1e3 / L,
+        "ms_per_step_range": [min(per_step_ms), statistics.median(per_step_ms), max(per_step_ms)],
+        "decode_call_us": {"mean": avg_call_us, "min": min(call_us) if call_us else None,
+                           "max": max(call_us) if call_us else None,
+                           "how": "CUDA events around each layer's decode call (split kernel + reduce) in the "
+                                  "last timed step" if call_us else "step time / layers"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": load_traffic(),
+                     "algorithmic_bytes_per_call": B * L * KV_BYTES_PER_TOKEN_LAYER},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "Python binding, eager calls, pinned host inputs copied in and outputs copied out every step"},
+        "gpu_launches": launches_per_step * args.steps,
+        "device_status": st,
+        "clocks": clocks.result,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget", type=float, default=60.0,
+                    help="wall seconds after which --impl reference stops taking steps")
+    args = ap.parse_args()
+    import torch  # noqa: F401
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            bench_reference(args, world, rank)
+        else:
+            bench_gpu(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

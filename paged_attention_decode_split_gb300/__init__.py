@@ -1,0 +1,169 @@
+"""Paged-attention split-KV decode for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libpagedattn.so`` (the C ABI of
+``include/pagedattn.h``).  It only marshals arguments: torch tensors supply
+device pointers and the current CUDA stream; every step of the computation runs
+in the library's CUDA kernels.  If the library is missing or cannot be loaded,
+every call raises -- there is no fallback.
+
+Names follow the C ABI: ``reshape_and_cache``, ``paged_attention_decode``,
+``paged_attention_verify``, ``workspace_bytes``, ``last_plan``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "AttnDesc", "PlanInfo", "PagedAttnError", "load_library", "make_desc", "workspace_bytes",
+    "reshape_and_cache", "paged_attention_decode", "paged_attention_verify", "last_plan",
+    "status_string", "PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_WORKSPACE",
+    "PA_ERR_CUDA", "PA_OUT_F32", "PA_OUT_BF16", "PA_DEV_BAD_SEQLEN", "PA_DEV_BAD_PAGE",
+    "PA_DEV_BAD_SLOT", "PA_DEV_TIMEOUT", "PA_PATH_DECODE_CUDA_CORE", "PA_PATH_VERIFY_MMA",
+    "PA_PATH_VERIFY_TCGEN05",
+]
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, 1, 2, 3, 4
+PA_OUT_F32, PA_OUT_BF16 = 0, 1
+PA_DEV_BAD_SEQLEN, PA_DEV_BAD_PAGE, PA_DEV_BAD_SLOT, PA_DEV_TIMEOUT = 1, 2, 4, 8
+PA_PATH_DECODE_CUDA_CORE, PA_PATH_VERIFY_MMA, PA_PATH_VERIFY_TCGEN05 = 1, 2, 3
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpagedattn.so")
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("max_pages_per_seq", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("num_pages", ctypes.c_int64),
+        ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("path_id", ctypes.c_int32), ("num_splits", ctypes.c_int32), ("chunks_per_split", ctypes.c_int32),
+        ("grid_ctas", ctypes.c_int32), ("block_size", ctypes.c_int32), ("reduce_launched", ctypes.c_int32),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def load_library(path: str | None = None):
+    """Load libpagedattn.so (built by ``_build.build()``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libpagedattn.so not found at {path}; build it with "
+                "`python -m paged_attention_decode_split_gb300._build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(path)
+        lib.pa_status_string.restype = ctypes.c_char_p
+        lib.pa_status_string.argtypes = [ctypes.c_int]
+        lib.pa_workspace_bytes.restype = ctypes.c_size_t
+        lib.pa_workspace_bytes.argtypes = [ctypes.POINTER(AttnDesc)]
+        lib.pa_last_plan.restype = ctypes.c_int
+        lib.pa_last_plan.argtypes = [ctypes.POINTER(PlanInfo)]
+        lib.pa_reshape_and_cache.restype = ctypes.c_int
+        lib.pa_reshape_and_cache.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _vp, _vp]
+        for name in ("pa_paged_attention_decode", "pa_paged_attention_verify"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc), _vp, _vp, ctypes.c_size_t, _vp, _vp]
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().pa_status_string(int(status)).decode()
+
+
+def make_desc(*, num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+              max_pages_per_seq: int, max_seq_len: int, num_pages: int, scale: float, q_len: int = 1,
+              out_dtype: int = PA_OUT_F32, num_splits: int = 0, num_sms: int = 0) -> AttnDesc:
+    return AttnDesc(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_pages_per_seq,
+                    max_seq_len, num_pages, scale, out_dtype, num_splits, num_sms)
+
+
+def workspace_bytes(desc: AttnDesc) -> int:
+    n = load_library().pa_workspace_bytes(ctypes.byref(desc))
+    if n == ctypes.c_size_t(-1).value:
+        raise PagedAttnError(PA_ERR_INVALID_ARG, "pa_workspace_bytes")
+    return int(n)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    assert t.is_contiguous(), "tensors passed to the library must be contiguous"
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PagedAttnError(status, what)
+
+
+def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, status=None, stream=None) -> None:
+    """Write new K/V rows ([N, Hkv, D] bf16) into cache slots (int64 [N])."""
+    num_pages, block_size, num_kv_heads, head_dim = k_cache.shape
+    rc = load_library().pa_reshape_and_cache(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), int(slot_mapping.shape[0]),
+        num_kv_heads, head_dim, block_size, num_pages, _ptr(status), _stream(stream))
+    _check(rc, "pa_reshape_and_cache")
+
+
+def paged_attention_decode(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, workspace=None,
+                           status=None, stream=None) -> None:
+    """out[b, h, :] = softmax(scale q K^T) V through the block table (q_len 1)."""
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().pa_paged_attention_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
+        _ptr(workspace), ws, _ptr(status), _stream(stream))
+    _check(rc, "pa_paged_attention_decode")
+
+
+def paged_attention_verify(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, workspace=None,
+                           status=None, stream=None) -> None:
+    """q_len > 1 rows per sequence, causal among them; q/out are [B*q_len, Hq, D]."""
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().pa_paged_attention_verify(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
+        _ptr(workspace), ws, _ptr(status), _stream(stream))
+    _check(rc, "pa_paged_attention_verify")
+
+
+def last_plan() -> dict:
+    info = PlanInfo()
+    _check(load_library().pa_last_plan(ctypes.byref(info)), "pa_last_plan")
+    return info.as_dict()

@@ -1,0 +1,28 @@
+// pa_internal.h -- host-side interfaces between the C-ABI layer and the
+// translation units that instantiate the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "decode_split.cuh"
+#include "verify_mma.cuh"
+
+namespace pa {
+
+// Kernel variants compiled into the library; returns false for (D, G) pairs
+// outside the set (the C ABI then answers PA_ERR_UNSUPPORTED).
+bool decode_supported(int head_dim, int group);
+bool verify_supported(int head_dim, int rows);  // rows = q_len * G
+
+// Launch helpers; they return the launch error (cudaSuccess if queued).
+cudaError_t launch_decode(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const DecodeParams &p, dim3 grid, cudaStream_t stream);
+cudaError_t launch_reduce(int head_dim, const ReduceParams &p, dim3 grid, cudaStream_t stream);
+cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const VerifyParams &p, dim3 grid, cudaStream_t stream);
+
+// Sets the dynamic shared-memory limit of `fn` once per device.
+cudaError_t ensure_smem_limit(const void *fn, int bytes, int slot);
+
+}  // namespace pa

@@ -1,0 +1,398 @@
+// pagedattn_api.cu -- the C ABI: argument validation, split planning, TMA
+// descriptors, and the reshape_and_cache kernel.
+//
+// Split planning follows the split-KV fix of "Hybrid SSM decode rate on dual
+// Radeon under vLLM": with one CTA per (sequence, KV head) a batch-1 decode of
+// a 4-KV-head model leaves most SMs idle, so each (sequence, KV head) context
+// is cut into S splits of whole 16-token chunks, enough that the grid
+// (S, Hkv, B) covers every SM; the partition reduce then merges the splits.
+// More splits cost more partial traffic and a longer reduce (the grid-versus-
+// partials trade-off that "Qwen3.8 on MI350P" spells out for split-K GEMMs),
+// so a split never drops below kMinChunksPerSplit chunks.  The plan depends
+// only on the description and the SM count, so it is deterministic.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pagedattn.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kMinChunksPerSplit = 2;   // 32 tokens
+constexpr int kMaxChunksPerSplit = 256; // 4096 tokens: bounds the longest CTA for load balance
+constexpr int kMaxDevices = 64;
+constexpr int kKernelSlots = 64;
+
+thread_local pa_plan_info g_last_plan;
+thread_local bool g_have_plan = false;
+
+struct Plan {
+    int num_sms;
+    int num_splits;
+    int chunks_per_split;
+    size_t ws_bytes;
+    size_t part_o_bytes;
+};
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sm_count(int *out) {
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) {
+        *out = cache[dev];
+        return 0;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return -1;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev] = n;
+    *out = n;
+    return 0;
+}
+
+// Validates a description; `verify` selects the q_len rule.
+pa_status check_desc(const pa_attn_desc *d, bool verify) {
+    if (!d) return PA_ERR_INVALID_ARG;
+    if (d->num_seqs < 0 || d->q_len < 1 || d->num_q_heads < 1 || d->num_kv_heads < 1 || d->head_dim < 1 ||
+        d->block_size < 1 || d->max_pages_per_seq < 0 || d->max_seq_len < 0 || d->num_pages < 1 ||
+        d->num_splits < 0 || d->num_sms < 0)
+        return PA_ERR_INVALID_ARG;
+    if (!verify && d->q_len != 1) return PA_ERR_INVALID_ARG;
+    if (d->num_q_heads % d->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (d->out_dtype != PA_OUT_F32 && d->out_dtype != PA_OUT_BF16) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(d->scale)) return PA_ERR_INVALID_ARG;
+    const int64_t need_pages = (static_cast<int64_t>(d->max_seq_len) + d->block_size - 1) / d->block_size;
+    if (need_pages > d->max_pages_per_seq) return PA_ERR_INVALID_ARG;
+    if (d->num_pages > INT32_MAX) return PA_ERR_UNSUPPORTED;  // TMA coordinates are 32-bit
+    // grid.z = num_seqs (split kernels), grid.y = num_seqs * q_len (reduce), grid.y = Hkv
+    if (static_cast<int64_t>(d->num_seqs) * d->q_len > 65535 || d->num_kv_heads > 65535)
+        return PA_ERR_UNSUPPORTED;
+    if (d->block_size % kChunk != 0) return PA_ERR_UNSUPPORTED;
+    const int group = d->num_q_heads / d->num_kv_heads;
+    if (verify) {
+        if (!verify_supported(d->head_dim, d->q_len * group)) return PA_ERR_UNSUPPORTED;
+    } else {
+        if (!decode_supported(d->head_dim, group)) return PA_ERR_UNSUPPORTED;
+    }
+    return PA_OK;
+}
+
+pa_status make_plan(const pa_attn_desc *d, bool verify, Plan *pl) {
+    pa_status st = check_desc(d, verify);
+    if (st != PA_OK) return st;
+    int sms = d->num_sms;
+    if (sms <= 0 && device_sm_count(&sms) != 0) return PA_ERR_CUDA;
+    const int n_chunks = (d->max_seq_len + kChunk - 1) / kChunk;
+    const int64_t units = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads;
+    int splits;
+    if (d->num_splits > 0) {
+        splits = d->num_splits;
+    } else if (units == 0 || n_chunks == 0) {
+        splits = 1;
+    } else {
+        splits = static_cast<int>((sms + units - 1) / units);  // enough CTAs to cover the SMs
+        splits = std::min(splits, std::max(1, n_chunks / kMinChunksPerSplit));
+        splits = std::max(splits, (n_chunks + kMaxChunksPerSplit - 1) / kMaxChunksPerSplit);
+    }
+    splits = std::max(1, std::min(splits, std::max(1, n_chunks)));
+    int cps = std::max(1, (n_chunks + splits - 1) / splits);
+    splits = std::max(1, (n_chunks + cps - 1) / cps);  // no trailing empty split for the longest sequence
+    pl->num_sms = sms;
+    pl->num_splits = splits;
+    pl->chunks_per_split = cps;
+    if (splits > 1) {
+        const size_t rows = static_cast<size_t>(d->num_seqs) * d->q_len * d->num_q_heads;
+        pl->part_o_bytes = (rows * splits * d->head_dim * sizeof(float) + 255) & ~size_t(255);
+        pl->ws_bytes = pl->part_o_bytes + rows * splits * sizeof(float2);
+    } else {
+        pl->part_o_bytes = 0;
+        pl->ws_bytes = 0;
+    }
+    return PA_OK;
+}
+
+// ---- TMA descriptors of a [P, BS, Hkv, D] bf16 cache ------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Box = [box_d elements of d, 1 head, 16 tokens, 1 page].
+bool encode_cache_map(CUtensorMap *map, const void *base, const pa_attn_desc *d, int box_d, bool swizzle128) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d->head_dim, (cuuint64_t)d->num_kv_heads, (cuuint64_t)d->block_size,
+                                (cuuint64_t)d->num_pages};
+    const cuuint64_t row = (cuuint64_t)d->head_dim * 2;
+    const cuuint64_t strides[3] = {row, row * d->num_kv_heads, row * d->num_kv_heads * d->block_size};
+    const cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)kChunk, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+void record_plan(int path, const Plan &pl, const pa_attn_desc *d, int ctas) {
+    g_last_plan.path_id = path;
+    g_last_plan.num_splits = pl.num_splits;
+    g_last_plan.chunks_per_split = pl.chunks_per_split;
+    g_last_plan.grid_ctas = ctas;
+    g_last_plan.block_size = d->block_size;
+    g_last_plan.reduce_launched = pl.num_splits > 1 ? 1 : 0;
+    g_have_plan = true;
+}
+
+pa_status check_common_ptrs(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                            const int32_t *seq_lens, const void *out) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+pa_status check_workspace(const Plan &pl, void *workspace, size_t ws_bytes) {
+    if (pl.ws_bytes == 0) return PA_OK;
+    if (!workspace || ws_bytes < pl.ws_bytes || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+    return PA_OK;
+}
+
+}  // namespace
+
+cudaError_t ensure_smem_limit(const void *fn, int bytes, int slot) {
+    static bool done[kMaxDevices][kKernelSlots] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kKernelSlots)
+        return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev][slot]) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[dev][slot] = true;
+    return e;
+}
+
+// ---- reshape_and_cache kernel ------------------------------------------------
+// One CTA per new token copies its [Hkv, D] rows of K and V into the slot's
+// cache row with 16-byte vector accesses.
+__global__ void __launch_bounds__(128) pa_reshape_and_cache_kernel(const uint4 *__restrict__ k_new,
+                                                                   const uint4 *__restrict__ v_new,
+                                                                   uint4 *__restrict__ k_cache,
+                                                                   uint4 *__restrict__ v_cache,
+                                                                   const int64_t *__restrict__ slots, int row_vecs,
+                                                                   int64_t num_slots, int32_t *status) {
+    const int i = blockIdx.x;
+    const int64_t s = slots[i];
+    if (s < 0) return;  // padding token
+    if (s >= num_slots) {
+        if (threadIdx.x == 0) set_status(status, PA_DEV_BAD_SLOT);
+        return;
+    }
+    const uint4 *ks = k_new + (size_t)i * row_vecs;
+    const uint4 *vs = v_new + (size_t)i * row_vecs;
+    uint4 *kd = k_cache + (size_t)s * row_vecs;
+    uint4 *vd = v_cache + (size_t)s * row_vecs;
+    for (int j = threadIdx.x; j < row_vecs; j += blockDim.x) {
+        kd[j] = ks[j];
+        vd[j] = vs[j];
+    }
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char *pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: invalid argument";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: shape outside the compiled kernels";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA call or launch failed";
+    }
+    return "unknown pa_status";
+}
+
+pa_status pa_last_plan(pa_plan_info *info) {
+    if (!info || !g_have_plan) return PA_ERR_INVALID_ARG;
+    *info = g_last_plan;
+    return PA_OK;
+}
+
+size_t pa_workspace_bytes(const pa_attn_desc *desc) {
+    Plan pl;
+    const bool verify = desc && desc->q_len > 1;
+    if (make_plan(desc, verify, &pl) != PA_OK) return static_cast<size_t>(-1);
+    return pl.ws_bytes;
+}
+
+pa_status pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                               const int64_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int64_t num_pages, int32_t *device_status,
+                               void *stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || num_pages < 1)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * 2;
+    if (row_bytes % 16 != 0 || row_bytes / 16 > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    pa_reshape_and_cache_kernel<<<num_tokens, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_cache),
+        static_cast<uint4 *>(v_cache), slot_mapping, static_cast<int>(row_bytes / 16), num_pages * block_size,
+        device_status);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_table, const int32_t *seq_lens, const pa_attn_desc *desc,
+                                    void *out, void *workspace, size_t workspace_bytes, int32_t *device_status,
+                                    void *stream) {
+    pa_status st = check_desc(desc, false);
+    if (st != PA_OK) return st;
+    if (desc->num_seqs == 0) return PA_OK;
+    st = check_common_ptrs(q, k_cache, v_cache, block_table, seq_lens, out);
+    if (st != PA_OK) return st;
+    Plan pl;
+    st = make_plan(desc, false, &pl);
+    if (st != PA_OK) return st;
+    st = check_workspace(pl, workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+
+    CUtensorMap tk, tv;
+    if (!encode_cache_map(&tk, k_cache, desc, desc->head_dim, false) ||
+        !encode_cache_map(&tv, v_cache, desc, desc->head_dim, false))
+        return PA_ERR_CUDA;
+
+    const int group = desc->num_q_heads / desc->num_kv_heads;
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
+    p.status = device_status;
+    p.num_pages = desc->num_pages;
+    p.num_q_heads = desc->num_q_heads;
+    p.max_pages_per_seq = desc->max_pages_per_seq;
+    p.max_seq_len = desc->max_seq_len;
+    p.block_size = desc->block_size;
+    p.chunks_per_split = pl.chunks_per_split;
+    p.num_splits = pl.num_splits;
+    p.scale_log2 = desc->scale * 1.4426950408889634f;
+    p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);
+    if (launch_decode(desc->head_dim, group, tk, tv, p, grid, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (pl.num_splits > 1) {
+        ReduceParams r;
+        r.part_o = p.part_o;
+        r.part_ml = p.part_ml;
+        r.seq_lens = seq_lens;
+        r.out = out;
+        r.num_q_heads = desc->num_q_heads;
+        r.q_len = 1;
+        r.max_seq_len = desc->max_seq_len;
+        r.chunks_per_split = pl.chunks_per_split;
+        r.num_splits = pl.num_splits;
+        r.out_bf16 = p.out_bf16;
+        if (launch_reduce(desc->head_dim, r, dim3(desc->num_q_heads, desc->num_seqs), s) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    record_plan(PA_PATH_DECODE_CUDA_CORE, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
+    return PA_OK;
+}
+
+pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_table, const int32_t *seq_lens, const pa_attn_desc *desc,
+                                    void *out, void *workspace, size_t workspace_bytes, int32_t *device_status,
+                                    void *stream) {
+    pa_status st = check_desc(desc, true);
+    if (st != PA_OK) return st;
+    if (desc->num_seqs == 0) return PA_OK;
+    st = check_common_ptrs(q, k_cache, v_cache, block_table, seq_lens, out);
+    if (st != PA_OK) return st;
+    Plan pl;
+    st = make_plan(desc, true, &pl);
+    if (st != PA_OK) return st;
+    st = check_workspace(pl, workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+
+    CUtensorMap tk, tv;
+    if (!encode_cache_map(&tk, k_cache, desc, 64, true) || !encode_cache_map(&tv, v_cache, desc, 64, true))
+        return PA_ERR_CUDA;
+
+    const int group = desc->num_q_heads / desc->num_kv_heads;
+    VerifyParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
+    p.status = device_status;
+    p.num_pages = desc->num_pages;
+    p.num_q_heads = desc->num_q_heads;
+    p.q_len = desc->q_len;
+    p.group = group;
+    p.max_pages_per_seq = desc->max_pages_per_seq;
+    p.max_seq_len = desc->max_seq_len;
+    p.block_size = desc->block_size;
+    p.chunks_per_split = pl.chunks_per_split;
+    p.num_splits = pl.num_splits;
+    p.scale_log2 = desc->scale * 1.4426950408889634f;
+    p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);
+    if (launch_verify(desc->head_dim, desc->q_len * group, tk, tv, p, grid, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (pl.num_splits > 1) {
+        ReduceParams r;
+        r.part_o = p.part_o;
+        r.part_ml = p.part_ml;
+        r.seq_lens = seq_lens;
+        r.out = out;
+        r.num_q_heads = desc->num_q_heads;
+        r.q_len = desc->q_len;
+        r.max_seq_len = desc->max_seq_len;
+        r.chunks_per_split = pl.chunks_per_split;
+        r.num_splits = pl.num_splits;
+        r.out_bf16 = p.out_bf16;
+        if (launch_reduce(desc->head_dim, r, dim3(desc->num_q_heads, desc->num_seqs * desc->q_len), s) !=
+            cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    record_plan(PA_PATH_VERIFY_MMA, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,131 @@
+"""Host-only checks of the C ABI: the library loads, exports what the header
+declares, plans deterministically, and rejects bad arguments before touching
+a GPU.  No test here launches a kernel or passes a pointer that could be
+dereferenced."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_attention_decode_split_gb300 as pa
+from paged_attention_decode_split_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pagedattn.h")
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(pa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_symbols_exported(lib):
+    names = declared_functions()
+    assert {"pa_reshape_and_cache", "pa_paged_attention_decode", "pa_paged_attention_verify",
+            "pa_workspace_bytes", "pa_status_string", "pa_last_plan"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in pagedattn.h but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert pa.status_string(code).startswith("PA_")
+    assert "unknown" in pa.status_string(99)
+
+
+def hybrid_desc(**kw):
+    base = dict(num_seqs=1, num_q_heads=24, num_kv_heads=4, head_dim=256, block_size=784,
+                max_pages_per_seq=42, max_seq_len=32768, num_pages=46, scale=1 / 16, num_sms=152)
+    base.update(kw)
+    return pa.make_desc(**base)
+
+
+def test_workspace_plan_hybrid_32k(lib):
+    # 2048 chunks of 16 tokens, 4 (seq, kv-head) units, 152 SMs -> 38 splits of 54 chunks
+    ws = pa.workspace_bytes(hybrid_desc())
+    splits, rows = 38, 24
+    part_o = (rows * splits * 256 * 4 + 255) // 256 * 256
+    assert ws == part_o + rows * splits * 8
+
+
+def test_workspace_plan_rules(lib):
+    assert pa.workspace_bytes(hybrid_desc(num_splits=1)) == 0
+    assert pa.workspace_bytes(hybrid_desc(num_splits=5)) == 24 * 5 * 256 * 4 + 24 * 5 * 8
+    # a 512-token context never splits below 2 chunks per split
+    small = hybrid_desc(block_size=16, max_pages_per_seq=32, max_seq_len=512, num_pages=64)
+    assert pa.workspace_bytes(small) == 24 * 16 * 256 * 4 + 24 * 16 * 8
+    # the plan depends only on the description
+    assert pa.workspace_bytes(hybrid_desc()) == pa.workspace_bytes(hybrid_desc())
+    # empty context / empty batch: nothing to split
+    assert pa.workspace_bytes(hybrid_desc(max_seq_len=0)) == 0
+    assert pa.workspace_bytes(hybrid_desc(num_seqs=0)) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_q_heads=25), pa.PA_ERR_INVALID_ARG),       # Hq % Hkv != 0
+    (dict(head_dim=64), pa.PA_ERR_UNSUPPORTED),
+    (dict(block_size=20, max_pages_per_seq=2000), pa.PA_ERR_UNSUPPORTED),  # not a multiple of 16
+    (dict(block_size=0), pa.PA_ERR_INVALID_ARG),
+    (dict(max_pages_per_seq=10), pa.PA_ERR_INVALID_ARG),   # table too narrow for max_seq_len
+    (dict(num_pages=0), pa.PA_ERR_INVALID_ARG),
+    (dict(num_seqs=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(out_dtype=7), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), pa.PA_ERR_INVALID_ARG),
+    (dict(q_len=2), pa.PA_ERR_INVALID_ARG),              # decode takes one row per sequence
+    (dict(num_q_heads=40, num_kv_heads=4), pa.PA_ERR_UNSUPPORTED),  # G = 10 not compiled
+])
+def test_decode_rejects_bad_descriptions(lib, kw, code):
+    desc = hybrid_desc(**kw)
+    rc = lib.pa_paged_attention_decode(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(desc), FAKE, FAKE, 1 << 30,
+                                       None, None)
+    assert rc == code
+
+
+def test_decode_rejects_bad_pointers_and_workspace(lib):
+    desc = hybrid_desc()
+    call = lib.pa_paged_attention_decode
+    assert call(None, FAKE, FAKE, FAKE, FAKE, ctypes.byref(desc), FAKE, FAKE, 1 << 30, None, None) == pa.PA_ERR_INVALID_ARG
+    assert call(FAKE + 8, FAKE, FAKE, FAKE, FAKE, ctypes.byref(desc), FAKE, FAKE, 1 << 30, None, None) == pa.PA_ERR_INVALID_ARG
+    assert call(FAKE, FAKE, FAKE, FAKE + 2, FAKE, ctypes.byref(desc), FAKE, FAKE, 1 << 30, None, None) == pa.PA_ERR_INVALID_ARG
+    need = pa.workspace_bytes(desc)
+    assert call(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(desc), FAKE, FAKE, need - 1, None, None) == pa.PA_ERR_WORKSPACE
+    assert call(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(desc), FAKE, None, need, None, None) == pa.PA_ERR_WORKSPACE
+    assert call(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, need, None, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_noop(lib):
+    desc = hybrid_desc(num_seqs=0)
+    assert lib.pa_paged_attention_decode(None, None, None, None, None, ctypes.byref(desc), None, None, 0,
+                                         None, None) == pa.PA_OK
+
+
+def test_verify_rejects_bad_descriptions(lib):
+    call = lib.pa_paged_attention_verify
+    too_many_rows = hybrid_desc(q_len=32)  # 32 * 6 = 192 rows > 128
+    assert call(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(too_many_rows), FAKE, FAKE, 1 << 30, None,
+                None) == pa.PA_ERR_UNSUPPORTED
+    bad_dim = hybrid_desc(q_len=16, head_dim=96)
+    assert call(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(bad_dim), FAKE, FAKE, 1 << 30, None,
+                None) == pa.PA_ERR_UNSUPPORTED
+
+
+def test_reshape_and_cache_rejects_bad_arguments(lib):
+    call = lib.pa_reshape_and_cache
+    assert call(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 256, 16, 10, None, None) == pa.PA_ERR_INVALID_ARG
+    assert call(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 0, 256, 16, 10, None, None) == pa.PA_ERR_INVALID_ARG
+    assert call(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 4, 16, 10, None, None) == pa.PA_ERR_UNSUPPORTED  # 8-byte rows
+    assert call(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 1, 4, 256, 16, 10, None, None) == pa.PA_ERR_INVALID_ARG
+    assert call(None, None, None, None, None, 0, 4, 256, 16, 10, None, None) == pa.PA_OK  # nothing to copy
+
+
+def test_last_plan_before_any_call(lib):
+    info = pa.PlanInfo()
+    # this process has made no successful attention call on this thread
+    assert lib.pa_last_plan(ctypes.byref(info)) == pa.PA_ERR_INVALID_ARG

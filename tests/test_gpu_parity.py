@@ -1,0 +1,276 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU fp64 oracle.
+
+Small problems are compared element by element; the full-size workloads run
+in the launch configuration the benchmark times (automatic split plan) and
+are compared on whole layers or sampled sequences.  Edge cases: ragged tails
+around every chunk/page boundary, empty sequences, NaN-poisoned unused cache
+slots, forced split counts, bad device inputs, bf16 output, graph capture.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import paged_attention_decode_split_gb300 as pa
+from paged_attention_decode_split_gb300 import _build
+from paged_attention_decode_split_gb300.inputs import WORKLOADS, make_new_tokens, make_problem, sweep_workload
+from tests.gpu_common import (REL_L2_DECODE, REL_L2_VERIFY, assert_parity, oracle_out, run_attention, to_dev)
+from tests.helpers import bits
+
+pytestmark = pytest.mark.gpu
+
+TAIL_LENGTHS = [1, 15, 16, 17, 63, 64, 65, 783, 784, 785, 831, 832, 833]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _build.build()
+    pa.load_library()
+
+
+def hybrid(seed, lens, bs, **kw):
+    args = dict(num_seqs=len(lens), seq_lens=list(lens), num_q_heads=24, num_kv_heads=4, head_dim=256,
+                block_size=bs, scale=1 / 16)
+    args.update(kw)
+    return make_problem(seed, **args)
+
+
+# -- decode ------------------------------------------------------------------------
+
+def test_decode_l512_bs16_workload(oracle_mod):
+    prob = make_problem(1001, **WORKLOADS["decode_l512_bs16"])
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_DECODE_CUDA_CORE
+    assert_parity(out, oracle_out(oracle_mod, prob), what="512-token decode")
+
+
+@pytest.mark.parametrize("bs", [16, 784, 832])
+def test_decode_ragged_tails_nan_poisoned(oracle_mod, bs):
+    prob = hybrid(7 + bs, TAIL_LENGTHS, bs, poison_unused=True)
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"tails bs={bs}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
+def test_decode_forced_split_counts(oracle_mod, splits):
+    prob = hybrid(21, [5000, 333, 1], 784, poison_unused=True)
+    out, status, plan = run_attention(prob, num_splits=splits)
+    assert status == 0
+    assert plan["num_splits"] == min(splits, math.ceil(5000 / 16))
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"splits={splits}")
+
+
+@pytest.mark.parametrize("G,hkv", [(1, 4), (2, 4), (4, 2), (6, 4)])
+def test_decode_group_sizes_d256(oracle_mod, G, hkv):
+    prob = hybrid(31 + G, [700, 1500], 16, num_q_heads=G * hkv, num_kv_heads=hkv)
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"G={G}")
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 6, 8])
+def test_decode_dense_control_d128(oracle_mod, G):
+    prob = make_problem(41 + G, num_seqs=3, seq_lens=[1, 100, 2049], num_q_heads=8 * G, num_kv_heads=8,
+                        head_dim=128, block_size=16, scale=1 / math.sqrt(128), poison_unused=True)
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"dense G={G}")
+
+
+def test_decode_empty_sequences_give_zero(oracle_mod):
+    prob = hybrid(51, [0, 100, 0], 16)
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+    assert_parity(out, oracle_out(oracle_mod, prob), what="empty")
+
+
+def test_decode_bf16_output(oracle_mod):
+    prob = hybrid(61, [3000, 17], 832)
+    out, status, _ = run_attention(prob, out_dtype=pa.PA_OUT_BF16)
+    ref = oracle_out(oracle_mod, prob)
+    ref_bf16 = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    err = np.abs(out.double().numpy() - ref_bf16)
+    # one bf16 rounding on each side of a <= 2e-3 difference
+    assert status == 0 and err.max() <= 2e-3 + 2 * 2.0 ** -8 * np.abs(ref).max()
+
+
+def test_decode_deterministic_and_page_size_invariant(oracle_mod):
+    """Same tokens, same split plan: results are bitwise identical run to run
+    and across 16-, 784- and 832-token pages (chunks never straddle pages)."""
+    lens = [4000, 1234]
+    outs = []
+    base = hybrid(71, lens, 16)
+    for bs in (16, 784, 832):
+        prob = hybrid(72, lens, bs)
+        # copy the logical K/V of `base` into this paging
+        for b, L in enumerate(lens):
+            for t in range(0, L, 16):
+                n = min(16, L - t)
+                src_p, src_o = int(base.block_table[b, t // 16]), t % 16
+                dst_p, dst_o = int(prob.block_table[b, t // bs]), t % bs
+                prob.k_cache[0][dst_p, dst_o:dst_o + n] = base.k_cache[0][src_p, src_o:src_o + n]
+                prob.v_cache[0][dst_p, dst_o:dst_o + n] = base.v_cache[0][src_p, src_o:src_o + n]
+        prob.q[0] = base.q[0].clone()
+        o1, _, _ = run_attention(prob, num_splits=5)
+        o2, _, _ = run_attention(prob, num_splits=5)
+        assert torch.equal(o1, o2)
+        outs.append(o1)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert_parity(outs[0], oracle_out(oracle_mod, base), what="paging invariance")
+
+
+def test_decode_bad_seq_len_sets_status_and_zeroes(oracle_mod):
+    prob = hybrid(81, [300, 200], 16)
+    q, kc, vc, bt, sl = to_dev(prob)
+    sl[1] = 10_000  # beyond max_seq_len (300)
+    out, status, _ = run_attention(prob, tensors=(q, kc, vc, bt, sl), max_seq_len=300)
+    assert status & pa.PA_DEV_BAD_SEQLEN
+    assert torch.all(out[1] == 0)
+    ref = oracle_out(oracle_mod, prob, rows=[0])
+    assert_parity(out[:1], ref, what="good row next to a bad one")
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_decode_bad_page_sets_status_and_zeroes(oracle_mod, splits):
+    prob = hybrid(91, [900, 900], 16)
+    q, kc, vc, bt, sl = to_dev(prob)
+    bt[1, 20] = prob.num_pages + 5  # out of range: read as zeros by the copy engine, flagged
+    out, status, _ = run_attention(prob, tensors=(q, kc, vc, bt, sl), num_splits=splits)
+    assert status & pa.PA_DEV_BAD_PAGE
+    assert torch.all(out[1] == 0)
+    assert_parity(out[:1], oracle_out(oracle_mod, prob, rows=[0]), what="good row next to a bad page")
+
+
+def test_decode_cuda_graph_replay_matches_eager():
+    prob = hybrid(101, [2500], 784)
+    q, kc, vc, bt, sl = to_dev(prob)
+    eager, _, _ = run_attention(prob, tensors=(q, kc, vc, bt, sl))
+    from tests.gpu_common import desc_for
+    desc = desc_for(prob)
+    ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device="cuda")
+    out = torch.zeros((1, 24, 256), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pa.paged_attention_decode(q, kc, vc, bt, sl, desc, out, ws)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.paged_attention_decode(q, kc, vc, bt, sl, desc, out, ws)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), eager)
+
+
+# -- full-size workloads, benchmark launch configuration -------------------------
+
+def test_hybrid_step_l32768_bs784_x16_layers(oracle_mod):
+    spec = dict(WORKLOADS["hybrid_step_l32768_bs784_x16"])
+    prob = make_problem(1002, **spec)
+    for layer in (0, 15):
+        out, status, plan = run_attention(prob, layer)
+        assert status == 0 and plan["num_splits"] > 1
+        assert_parity(out, oracle_out(oracle_mod, prob, layer), what=f"32K layer {layer}")
+
+
+@pytest.mark.parametrize("depth", [500, 4096, 32768])
+@pytest.mark.parametrize("dense", [False, True])
+def test_context_sweep_depths(oracle_mod, depth, dense):
+    prob = make_problem(1003 + depth + dense, **sweep_workload(depth, dense, num_layers=1))
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"sweep depth={depth} dense={dense}")
+
+
+def test_batch32_uniform_bs784_sampled(oracle_mod):
+    prob = make_problem(1004, **WORKLOADS["batch32_uniform_bs784"], device="cuda")
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    rows = [0, 5, 11, 17, 26, 31]
+    ref = oracle_out(oracle_mod, prob, rows=rows)
+    assert_parity(out[rows], ref, what="batch 32 sampled sequences")
+
+
+# -- verify ----------------------------------------------------------------------
+
+def write_new_rows(prob, seed):
+    """reshape_and_cache of the q_len newest tokens of every sequence (GPU)."""
+    k_new, v_new = make_new_tokens(seed, prob.num_seqs * prob.q_len, prob.num_kv_heads, prob.head_dim)
+    slots = prob.new_token_slots()
+    kc, vc = prob.k_cache[0].cuda(), prob.v_cache[0].cuda()
+    pa.reshape_and_cache(k_new.cuda(), v_new.cuda(), kc, vc, slots.cuda())
+    torch.cuda.synchronize()
+    prob.k_cache[0], prob.v_cache[0] = kc.cpu(), vc.cpu()
+
+
+@pytest.mark.parametrize("q_len,lens,bs", [(2, [2, 33, 900], 16), (5, [5, 64, 785], 784),
+                                           (16, [16, 17, 831, 1700], 832), (16, [3000], 16)])
+def test_verify_small(oracle_mod, q_len, lens, bs):
+    prob = hybrid(111 + q_len, lens, bs, q_len=q_len, poison_unused=True)
+    write_new_rows(prob, 5)
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] in (pa.PA_PATH_VERIFY_MMA, pa.PA_PATH_VERIFY_TCGEN05)
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"verify q_len={q_len}")
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_verify_dense_shape_d128(oracle_mod, splits):
+    prob = make_problem(121, num_seqs=2, seq_lens=[300, 77], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, q_len=8, scale=1 / math.sqrt(128))
+    out, status, _ = run_attention(prob, num_splits=splits)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what="verify d128")
+
+
+def test_verify_short_context_sets_status():
+    prob = hybrid(131, [40, 40], 16, q_len=16)
+    q, kc, vc, bt, sl = to_dev(prob)
+    sl[0] = 10  # fewer cached tokens than new rows
+    out, status, _ = run_attention(prob, tensors=(q, kc, vc, bt, sl))
+    assert status & pa.PA_DEV_BAD_SEQLEN
+    assert torch.all(out[:16] == 0) and torch.all(torch.isfinite(out))
+
+
+def test_verify_b8_q16_l8192_bs832_workload(oracle_mod):
+    prob = make_problem(1005, **WORKLOADS["verify_b8_q16_l8192_bs832"])
+    write_new_rows(prob, 9)
+    out, status, plan = run_attention(prob)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what="verify workload")
+
+
+# -- reshape_and_cache ----------------------------------------------------------------
+
+def test_reshape_and_cache_bit_exact(oracle_mod):
+    gen = torch.Generator().manual_seed(3)
+    P, bs, hkv, d = 8, 784, 4, 256
+    kc = torch.randn((P, bs, hkv, d), generator=gen).to(torch.bfloat16)
+    vc = torch.randn((P, bs, hkv, d), generator=gen).to(torch.bfloat16)
+    n = 300
+    k_new, v_new = make_new_tokens(4, n, hkv, d)
+    slots = torch.randperm(P * bs, generator=gen)[:n].to(torch.int64)
+    slots[::17] = -1  # padding tokens
+    kd, vd = kc.cuda(), vc.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.reshape_and_cache(k_new.cuda(), v_new.cuda(), kd, vd, slots.cuda(), status=status)
+    torch.cuda.synchronize()
+    k_ref, v_ref = bits(kc).copy(), bits(vc).copy()
+    oracle_mod.reshape_and_cache(bits(k_new), bits(v_new), k_ref, v_ref, slots.numpy())
+    assert status.item() == 0
+    assert np.array_equal(bits(kd), k_ref) and np.array_equal(bits(vd), v_ref)
+
+
+def test_reshape_and_cache_bad_slot_flagged():
+    kc = torch.zeros((2, 16, 4, 256), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    k_new, v_new = make_new_tokens(5, 2, 4, 256)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.reshape_and_cache(k_new.cuda(), v_new.cuda(), kc, vc, torch.tensor([3, 32], device="cuda"), status=status)
+    torch.cuda.synchronize()
+    assert status.item() & pa.PA_DEV_BAD_SLOT
+    assert torch.equal(kc[0, 3].cpu(), k_new[0]) and torch.count_nonzero(kc[1]) == 0
