@@ -11,7 +11,7 @@
 //
 // This is the mma.sync (m16n8k16, bf16 in, fp32 accumulate) version: one
 // consumer warp per 16-row slice, S = Q K^T and O += P V per 16-token chunk,
-// with P rounded to bf16 as the A operand of the second product.  K and V
+// with P carried as a bf16 head plus a bf16 residual in the second product.  K and V
 // chunks arrive by TMA with the 128-byte swizzle so ldmatrix reads are free
 // of bank conflicts.
 #pragma once
@@ -86,6 +86,13 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// x = head + residual with both parts in bf16 (packed pairs for elements a, b).
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t &head, uint32_t &resid) {
+    head = pack_bf16(a, b);
+    const float ha = __uint_as_float(head << 16), hb = __uint_as_float(head & 0xffff0000u);
+    resid = pack_bf16(a - ha, b - hb);
 }
 
 template <int D, int NWC, int NS>
@@ -279,11 +286,14 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1)
             o[j][2] *= al_hi;
             o[j][3] *= al_hi;
         }
-        // P (bf16) as the A operand: the two S n-tiles are exactly one k=16 slice
-        const uint32_t pa0 = pack_bf16(sacc[0][0], sacc[0][1]);
-        const uint32_t pa1 = pack_bf16(sacc[0][2], sacc[0][3]);
-        const uint32_t pa2 = pack_bf16(sacc[1][0], sacc[1][1]);
-        const uint32_t pa3 = pack_bf16(sacc[1][2], sacc[1][3]);
+        // P as the A operand: the two S n-tiles are exactly one k=16 slice.  P is
+        // split into a bf16 head and a bf16 residual (two products), so the
+        // probabilities keep about 16 significant bits instead of bf16's 8.
+        uint32_t ph[4], pl[4];
+        split_bf16(sacc[0][0], sacc[0][1], ph[0], pl[0]);
+        split_bf16(sacc[0][2], sacc[0][3], ph[1], pl[1]);
+        split_bf16(sacc[1][0], sacc[1][1], ph[2], pl[2]);
+        split_bf16(sacc[1][2], sacc[1][3], ph[3], pl[3]);
         // rows of V past the end of the sequence may hold anything (NaN):
         // zero them in the B fragments of the last, partial chunk
         const int nv = min(kChunk, L - t0);
@@ -302,8 +312,10 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1)
                 b1 &= m1;
                 b3 &= m1;
             }
-            mma_bf16(o[2 * jj], pa0, pa1, pa2, pa3, b0, b1);
-            mma_bf16(o[2 * jj + 1], pa0, pa1, pa2, pa3, b2, b3);
+            mma_bf16(o[2 * jj], ph[0], ph[1], ph[2], ph[3], b0, b1);
+            mma_bf16(o[2 * jj + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+            mma_bf16(o[2 * jj], pl[0], pl[1], pl[2], pl[3], b0, b1);
+            mma_bf16(o[2 * jj + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);

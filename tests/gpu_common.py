@@ -5,9 +5,9 @@ The parity gate (the stated tolerance for bf16 inputs with fp32 accumulation):
   * max |gpu - oracle| <= 2e-3 over all elements;
   * |gpu - oracle| / |oracle| <= 1e-2 wherever |oracle| >= 0.2 (= 2e-3 / 1e-2,
     the magnitude above which the relative bound is the tighter one);
-  * relative L2 error per (row, head) <= ``rel_l2`` (a tighter internal target:
-    1e-4 for the fp32 CUDA-core decode, 5e-3 for the tensor-core verify whose
-    probabilities are rounded to bf16 before the P.V product).
+  * relative L2 error per (row, head) <= ``rel_l2`` = 1e-4, a tighter internal
+    target (fp32 accumulation; the verify kernel carries P as a bf16 head plus
+    a bf16 residual into its tensor-core P.V product).
 A row whose oracle output is exactly zero (no visible key) must be exactly zero.
 """
 from __future__ import annotations
@@ -20,7 +20,7 @@ import paged_attention_decode_split_gb300 as pa
 ATOL = 2e-3
 RTOL = 1e-2
 REL_L2_DECODE = 1e-4
-REL_L2_VERIFY = 5e-3
+REL_L2_VERIFY = 1e-4
 
 
 def to_dev(prob, layer=0, device="cuda"):

@@ -60,7 +60,9 @@ def test_decode_forced_split_counts(oracle_mod, splits):
     prob = hybrid(21, [5000, 333, 1], 784, poison_unused=True)
     out, status, plan = run_attention(prob, num_splits=splits)
     assert status == 0
-    assert plan["num_splits"] == min(splits, math.ceil(5000 / 16))
+    n_chunks = math.ceil(5000 / 16)
+    per_split = math.ceil(n_chunks / min(splits, n_chunks))
+    assert plan["num_splits"] == math.ceil(n_chunks / per_split)  # no empty trailing split
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"splits={splits}")
 
 
