@@ -7,23 +7,27 @@ namespace pa {
 
 namespace {
 
-constexpr int kDecodeWarps = 7;  // consumer warps per CTA (+1 producer warp): 8 warps keep the 255-register budget
-
-template <int D>
-constexpr int decode_stages() {
-    return D == 256 ? 12 : 16;  // 12 x 16 KiB or 16 x 8 KiB of K/V in flight per CTA
-}
-
-template <int D, int G>
+template <int D, int G, int HS, int NST, int SPS>
 cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, dim3 grid,
                             cudaStream_t stream, int slot) {
-    constexpr int NS = decode_stages<D>();
-    using C = DecodeCfg<D, G, kDecodeWarps, NS>;
-    auto kern = pa_decode_split_kernel<D, G, kDecodeWarps, NS>;
+    using C = DecodeCfg<D, G, HS, NST, SPS>;
+    auto kern = pa_decode_split_kernel<D, G, HS, NST, SPS>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the kernel's set-up overlaps the previous
+    // kernel in the stream (e.g. reshape_and_cache); it waits for that kernel
+    // before touching global memory.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace
@@ -34,22 +38,27 @@ bool decode_supported(int head_dim, int group) {
     return false;
 }
 
+// Per (head_dim, group): warps per chunk (HS), chunk streams (NST), stages per
+// stream (SPS).  D = 256: 6 streams x 2 stages x 16 KiB; groups of 4 and 6
+// heads are split over 2 warps per chunk, giving 13 warps per CTA at up to
+// 128 registers per thread (more warps to hide latency).  D = 128: 12
+// streams x 2 x 8 KiB, or 6 streams x 4 with the heads split over 2 warps.
 cudaError_t launch_decode(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                           const DecodeParams &p, dim3 grid, cudaStream_t stream) {
     if (head_dim == 256) {
         switch (group) {
-            case 1: return launch_decode_t<256, 1>(tk, tv, p, grid, stream, 0);
-            case 2: return launch_decode_t<256, 2>(tk, tv, p, grid, stream, 1);
-            case 4: return launch_decode_t<256, 4>(tk, tv, p, grid, stream, 2);
-            case 6: return launch_decode_t<256, 6>(tk, tv, p, grid, stream, 3);
+            case 1: return launch_decode_t<256, 1, 1, 6, 2>(tk, tv, p, grid, stream, 0);
+            case 2: return launch_decode_t<256, 2, 1, 6, 2>(tk, tv, p, grid, stream, 1);
+            case 4: return launch_decode_t<256, 4, 2, 6, 2>(tk, tv, p, grid, stream, 2);
+            case 6: return launch_decode_t<256, 6, 2, 6, 2>(tk, tv, p, grid, stream, 3);
         }
     } else if (head_dim == 128) {
         switch (group) {
-            case 1: return launch_decode_t<128, 1>(tk, tv, p, grid, stream, 4);
-            case 2: return launch_decode_t<128, 2>(tk, tv, p, grid, stream, 5);
-            case 4: return launch_decode_t<128, 4>(tk, tv, p, grid, stream, 6);
-            case 6: return launch_decode_t<128, 6>(tk, tv, p, grid, stream, 7);
-            case 8: return launch_decode_t<128, 8>(tk, tv, p, grid, stream, 8);
+            case 1: return launch_decode_t<128, 1, 1, 12, 2>(tk, tv, p, grid, stream, 4);
+            case 2: return launch_decode_t<128, 2, 1, 12, 2>(tk, tv, p, grid, stream, 5);
+            case 4: return launch_decode_t<128, 4, 1, 12, 2>(tk, tv, p, grid, stream, 6);
+            case 6: return launch_decode_t<128, 6, 2, 6, 4>(tk, tv, p, grid, stream, 7);
+            case 8: return launch_decode_t<128, 8, 2, 6, 4>(tk, tv, p, grid, stream, 8);
         }
     }
     return cudaErrorInvalidValue;
@@ -58,7 +67,7 @@ cudaError_t launch_decode(int head_dim, int group, const CUtensorMap &tk, const 
 cudaError_t launch_reduce(int head_dim, const ReduceParams &p, dim3 grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

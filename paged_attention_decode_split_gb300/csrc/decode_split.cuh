@@ -15,20 +15,23 @@
 //    [pages, BS, Hkv, D] cache.  16 divides 784 = 49 x 16, 832 and 16, so a
 //    chunk never straddles a page and the 16-token tail of a 784-token page
 //    (784 = 12 x 64 + 16) is just the 49th chunk of the page: no masks inside
-//    a page, and the block table is read once per page in chunk order
-//    (the page-contiguous walk of Sec.7).  Only the last chunk of a sequence
+//    a page, and the split's block-table entries are staged in shared memory
+//    once (the page-contiguous walk of Sec.7 reads the table once per page).  Only the last chunk of a sequence
 //    can be partial; its rows past the end are masked (scores) and skipped (PV).
-//  * One producer warp issues the copies into an NS-stage mbarrier ring; NW
-//    consumer warps take chunks round-robin, each with its own online softmax.
-//  * Each K/V row is read from shared memory once and used by all G query
-//    heads of the group (GQA reuse).  A lane owns E = D/32 consecutive
+//  * One producer lane issues the copies into NS stages; NST chunk streams
+//    take chunks round-robin, each with its own online softmax and its own
+//    SPS stages, refilled as soon as the stream frees one.  A chunk is shared
+//    by HS warps that split the G heads of the group among them.
+//  * A K/V row is read from shared memory once per warp and used by all of
+//    that warp's query heads (GQA reuse).  A lane owns E = D/32 consecutive
 //    elements of d: q (pre-scaled to log2 units) and the output accumulator
-//    for its G heads stay in registers.
-//  * Scores: per micro-batch of 8 tokens a lane forms 8 x G partial dot
+//    for its heads stay in registers.  Arithmetic runs on packed fp32 pairs
+//    (FFMA2).
+//  * Scores: per micro-batch of 8 tokens a lane forms 8 x GW partial dot
 //    products over its d slice, and a transposing butterfly sums them across
 //    the 32 lanes.  Lane l computes token (slot XOR ((l >> 2) & 7)) in slot, so
 //    at every halving step each lane keeps its low slots and sends its high
-//    ones (no selects); afterwards lane l holds all G scores of token
+//    ones (no selects); afterwards lane l holds all scores of token
 //    (l >> 2) & 7 of the micro-batch.
 //  * Probabilities go through a per-warp shared buffer so every lane can
 //    broadcast-read p for each token of the PV accumulation.
@@ -38,7 +41,8 @@
 
 namespace pa {
 
-constexpr int kChunk = 16;  // tokens per TMA copy and per pipeline stage
+constexpr int kChunk = 16;    // tokens per TMA copy and per pipeline stage
+constexpr int kPageTab = 512;  // block-table entries a CTA stages in shared memory
 
 struct DecodeParams {
     const __nv_bfloat16 *q;  // [B, Hq, D]
@@ -59,36 +63,54 @@ struct DecodeParams {
     int out_bf16;
 };
 
-template <int D, int G, int NW, int NS>
+// D: head_dim.  G: query heads per KV head.  HS: warps sharing one chunk,
+// each taking G / HS of the heads (fewer registers per thread, so more warps
+// per SM).  NST: chunk streams (consumer warps = HS * NST).  SPS: stages owned
+// by each stream (NS = NST * SPS in all).
+//
+// Stage ownership matters for correctness: an mbarrier wait tests the parity
+// of a phase, so a waiter must never run two phases ahead of the barrier.
+// Each stream therefore owns SPS stages and cycles through them in order; it
+// has consumed every earlier phase of a stage before it waits on the next,
+// and the producer waits on every phase of a stage's empty barrier in order.
+template <int D, int G, int HS, int NST, int SPS>
 struct DecodeCfg {
+    static constexpr int NS = NST * SPS;
     static constexpr int E = D / 32;
+    static constexpr int GW = G / HS;                    // heads per consumer warp
+    static constexpr int NWC = HS * NST;                 // consumer warps
     static constexpr int ROW_BYTES = D * 2;
     static constexpr int CHUNK_BYTES = kChunk * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;  // K chunk, then V chunk
-    static constexpr int GP = (G + 3) & ~3;              // floats per P row (16-byte rows)
+    static constexpr int GP2 = (GW + 1) & ~1;            // (p, p) pairs per P row (16-byte rows)
     static constexpr int STAGES_BYTES = NS * STAGE_BYTES;
-    static constexpr int MERGE_BYTES = NW * G * D * 4;
+    static constexpr int MERGE_BYTES = NST * G * D * 4;
     static constexpr int OFF_P = STAGES_BYTES;
-    static constexpr int OFF_ML = OFF_P + NW * kChunk * GP * 4;
-    static constexpr int OFF_BAR = OFF_ML + NW * G * 8;
+    static constexpr int OFF_ML = OFF_P + NWC * kChunk * GP2 * 8;
+    static constexpr int OFF_BAR = OFF_ML + NST * G * 8;
     static constexpr int OFF_FLAGS = OFF_BAR + 2 * NS * 8;
-    static constexpr int SMEM_BYTES = OFF_FLAGS + 16 + 1024;  // + slack to align the base to 1 KiB
-    static constexpr int THREADS = (NW + 1) * 32;
+    static constexpr int OFF_PT = OFF_FLAGS + 16;
+    static constexpr int SMEM_BYTES = OFF_PT + kPageTab * 4 + 1024;  // + slack to align the base to 1 KiB
+    static constexpr int THREADS = (NWC + 1) * 32;
     static_assert(D % 32 == 0 && (E == 8 || E == 4), "head_dim 256 or 128");
+    static_assert(G % HS == 0, "heads split evenly across the warps of a chunk");
     static_assert(MERGE_BYTES <= STAGES_BYTES, "the CTA merge reuses the stage buffers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-// E consecutive bf16 of a row -> floats.
+// E consecutive bf16 of a row -> E/2 float pairs (element 2j in .x, 2j+1 in .y).
 template <int E>
-__device__ __forceinline__ void load_bf16_row(const uint8_t *src, float (&f)[E]) {
+__device__ __forceinline__ void load_bf16_pairs(const uint8_t *src, float2 (&f)[E / 2]) {
     if constexpr (E == 8) {
         const uint4 w = *reinterpret_cast<const uint4 *>(src);
-        f[0] = bf16lo(w.x); f[1] = bf16hi(w.x); f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
-        f[4] = bf16lo(w.z); f[5] = bf16hi(w.z); f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+        f[0] = make_float2(bf16lo(w.x), bf16hi(w.x));
+        f[1] = make_float2(bf16lo(w.y), bf16hi(w.y));
+        f[2] = make_float2(bf16lo(w.z), bf16hi(w.z));
+        f[3] = make_float2(bf16lo(w.w), bf16hi(w.w));
     } else {
         const uint2 w = *reinterpret_cast<const uint2 *>(src);
-        f[0] = bf16lo(w.x); f[1] = bf16hi(w.x); f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+        f[0] = make_float2(bf16lo(w.x), bf16hi(w.x));
+        f[1] = make_float2(bf16lo(w.y), bf16hi(w.y));
     }
 }
 
@@ -99,25 +121,43 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
         reinterpret_cast<float *>(out)[idx] = v;
 }
 
-template <int D, int G, int NW, int NS>
-__global__ void __launch_bounds__((NW + 1) * 32, 1)
+template <int D, int G, int HS, int NST, int SPS>
+__global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
     pa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecodeParams p) {
-    using C = DecodeCfg<D, G, NW, NS>;
-    constexpr int E = C::E;
+    using C = DecodeCfg<D, G, HS, NST, SPS>;
+    constexpr int E = C::E, GW = C::GW, NWC = C::NWC, NS = C::NS;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    float *pbuf_all = reinterpret_cast<float *>(smem + C::OFF_P);
+    float2 *pbuf_all = reinterpret_cast<float2 *>(smem + C::OFF_P);
     float2 *merge_ml = reinterpret_cast<float2 *>(smem + C::OFF_ML);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *empty = full + NS;
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::OFF_FLAGS);  // [0] abort, [1] bad page
+    int32_t *page_tab = reinterpret_cast<int32_t *>(smem + C::OFF_PT);
 
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hq0 = kvh * G;
 
+    // Programmatic dependent launch: the reduce grid may be scheduled now, and
+    // this grid's set-up overlaps the kernel before it in the stream (which
+    // may be writing the cache); every global read waits for that kernel.
     pdl_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], HS);
+        }
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == NWC && lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+    }
+    pdl_wait_primary();
 
     int L = p.seq_lens[b];
     if (L < 0 || L > p.max_seq_len) {
@@ -135,86 +175,108 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
                 store_out(p.out, ((size_t)b * p.num_q_heads + hq0) * D + idx, 0.f, p.out_bf16);
         return;
     }
+    // The pages this split touches, staged once: the producer then resolves
+    // every chunk's page from shared memory instead of a dependent global load.
+    const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
+    const int lp_first = (c_begin * kChunk) / p.block_size;
+    const int n_pt = ((c_begin + n_my) * kChunk - 1) / p.block_size - lp_first + 1;
+    const bool staged = n_pt <= kPageTab;
+    if (staged)
+        for (int j = threadIdx.x; j < n_pt; j += C::THREADS) page_tab[j] = bt[lp_first + j];
+    __syncthreads();  // barrier initialisation and the page table are visible to every thread
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        flags[0] = 0;
-        flags[1] = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    float m_run[G], l_run[G], acc[G][E];
-    if (warp == NW) {
+    const int hg = warp % HS, stream = warp / HS;  // consumer warps: head group, chunk stream
+    const int gbase = hg * GW;
+    float m_run[GW], l_run[GW];
+    float2 acc[GW][E / 2];
+    if (warp == NWC) {
         // ---------------- producer: one lane issues every copy ----------------
+        // Streams are refilled independently: the lane probes each stream's
+        // next stage without blocking and issues as soon as that stage is
+        // free, so a slow stream never holds back the others.  Within a
+        // stream, chunks and stage phases are issued strictly in order.
         if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
             const uint64_t policy = l2_policy_evict_first();
-            const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
-            int cur_lp = -1, page = 0, issued = 0;
-            for (int i = 0; i < n_my; ++i) {
-                const int s = i % NS;
-                if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, &flags[0])) {
-                    flags[0] = 1;
-                    break;
-                }
-                const int t0 = (c_begin + i) * kChunk;
-                const int lp = t0 / p.block_size;
-                if (lp != cur_lp) {  // one table read per page
-                    cur_lp = lp;
-                    page = bt[lp];
+            int next[NST];
+#pragma unroll
+            for (int c = 0; c < NST; ++c) next[c] = 0;
+            int remaining = n_my;
+            uint32_t idle = 0;
+            while (remaining > 0) {
+                bool progress = false;
+#pragma unroll
+                for (int c = 0; c < NST; ++c) {
+                    const int k = next[c], i = c + k * NST;
+                    if (i >= n_my) continue;
+                    const int s = c * SPS + k % SPS, ph = k / SPS;
+                    if (ph > 0 && !mbar_test_wait(&empty[s], (ph - 1) & 1)) continue;
+                    const int t0 = (c_begin + i) * kChunk;
+                    const int lp = t0 / p.block_size;
+                    const int page = staged ? page_tab[lp - lp_first] : bt[lp];
                     if (page < 0 || (int64_t)page >= p.num_pages) {
                         flags[1] = 1;  // the copy below reads zeros (box outside the tensor)
                         set_status(p.status, PA_DEV_BAD_PAGE);
                     }
+                    const int off = t0 - lp * p.block_size;
+                    uint8_t *st = smem + s * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+                    tma_load_4d(st, &tm_k, &full[s], 0, kvh, off, page, policy);
+                    tma_load_4d(st + C::CHUNK_BYTES, &tm_v, &full[s], 0, kvh, off, page, policy);
+                    next[c] = k + 1;
+                    --remaining;
+                    progress = true;
                 }
-                const int off = t0 - lp * p.block_size;
-                uint8_t *st = smem + s * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-                tma_load_4d(st, &tm_k, &full[s], 0, kvh, off, page, policy);
-                tma_load_4d(st + C::CHUNK_BYTES, &tm_v, &full[s], 0, kvh, off, page, policy);
-                issued = i + 1;
+                if (progress) {
+                    idle = 0;
+                } else if (++idle > kWaitPollLimit || flags[0]) {
+                    flags[0] = 1;
+                    break;
+                }
             }
             if (flags[0]) {
-                // Giving up: let the copies already in flight land before the CTA ends.
-                for (int i = max(0, issued - NS); i < issued; ++i) {
-                    uint64_t *bar = &full[i % NS];
-                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(bar, (i / NS) & 1); ++n) {
+                // Giving up: let the copies already in flight land before the
+                // CTA ends (each stream's last SPS chunks, one per stage).
+#pragma unroll
+                for (int c = 0; c < NST; ++c)
+                    for (int k = max(0, next[c] - SPS); k < next[c]; ++k) {
+                        uint64_t *bar = &full[c * SPS + k % SPS];
+                        for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(bar, (k / SPS) & 1); ++n) {
+                        }
                     }
-                }
                 set_status(p.status, PA_DEV_TIMEOUT);
             }
         }
     } else {
         // ---------------- consumers ----------------
+        // Arithmetic runs on fp32 pairs (packed FFMA2): dot products pair
+        // adjacent dims (even/odd partial sums), the P.V update pairs adjacent
+        // output dims with the probability duplicated in both halves.
         const int cg = (lane >> 2) & 7;
-        float *pbuf = pbuf_all + warp * (kChunk * C::GP);
-        float qf[G][E];
+        float2 *pbuf = pbuf_all + warp * (kChunk * C::GP2);
+        float2 q2[GW][E / 2];
         {
-            const uint8_t *qrow = reinterpret_cast<const uint8_t *>(p.q + ((size_t)b * p.num_q_heads + hq0) * D) +
+            const uint8_t *qrow = reinterpret_cast<const uint8_t *>(
+                                      p.q + ((size_t)b * p.num_q_heads + hq0 + gbase) * D) +
                                   lane * E * 2;
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                load_bf16_row<E>(qrow + g * D * 2, qf[g]);
+            for (int g = 0; g < GW; ++g) {
+                load_bf16_pairs<E>(qrow + g * D * 2, q2[g]);
 #pragma unroll
-                for (int e = 0; e < E; ++e) qf[g][e] *= p.scale_log2;
+                for (int j = 0; j < E / 2; ++j) q2[g][j] = __fmul2_rn(q2[g][j], sc2);
             }
         }
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < GW; ++g) {
             m_run[g] = -INFINITY;
             l_run[g] = 0.f;
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
+            for (int j = 0; j < E / 2; ++j) acc[g][j] = make_float2(0.f, 0.f);
         }
 
-        for (int i = warp; i < n_my; i += NW) {
-            const int s = i % NS;
-            if (!mbar_wait(&full[s], (i / NS) & 1, &flags[0])) {
+        for (int i = stream, k = 0; i < n_my; i += NST, ++k) {
+            const int s = stream * SPS + k % SPS;
+            if (!mbar_wait(&full[s], (k / SPS) & 1, &flags[0])) {
                 flags[0] = 1;
                 break;
             }
@@ -222,27 +284,37 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
             const uint8_t *vst = kst + C::CHUNK_BYTES;
             const int nv = min(kChunk, L - (c_begin + i) * kChunk);  // valid rows, >= 1
 
-            float sc[2][G];
+            float sc[2][GW];
 #pragma unroll
             for (int mb = 0; mb < 2; ++mb) {
-                float part[8][G];
+                // Slots j and j + 4 are formed together and the first butterfly
+                // step (lane XOR 16) folds the high one into the low one at once.
+                float part[4][GW];
 #pragma unroll
-                for (int slot = 0; slot < 8; ++slot) {
-                    float kf[E];
-                    load_bf16_row<E>(kst + (mb * 8 + (slot ^ cg)) * C::ROW_BYTES + lane * E * 2, kf);
+                for (int j = 0; j < 4; ++j) {
+                    float hi[GW];
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        float a = qf[g][0] * kf[0];
+                    for (int h = 0; h < 2; ++h) {
+                        const int slot = j + 4 * h;
+                        float2 k2[E / 2];
+                        load_bf16_pairs<E>(kst + (mb * 8 + (slot ^ cg)) * C::ROW_BYTES + lane * E * 2, k2);
 #pragma unroll
-                        for (int e = 1; e < E; ++e) a = fmaf(qf[g][e], kf[e], a);
-                        part[slot][g] = a;
+                        for (int g = 0; g < GW; ++g) {
+                            float2 a = __fmul2_rn(q2[g][0], k2[0]);
+#pragma unroll
+                            for (int jj = 1; jj < E / 2; ++jj) a = __ffma2_rn(q2[g][jj], k2[jj], a);
+                            if (h == 0)
+                                part[j][g] = a.x + a.y;
+                            else
+                                hi[g] = a.x + a.y;
+                        }
                     }
+#pragma unroll
+                    for (int g = 0; g < GW; ++g) part[j][g] += __shfl_xor_sync(0xffffffffu, hi[g], 16);
                 }
-                // Transposing butterfly: 8 slots x G -> 1 slot x G, summed over all lanes.
+                // Rest of the transposing butterfly: 4 slots x GW -> 1 slot x GW.
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) part[j][g] += __shfl_xor_sync(0xffffffffu, part[j + 4][g], 16);
+                for (int g = 0; g < GW; ++g) {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) part[j][g] += __shfl_xor_sync(0xffffffffu, part[j + 2][g], 8);
                     part[0][g] += __shfl_xor_sync(0xffffffffu, part[1][g], 4);
@@ -251,18 +323,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
                 }
                 const bool valid = (mb * 8 + cg) < nv;
 #pragma unroll
-                for (int g = 0; g < G; ++g) sc[mb][g] = valid ? part[0][g] : -INFINITY;
+                for (int g = 0; g < GW; ++g) sc[mb][g] = valid ? part[0][g] : -INFINITY;
             }
 
             // Online softmax update (log2 domain); every chunk has >= 1 valid row,
             // so the chunk max is finite.
-            float alpha[G];
+            float alpha[GW];
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float mx = fmaxf(sc[0][g], sc[1][g]);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            for (int g = 0; g < GW; ++g) {
+                const float mx = warp_max(fmaxf(sc[0][g], sc[1][g]));
                 const float m_new = fmaxf(m_run[g], mx);
                 alpha[g] = fast_exp2(m_run[g] - m_new);
                 const float p0 = fast_exp2(sc[0][g] - m_new);
@@ -274,35 +343,39 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
             }
             if ((lane & 3) == 0) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    pbuf[cg * C::GP + g] = sc[0][g];
-                    pbuf[(8 + cg) * C::GP + g] = sc[1][g];
+                for (int g = 0; g < GW; ++g) {
+                    pbuf[cg * C::GP2 + g] = make_float2(sc[0][g], sc[0][g]);
+                    pbuf[(8 + cg) * C::GP2 + g] = make_float2(sc[1][g], sc[1][g]);
                 }
             }
             __syncwarp();
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+            for (int g = 0; g < GW; ++g) {
+                const float2 a2 = make_float2(alpha[g], alpha[g]);
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[g][e] *= alpha[g];
+                for (int j = 0; j < E / 2; ++j) acc[g][j] = __fmul2_rn(acc[g][j], a2);
+            }
 
             auto pv_row = [&](int t) {
-                float vf[E];
-                load_bf16_row<E>(vst + t * C::ROW_BYTES + lane * E * 2, vf);
-                float pr[C::GP];
+                float2 v2[E / 2];
+                load_bf16_pairs<E>(vst + t * C::ROW_BYTES + lane * E * 2, v2);
+                float2 pp[C::GP2];
 #pragma unroll
-                for (int j = 0; j < C::GP; j += 4) {
-                    const float4 v4 = *reinterpret_cast<const float4 *>(pbuf + t * C::GP + j);
-                    pr[j] = v4.x; pr[j + 1] = v4.y; pr[j + 2] = v4.z; pr[j + 3] = v4.w;
+                for (int j = 0; j < C::GP2; j += 2) {
+                    const float4 x = *reinterpret_cast<const float4 *>(pbuf + t * C::GP2 + j);
+                    pp[j] = make_float2(x.x, x.y);
+                    pp[j + 1] = make_float2(x.z, x.w);
                 }
 #pragma unroll
-                for (int g = 0; g < G; ++g)
+                for (int g = 0; g < GW; ++g)
 #pragma unroll
-                    for (int e = 0; e < E; ++e) acc[g][e] = fmaf(pr[g], vf[e], acc[g][e]);
+                    for (int j = 0; j < E / 2; ++j) acc[g][j] = __ffma2_rn(pp[g], v2[j], acc[g][j]);
             };
             if (nv == kChunk) {
-#pragma unroll
+#pragma unroll 4
                 for (int t = 0; t < kChunk; ++t) pv_row(t);
             } else {
+#pragma unroll 1
                 for (int t = 0; t < nv; ++t) pv_row(t);
             }
             __syncwarp();
@@ -310,7 +383,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         }
         // l_run is replicated across lane bits 0-1 and split across bits 2-4.
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < GW; ++g) {
             float l = l_run[g];
             l += __shfl_xor_sync(0xffffffffu, l, 4);
             l += __shfl_xor_sync(0xffffffffu, l, 8);
@@ -321,31 +394,33 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
 
     __syncthreads();  // every chunk is consumed: the stage buffers become the merge area
     const bool aborted = flags[0] != 0;
-    float *merge_acc = reinterpret_cast<float *>(smem);  // [NW][G][D]
-    if (warp < NW) {
+    float *merge_acc = reinterpret_cast<float *>(smem);  // [NST][G][D]
+    if (warp < NWC) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float *dst = merge_acc + (warp * G + g) * D + lane * E;
+        for (int g = 0; g < GW; ++g) {
+            float *dst = merge_acc + (stream * G + gbase + g) * D + lane * E;
 #pragma unroll
-            for (int e = 0; e < E; e += 4) *reinterpret_cast<float4 *>(dst + e) = make_float4(acc[g][e], acc[g][e + 1], acc[g][e + 2], acc[g][e + 3]);
-            if (lane == 0) merge_ml[warp * G + g] = make_float2(m_run[g], l_run[g]);
+            for (int j = 0; j < E / 2; j += 2)
+                *reinterpret_cast<float4 *>(dst + 2 * j) =
+                    make_float4(acc[g][j].x, acc[g][j].y, acc[g][j + 1].x, acc[g][j + 1].y);
+            if (lane == 0) merge_ml[stream * G + gbase + g] = make_float2(m_run[g], l_run[g]);
         }
     }
     __syncthreads();
 
-    // Merge the NW warp states of this split (same log-sum-exp rule as the
+    // Merge the NST stream states of this split (same log-sum-exp rule as the
     // split reduce) and write the split result.
     const bool poisoned = aborted || flags[1] != 0;
     for (int idx = threadIdx.x; idx < G * D; idx += C::THREADS) {
         const int g = idx / D, d = idx - (idx / D) * D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, merge_ml[w * G + g].x);
+        for (int w = 0; w < NST; ++w) M = fmaxf(M, merge_ml[w * G + g].x);
         float lsum = 0.f, o = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
+        for (int w = 0; w < NST; ++w) {
             const float2 ml = merge_ml[w * G + g];
-            const float wgt = fast_exp2(ml.x - M);  // 0 for a warp without chunks (m = -inf)
+            const float wgt = fast_exp2(ml.x - M);  // 0 for a stream without chunks (m = -inf)
             lsum = fmaf(ml.y, wgt, lsum);
             o = fmaf(merge_acc[(w * G + g) * D + d], wgt, o);
         }
@@ -379,14 +454,39 @@ struct ReduceParams {
     int out_bf16;
 };
 
+// Block-wide max / sum over 128 threads (4 warps) through shared scratch.
+__device__ __forceinline__ float block128_max(float v, float *scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = fmaxf(fmaxf(scratch[0], scratch[1]), fmaxf(scratch[2], scratch[3]));
+    __syncthreads();
+    return v;
+}
+
+__device__ __forceinline__ float block128_sum(float v, float *scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = (scratch[0] + scratch[1]) + (scratch[2] + scratch[3]);
+    __syncthreads();
+    return v;
+}
+
+// Grid (Hq, rows, D / 64), 128 threads: each CTA merges a 64-wide slice of
+// one (row, head) output; its threads split the splits 8 ways, and the split
+// statistics are loaded by all threads in parallel.
 template <int D>
-__global__ void __launch_bounds__(256) pa_split_reduce_kernel(const ReduceParams p) {
-    constexpr int QD = D / 4;       // float4 columns
-    constexpr int SG = 256 / QD;    // split groups
+__global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams p) {
+    constexpr int QD = 16;  // float4 columns of the 64-wide slice
+    constexpr int SG = 8;   // split groups
     __shared__ float4 red[SG][QD];
+    __shared__ float scratch[4];
     pdl_wait_primary();  // partials of the split kernel are complete and visible
 
-    const int hq = blockIdx.x, row = blockIdx.y;
+    const int hq = blockIdx.x, row = blockIdx.y, slice = blockIdx.z;
     const int b = row / p.q_len;
     int L = p.seq_lens[b];
     if (L < 0 || L > p.max_seq_len || L < p.q_len) L = 0;  // same rule as the split kernels
@@ -395,37 +495,43 @@ __global__ void __launch_bounds__(256) pa_split_reduce_kernel(const ReduceParams
     const size_t r = (size_t)row * p.num_q_heads + hq;
     const float2 *ml = p.part_ml + r * p.num_splits;
 
-    float M = -INFINITY;
-    bool bad = false;
-    for (int i = 0; i < S_b; ++i) {
+    // max over the non-empty splits, poison check, then the weight sum
+    float M = -INFINITY, bad = 0.f;
+    for (int i = threadIdx.x; i < S_b; i += 128) {
         const float2 v = ml[i];
-        bad |= v.y < 0.f;
+        if (v.y < 0.f) bad = 1.f;
         if (v.y > 0.f) M = fmaxf(M, v.x);
     }
-    float wsum = 0.f;
-    for (int i = 0; i < S_b; ++i) {
+    M = block128_max(M, scratch);
+    bad = block128_max(bad, scratch);
+    float ws = 0.f;
+    for (int i = threadIdx.x; i < S_b; i += 128) {
         const float2 v = ml[i];
-        if (v.y > 0.f) wsum = fmaf(v.y, fast_exp2(v.x - M), wsum);
+        if (v.y > 0.f) ws = fmaf(v.y, fast_exp2(v.x - M), ws);
     }
+    ws = block128_sum(ws, scratch);
+
     const int qd = threadIdx.x % QD, sg = threadIdx.x / QD;
+    const float *po = p.part_o + r * p.num_splits * D + slice * 64 + qd * 4;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int i = sg; i < S_b; i += SG) {
         const float2 v = ml[i];
-        if (!(v.y > 0.f)) continue;
-        const float w = v.y * fast_exp2(v.x - M);
-        const float4 o = *reinterpret_cast<const float4 *>(p.part_o + (r * p.num_splits + i) * D + qd * 4);
+        const float w = v.y > 0.f ? v.y * fast_exp2(v.x - M) : 0.f;
+        const float4 o = *reinterpret_cast<const float4 *>(po + (size_t)i * D);
         a.x = fmaf(w, o.x, a.x); a.y = fmaf(w, o.y, a.y); a.z = fmaf(w, o.z, a.z); a.w = fmaf(w, o.w, a.w);
     }
     red[sg][qd] = a;
     __syncthreads();
     if (sg == 0) {
+#pragma unroll
         for (int j = 1; j < SG; ++j) {
             const float4 o = red[j][qd];
             a.x += o.x; a.y += o.y; a.z += o.z; a.w += o.w;
         }
-        const bool zero = bad || !(wsum > 0.f);
-        const float inv = zero ? 0.f : 1.f / wsum;
-        const size_t base = r * D + qd * 4;
+        const bool zero = bad > 0.f || !(ws > 0.f);
+        const float inv = zero ? 0.f : 1.f / ws;
+        const size_t base = r * D + slice * 64 + qd * 4;
         store_out(p.out, base + 0, a.x * inv, p.out_bf16);
         store_out(p.out, base + 1, a.y * inv, p.out_bf16);
         store_out(p.out, base + 2, a.z * inv, p.out_bf16);

@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(128) pa_reshape_and_cache_kernel(const uint4 *
                                                                    uint4 *__restrict__ v_cache,
                                                                    const int64_t *__restrict__ slots, int row_vecs,
                                                                    int64_t num_slots, int32_t *status) {
+    pdl_launch_dependents();  // the attention kernel behind may start its set-up
     const int i = blockIdx.x;
     const int64_t s = slots[i];
     if (s < 0) return;  // padding token
@@ -325,7 +326,8 @@ pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const vo
         r.chunks_per_split = pl.chunks_per_split;
         r.num_splits = pl.num_splits;
         r.out_bf16 = p.out_bf16;
-        if (launch_reduce(desc->head_dim, r, dim3(desc->num_q_heads, desc->num_seqs), s) != cudaSuccess)
+        if (launch_reduce(desc->head_dim, r, dim3(desc->num_q_heads, desc->num_seqs, desc->head_dim / 64), s) !=
+            cudaSuccess)
             return PA_ERR_CUDA;
     }
     record_plan(PA_PATH_DECODE_CUDA_CORE, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
@@ -387,7 +389,8 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
         r.chunks_per_split = pl.chunks_per_split;
         r.num_splits = pl.num_splits;
         r.out_bf16 = p.out_bf16;
-        if (launch_reduce(desc->head_dim, r, dim3(desc->num_q_heads, desc->num_seqs * desc->q_len), s) !=
+        if (launch_reduce(desc->head_dim, r,
+                          dim3(desc->num_q_heads, desc->num_seqs * desc->q_len, desc->head_dim / 64), s) !=
             cudaSuccess)
             return PA_ERR_CUDA;
     }
