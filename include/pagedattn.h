@@ -161,6 +161,34 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
                                     const pa_attn_desc *desc, void *out, void *workspace,
                                     size_t workspace_bytes, int32_t *device_status, void *stream);
 
+/* Size of the scratch array that pa_paged_attention_decode_noalloc keeps in
+ * device memory (8 MiB per GPU that loads the library, held until exit). */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* pa_paged_attention_decode_noalloc -- the same decode as
+ * pa_paged_attention_decode, for callers that cannot allocate device memory
+ * (for example a plugin inside a serving engine that has already claimed
+ * nearly all of HBM for its own KV-cache pool and owns every allocation, so
+ * it has no spare buffer to hand over).  The pages have no counterpart of
+ * this entry point; it is a convenience of this library.
+ *   - No workspace argument: the split partials go to a scratch array of
+ *     PA_NOALLOC_SCRATCH_BYTES compiled into the library.  A description whose
+ *     pa_workspace_bytes() exceeds that size is rejected with PA_ERR_WORKSPACE
+ *     before anything is launched.
+ *   - The first call on a device looks up the array's device address (a
+ *     cudaGetSymbolAddress on the current device); make that first call before
+ *     any stream capture.  The call allocates nothing (no cudaMalloc/cudaFree).
+ *   - Every call on a device shares the one array, and it keeps the last
+ *     call's contents; nothing in it needs to start at zero, because each call
+ *     writes every partial it later reads.  Calls whose kernels overlap on the
+ *     GPU (different streams, no ordering between them) race on the array and
+ *     give wrong results: order them.
+ * Other arguments, results and errors as for pa_paged_attention_decode. */
+pa_status pa_paged_attention_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                            const int32_t *block_table, const int32_t *seq_lens,
+                                            const pa_attn_desc *desc, void *out, int32_t *device_status,
+                                            void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *pa_status_string(pa_status status);
 
