@@ -87,7 +87,7 @@ struct DecodeCfg {
     static constexpr int MERGE_BYTES = NST * G * D * 4;
     static constexpr int OFF_P = STAGES_BYTES;
     static constexpr int OFF_ML = OFF_P + NWC * kChunk * GP2 * 8;
-    static constexpr int OFF_BAR = OFF_ML + NST * G * 8;
+    static constexpr int OFF_BAR = OFF_ML + NST * G * 12;  // (m, l) pairs, then the merge weights
     static constexpr int OFF_FLAGS = OFF_BAR + 2 * NS * 8;
     static constexpr int OFF_PT = OFF_FLAGS + 16;
     static constexpr int SMEM_BYTES = OFF_PT + kPageTab * 4 + 1024;  // + slack to align the base to 1 KiB
@@ -159,13 +159,25 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
     }
     pdl_wait_primary();
 
+    // The pages this split may touch are staged in shared memory once, so the
+    // producer resolves every chunk's page without a dependent global load.
+    // Their range depends only on the split (entries past the sequence's end
+    // are staged but never used), so these loads are in flight together with
+    // the seq_lens load instead of after it.
+    const int c_begin = split * p.chunks_per_split;
+    const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
+    const int lp_first = (c_begin * kChunk) / p.block_size;
+    const int lp_last = min(((c_begin + p.chunks_per_split) * kChunk - 1) / p.block_size, p.max_pages_per_seq - 1);
+    const int n_pt = lp_last - lp_first + 1;
+    const bool staged = n_pt <= kPageTab;
     int L = p.seq_lens[b];
+    if (staged)
+        for (int j = threadIdx.x; j < n_pt; j += C::THREADS) page_tab[j] = bt[lp_first + j];
     if (L < 0 || L > p.max_seq_len) {
         if (threadIdx.x == 0 && split == 0 && kvh == 0) set_status(p.status, PA_DEV_BAD_SEQLEN);
         L = 0;
     }
     const int n_chunks = (L + kChunk - 1) / kChunk;
-    const int c_begin = split * p.chunks_per_split;
     const int n_my = min(n_chunks - c_begin, p.chunks_per_split);
     if (n_my <= 0) {
         // Nothing of this sequence falls in this split.  The merge reads only
@@ -175,14 +187,6 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
                 store_out(p.out, ((size_t)b * p.num_q_heads + hq0) * D + idx, 0.f, p.out_bf16);
         return;
     }
-    // The pages this split touches, staged once: the producer then resolves
-    // every chunk's page from shared memory instead of a dependent global load.
-    const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
-    const int lp_first = (c_begin * kChunk) / p.block_size;
-    const int n_pt = ((c_begin + n_my) * kChunk - 1) / p.block_size - lp_first + 1;
-    const bool staged = n_pt <= kPageTab;
-    if (staged)
-        for (int j = threadIdx.x; j < n_pt; j += C::THREADS) page_tab[j] = bt[lp_first + j];
     __syncthreads();  // barrier initialisation and the page table are visible to every thread
 
     const int hg = warp % HS, stream = warp / HS;  // consumer warps: head group, chunk stream
@@ -409,29 +413,43 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
     __syncthreads();
 
     // Merge the NST stream states of this split (same log-sum-exp rule as the
-    // split reduce) and write the split result.
+    // split reduce) and write the split result.  The per-(stream, head)
+    // weights 2^(m_w - M) / sum are formed once, then every output element is
+    // a short weighted sum over the streams.
     const bool poisoned = aborted || flags[1] != 0;
-    for (int idx = threadIdx.x; idx < G * D; idx += C::THREADS) {
-        const int g = idx / D, d = idx - (idx / D) * D;
+    float *wgt = reinterpret_cast<float *>(merge_ml + NST * G);  // [NST][G] after (m, l)
+    if (threadIdx.x < G) {
+        const int g = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NST; ++w) M = fmaxf(M, merge_ml[w * G + g].x);
-        float lsum = 0.f, o = 0.f;
+        float lsum = 0.f;
 #pragma unroll
         for (int w = 0; w < NST; ++w) {
             const float2 ml = merge_ml[w * G + g];
-            const float wgt = fast_exp2(ml.x - M);  // 0 for a stream without chunks (m = -inf)
-            lsum = fmaf(ml.y, wgt, lsum);
-            o = fmaf(merge_acc[(w * G + g) * D + d], wgt, o);
+            const float e = fast_exp2(ml.x - M);  // 0 for a stream without chunks (m = -inf)
+            lsum = fmaf(ml.y, e, lsum);
+            wgt[w * G + g] = e;
         }
-        const float res = (poisoned || !(lsum > 0.f)) ? 0.f : o / lsum;
+        const bool zero = poisoned || !(lsum > 0.f);
+        const float inv = zero ? 0.f : 1.f / lsum;
+#pragma unroll
+        for (int w = 0; w < NST; ++w) wgt[w * G + g] *= inv;
+        if (p.num_splits > 1)
+            p.part_ml[((size_t)b * p.num_q_heads + hq0 + g) * p.num_splits + split] =
+                make_float2(M, poisoned ? -1.f : lsum);
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * D; idx += C::THREADS) {
+        const int g = idx / D, d = idx - (idx / D) * D;
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < NST; ++w) o = fmaf(merge_acc[(w * G + g) * D + d], wgt[w * G + g], o);
         const size_t row = (size_t)b * p.num_q_heads + hq0 + g;
-        if (p.num_splits == 1) {
-            store_out(p.out, row * D + d, res, p.out_bf16);
-        } else {
-            p.part_o[(row * p.num_splits + split) * D + d] = res;
-            if (d == 0) p.part_ml[row * p.num_splits + split] = make_float2(M, poisoned ? -1.f : lsum);
-        }
+        if (p.num_splits == 1)
+            store_out(p.out, row * D + d, o, p.out_bf16);
+        else
+            p.part_o[(row * p.num_splits + split) * D + d] = o;
     }
 }
 
@@ -454,37 +472,24 @@ struct ReduceParams {
     int out_bf16;
 };
 
-// Block-wide max / sum over 128 threads (4 warps) through shared scratch.
-__device__ __forceinline__ float block128_max(float v, float *scratch) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-    __syncthreads();
-    v = fmaxf(fmaxf(scratch[0], scratch[1]), fmaxf(scratch[2], scratch[3]));
-    __syncthreads();
-    return v;
-}
 
-__device__ __forceinline__ float block128_sum(float v, float *scratch) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-    __syncthreads();
-    v = (scratch[0] + scratch[1]) + (scratch[2] + scratch[3]);
-    __syncthreads();
-    return v;
-}
 
 // Grid (Hq, rows, D / 64), 128 threads: each CTA merges a 64-wide slice of
-// one (row, head) output; its threads split the splits 8 ways, and the split
-// statistics are loaded by all threads in parallel.
+// one (row, head) output.  Its threads split the splits 8 ways; every thread
+// issues the loads of all its splits' statistics and partial outputs at once,
+// folds them with a running log-sum-exp, and a single exchange merges the 8
+// per-group states.
 template <int D>
 __global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams p) {
     constexpr int QD = 16;  // float4 columns of the 64-wide slice
     constexpr int SG = 8;   // split groups
-    __shared__ float4 red[SG][QD];
-    __shared__ float scratch[4];
-    pdl_wait_primary();  // partials of the split kernel are complete and visible
+    constexpr int UNROLL = 8;
+    __shared__ float4 red_o[SG][QD];
+    __shared__ float2 red_ml[SG];
+    __shared__ int red_bad;
+    pdl_launch_dependents();  // a following attention call may start its set-up
+    if (threadIdx.x == 0) red_bad = 0;
+    pdl_wait_primary();       // partials of the split kernel are complete and visible
 
     const int hq = blockIdx.x, row = blockIdx.y, slice = blockIdx.z;
     const int b = row / p.q_len;
@@ -494,48 +499,64 @@ __global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams
     const int S_b = min(p.num_splits, (n_chunks + p.chunks_per_split - 1) / p.chunks_per_split);
     const size_t r = (size_t)row * p.num_q_heads + hq;
     const float2 *ml = p.part_ml + r * p.num_splits;
-
-    // max over the non-empty splits, poison check, then the weight sum
-    float M = -INFINITY, bad = 0.f;
-    for (int i = threadIdx.x; i < S_b; i += 128) {
-        const float2 v = ml[i];
-        if (v.y < 0.f) bad = 1.f;
-        if (v.y > 0.f) M = fmaxf(M, v.x);
-    }
-    M = block128_max(M, scratch);
-    bad = block128_max(bad, scratch);
-    float ws = 0.f;
-    for (int i = threadIdx.x; i < S_b; i += 128) {
-        const float2 v = ml[i];
-        if (v.y > 0.f) ws = fmaf(v.y, fast_exp2(v.x - M), ws);
-    }
-    ws = block128_sum(ws, scratch);
-
     const int qd = threadIdx.x % QD, sg = threadIdx.x / QD;
     const float *po = p.part_o + r * p.num_splits * D + slice * 64 + qd * 4;
+
+    float M = -INFINITY, W = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int i = sg; i < S_b; i += SG) {
-        const float2 v = ml[i];
-        const float w = v.y > 0.f ? v.y * fast_exp2(v.x - M) : 0.f;
-        const float4 o = *reinterpret_cast<const float4 *>(po + (size_t)i * D);
-        a.x = fmaf(w, o.x, a.x); a.y = fmaf(w, o.y, a.y); a.z = fmaf(w, o.z, a.z); a.w = fmaf(w, o.w, a.w);
+    bool bad = false;
+    for (int i0 = sg; i0 < S_b; i0 += SG * UNROLL) {
+        float2 v[UNROLL];
+        float4 o[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {  // all loads first
+            const int i = i0 + u * SG;
+            if (i < S_b) {
+                v[u] = ml[i];
+                o[u] = *reinterpret_cast<const float4 *>(po + (size_t)i * D);
+            } else {
+                v[u] = make_float2(-INFINITY, 0.f);
+                o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            bad |= v[u].y < 0.f;
+            if (!(v[u].y > 0.f)) continue;  // empty split (or poisoned, flagged above)
+            const float Mn = fmaxf(M, v[u].x);
+            const float c = fast_exp2(M - Mn), e = fast_exp2(v[u].x - Mn) * v[u].y;
+            W = fmaf(W, c, e);
+            a.x = fmaf(a.x, c, e * o[u].x); a.y = fmaf(a.y, c, e * o[u].y);
+            a.z = fmaf(a.z, c, e * o[u].z); a.w = fmaf(a.w, c, e * o[u].w);
+            M = Mn;
+        }
     }
-    red[sg][qd] = a;
+    if (bad) red_bad = 1;
+    red_o[sg][qd] = a;
+    if (qd == 0) red_ml[sg] = make_float2(M, W);
     __syncthreads();
     if (sg == 0) {
+        float Mt = -INFINITY;
 #pragma unroll
-        for (int j = 1; j < SG; ++j) {
-            const float4 o = red[j][qd];
-            a.x += o.x; a.y += o.y; a.z += o.z; a.w += o.w;
+        for (int j = 0; j < SG; ++j) Mt = fmaxf(Mt, red_ml[j].x);
+        float Wt = 0.f;
+        float4 at = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < SG; ++j) {
+            const float2 mw = red_ml[j];
+            if (!(mw.y > 0.f)) continue;
+            const float c = fast_exp2(mw.x - Mt);
+            const float4 o = red_o[j][qd];
+            Wt = fmaf(mw.y, c, Wt);
+            at.x = fmaf(o.x, c, at.x); at.y = fmaf(o.y, c, at.y); at.z = fmaf(o.z, c, at.z); at.w = fmaf(o.w, c, at.w);
         }
-        const bool zero = bad > 0.f || !(ws > 0.f);
-        const float inv = zero ? 0.f : 1.f / ws;
+        const bool zero = red_bad != 0 || !(Wt > 0.f);
+        const float inv = zero ? 0.f : 1.f / Wt;
         const size_t base = r * D + slice * 64 + qd * 4;
-        store_out(p.out, base + 0, a.x * inv, p.out_bf16);
-        store_out(p.out, base + 1, a.y * inv, p.out_bf16);
-        store_out(p.out, base + 2, a.z * inv, p.out_bf16);
-        store_out(p.out, base + 3, a.w * inv, p.out_bf16);
+        store_out(p.out, base + 0, at.x * inv, p.out_bf16);
+        store_out(p.out, base + 1, at.y * inv, p.out_bf16);
+        store_out(p.out, base + 2, at.z * inv, p.out_bf16);
+        store_out(p.out, base + 3, at.w * inv, p.out_bf16);
     }
 }
 
