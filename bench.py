@@ -17,6 +17,11 @@ with CUDA events on the same stream over replays of a graph holding the 16
 layers' decode calls alone (no events inside the graphs, which would break
 the launch overlap between kernels).
 
+After the headline line's measurements, the other workloads of the pages are
+timed as graph replays (`workloads`): the 512-token case (L2-warm and
+L2-flushed), the 11-depth context sweep for the hybrid and dense shapes with a
+fitted per-token slope and a flatness check, batch-32 decode, and verify.
+
 `--impl reference` times the CPU fp64 oracle on the host cores instead (a
 bounded sample of the same workload) and prints the same line shape.
 """
@@ -369,6 +374,7 @@ def bench_gpu(args, world, rank, local):
 
     if rank != 0:
         return
+    suite = None if args.no_suite else secondary_workloads(args, dev, stream, peak)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -392,8 +398,132 @@ def bench_gpu(args, world, rank, local):
         "device_status": st,
         "clocks": clocks.result,
         "cpu_baseline": cpu,
+        "workloads": suite,
     }
     print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------
+# The other workloads of the pages, timed after the headline step (rank 0).
+
+def _time_graph(calls, stream, reps, warm=3):
+    """Captures the callables into one CUDA graph; returns ms per replay."""
+    import torch
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in calls:
+            c()
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def _attention_calls(pa, prob, dev):
+    """One decode (or verify) call per layer of the problem, with its buffers."""
+    import torch
+    bt, sl = prob.block_table.to(dev), prob.seq_lens.to(dev)
+    desc = pa.make_desc(num_seqs=prob.num_seqs, q_len=prob.q_len, num_q_heads=prob.num_q_heads,
+                        num_kv_heads=prob.num_kv_heads, head_dim=prob.head_dim, block_size=prob.block_size,
+                        max_pages_per_seq=prob.max_pages_per_seq, max_seq_len=prob.max_seq_len,
+                        num_pages=prob.num_pages, scale=prob.scale)
+    ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=dev)
+    out = torch.empty((prob.num_seqs * prob.q_len, prob.num_q_heads, prob.head_dim), dtype=torch.float32,
+                      device=dev)
+    fn = pa.paged_attention_decode if prob.q_len == 1 else pa.paged_attention_verify
+    calls = [(lambda l=l: fn(prob.q[l], prob.k_cache[l], prob.v_cache[l], bt, sl, desc, out, ws))
+             for l in range(prob.num_layers)]
+    return calls
+
+
+def _layers_beyond_l2(bytes_per_layer, minimum, l2_bytes=256 << 20):
+    return max(minimum, -(-l2_bytes // max(1, bytes_per_layer)))
+
+
+def secondary_workloads(args, dev, stream, peak):
+    import torch
+    import paged_attention_decode_split_gb300 as pa
+    from paged_attention_decode_split_gb300.inputs import SWEEP_DEPTHS, WORKLOADS, make_problem, sweep_workload
+    res = {}
+
+    # 512-token decode on 16-token pages: 2 MiB of KV, launch-bound.  Timed with
+    # the caches L2-resident, and again after writing a 256 MiB buffer each call.
+    prob = make_problem(1001, **dict(WORKLOADS["decode_l512_bs16"], num_layers=16), device=dev)
+    calls = _attention_calls(pa, prob, dev)
+    warm_us = _time_graph(calls, stream, 200) * 1e3 / len(calls)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * 50)]
+    with torch.cuda.stream(stream):
+        for k in range(50):
+            flush.fill_(k & 0xff)
+            ev[2 * k].record()
+            calls[k % len(calls)]()
+            ev[2 * k + 1].record()
+    torch.cuda.synchronize()
+    flushed = sorted(ev[2 * k].elapsed_time(ev[2 * k + 1]) * 1e3 for k in range(50))
+    kv = 512 * KV_BYTES_PER_TOKEN_LAYER
+    res["decode_l512_bs16"] = {"us_per_call_l2_warm": warm_us, "us_per_call_l2_flushed_median": flushed[25],
+                               "GBps_l2_flushed": kv / (flushed[25] * 1e-6) / 1e9, "plan": pa.last_plan()}
+    del prob, calls, flush
+
+    # Context sweep: a 16-layer step at 11 depths, hybrid (832-token pages) and
+    # dense control (32Q/8KV, head_dim 128, 16-token pages).  Enough distinct
+    # layer copies are cycled to keep the caches out of L2.
+    sweep = {}
+    for dense in (False, True):
+        rows = []
+        for depth in SWEEP_DEPTHS:
+            n = _layers_beyond_l2(depth * KV_BYTES_PER_TOKEN_LAYER, 16)
+            prob = make_problem(1003 + depth + dense, **sweep_workload(depth, dense, num_layers=n), device=dev)
+            calls = _attention_calls(pa, prob, dev)
+            us = _time_graph(calls, stream, max(10, 3200 // n)) * 1e3 / n
+            rows.append({"depth": depth, "us_per_call": us, "us_per_step_16": 16 * us,
+                         "GBps": depth * KV_BYTES_PER_TOKEN_LAYER / (us * 1e-6) / 1e9,
+                         "splits": pa.last_plan()["num_splits"]})
+            del prob, calls
+        xs = [r["depth"] for r in rows]
+        ys = [r["us_per_step_16"] for r in rows]
+        mx, my = sum(xs) / len(xs), sum(ys) / len(ys)
+        slope = sum((x - mx) * (y - my) for x, y in zip(xs, ys)) / sum((x - mx) ** 2 for x in xs)
+        icpt = my - slope * mx
+        dev_pct = [100.0 * ((y - icpt) / x / slope - 1.0) for x, y in zip(xs, ys) if x >= 4096]
+        sweep["dense_control" if dense else "hybrid"] = {
+            "rows": rows, "fit_us_per_context_token_16_layers": slope, "fit_intercept_us": icpt,
+            "max_abs_deviation_pct_depth_ge_4k": max(abs(d) for d in dev_pct),
+            "flat_within_15pct": all(abs(d) <= 15.0 for d in dev_pct)}
+    res["context_sweep"] = sweep
+
+    # Batched decode: 32 sequences, lengths uniform in [1024, 32768].
+    prob = make_problem(1004, **dict(WORKLOADS["batch32_uniform_bs784"], num_layers=2), device=dev)
+    calls = _attention_calls(pa, prob, dev)
+    us = _time_graph(calls, stream, 50) * 1e3 / len(calls)
+    kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER
+    res["batch32_uniform_bs784"] = {"us_per_call": us, "context_tokens": prob.context_tokens(),
+                                    "GBps": kv / (us * 1e-6) / 1e9, "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak,
+                                    "plan": pa.last_plan()}
+    del prob, calls
+
+    # Speculative verify: 8 sequences x 16 new rows, 8192 prior tokens.
+    prob = make_problem(1005, **dict(WORKLOADS["verify_b8_q16_l8192_bs832"], num_layers=4), device=dev)
+    calls = _attention_calls(pa, prob, dev)
+    us = _time_graph(calls, stream, 100) * 1e3 / len(calls)
+    kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER
+    flops = sum(4 * 256 * 24 * (int(L) - 16 + r + 1) for L in prob.seq_lens.tolist() for r in range(16))
+    res["verify_b8_q16_l8192_bs832"] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
+                                        "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak,
+                                        "TFLOPs": flops / (us * 1e-6) / 1e12, "plan": pa.last_plan()}
+    return res
 
 
 def main():
@@ -406,6 +536,7 @@ def main():
                     help="layers per step (16 = the workload; fewer only for small profiling runs)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-suite", action="store_true", help="skip the other workloads (sweep, batch 32, verify)")
     ap.add_argument("--reference-budget", type=float, default=60.0,
                     help="wall seconds after which --impl reference stops taking steps")
     args = ap.parse_args()

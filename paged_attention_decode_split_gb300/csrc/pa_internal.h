@@ -20,7 +20,8 @@ cudaError_t launch_decode(int head_dim, int group, const CUtensorMap &tk, const 
                           const DecodeParams &p, dim3 grid, cudaStream_t stream);
 cudaError_t launch_reduce(int head_dim, const ReduceParams &p, dim3 grid, cudaStream_t stream);
 cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const VerifyParams &p, dim3 grid, cudaStream_t stream);
+                          const CUtensorMap &tk64, const CUtensorMap &tv64, const VerifyParams &p, dim3 grid,
+                          cudaStream_t stream);
 
 // Sets the dynamic shared-memory limit of `fn` once per device.
 cudaError_t ensure_smem_limit(const void *fn, int bytes, int slot);

@@ -95,12 +95,15 @@ pa_status make_plan(const pa_attn_desc *d, bool verify, Plan *pl) {
     } else if (units == 0 || n_chunks == 0) {
         splits = 1;
     } else {
-        splits = static_cast<int>((sms + units - 1) / units);  // enough CTAs to cover the SMs
+        // as many splits as whole waves allow: a grid of units x splits CTAs
+        // never spills a few CTAs into a second wave
+        splits = static_cast<int>(std::max<int64_t>(1, sms / units));
         splits = std::min(splits, std::max(1, n_chunks / kMinChunksPerSplit));
         splits = std::max(splits, (n_chunks + kMaxChunksPerSplit - 1) / kMaxChunksPerSplit);
     }
     splits = std::max(1, std::min(splits, std::max(1, n_chunks)));
     int cps = std::max(1, (n_chunks + splits - 1) / splits);
+    if (verify) cps = (cps + 3) & ~3;  // the tensor-core path walks 64-token tiles: splits of whole tiles
     splits = std::max(1, (n_chunks + cps - 1) / cps);  // no trailing empty split for the longest sequence
     pl->num_sms = sms;
     pl->num_splits = splits;
@@ -150,6 +153,25 @@ bool encode_cache_map(CUtensorMap *map, const void *base, const pa_attn_desc *d,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 5-D view for the tensor-core path: {64 dims, tokens, 64-dim blocks, head,
+// page}; one box of {64, 64 tokens, D/64 blocks, 1, 1} lands in shared memory
+// as [D/64 blocks][64 tokens][128 B] with the 128-byte swizzle -- the K-major
+// (and MN-major) operand layout the MMA reads -- in a single copy.
+bool encode_cache_map_blocks(CUtensorMap *map, const void *base, const pa_attn_desc *d) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t row = (cuuint64_t)d->head_dim * 2;
+    const cuuint64_t dims[5] = {64, (cuuint64_t)d->block_size, (cuuint64_t)(d->head_dim / 64),
+                                (cuuint64_t)d->num_kv_heads, (cuuint64_t)d->num_pages};
+    const cuuint64_t strides[4] = {row * d->num_kv_heads, 128, row, row * d->num_kv_heads * d->block_size};
+    const cuuint32_t box[5] = {64, 64, (cuuint32_t)(d->head_dim / 64), 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -352,6 +374,14 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
     CUtensorMap tk, tv;
     if (!encode_cache_map(&tk, k_cache, desc, 64, true) || !encode_cache_map(&tv, v_cache, desc, 64, true))
         return PA_ERR_CUDA;
+    CUtensorMap tk64, tv64;  // whole-tile copies; only used where a 64-token tile fits in a page
+    if (desc->block_size >= 64) {
+        if (!encode_cache_map_blocks(&tk64, k_cache, desc) || !encode_cache_map_blocks(&tv64, v_cache, desc))
+            return PA_ERR_CUDA;
+    } else {
+        tk64 = tk;  // never used: no 64-token tile fits in a smaller page
+        tv64 = tv;
+    }
 
     const int group = desc->num_q_heads / desc->num_kv_heads;
     VerifyParams p;
@@ -376,7 +406,8 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);
-    if (launch_verify(desc->head_dim, desc->q_len * group, tk, tv, p, grid, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_verify(desc->head_dim, desc->q_len * group, tk, tv, tk64, tv64, p, grid, s) != cudaSuccess)
+        return PA_ERR_CUDA;
     if (pl.num_splits > 1) {
         ReduceParams r;
         r.part_o = p.part_o;
@@ -394,7 +425,7 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
             cudaSuccess)
             return PA_ERR_CUDA;
     }
-    record_plan(PA_PATH_VERIFY_MMA, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
+    record_plan(PA_PATH_VERIFY_TCGEN05, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
     return PA_OK;
 }
 

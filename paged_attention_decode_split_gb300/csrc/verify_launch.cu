@@ -1,6 +1,7 @@
 // verify_launch.cu -- instantiates the multi-row verify kernel per head_dim
 // and number of 16-row slices, and launches it.
 #include "pa_internal.h"
+#include "verify_tc.cuh"
 
 namespace pa {
 
@@ -15,6 +16,18 @@ cudaError_t launch_verify_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+template <int D, int NS>
+cudaError_t launch_verify_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tk64,
+                             const CUtensorMap &tv64, const VerifyParams &p, dim3 grid, cudaStream_t stream,
+                             int slot) {
+    using C = VerifyTcCfg<D, NS>;
+    auto kern = pa_verify_tc_kernel<D, NS>;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, tk64, tv64, p);
     return cudaGetLastError();
 }
 
@@ -41,10 +54,11 @@ bool verify_supported(int head_dim, int rows) {
 }
 
 cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const VerifyParams &p, dim3 grid, cudaStream_t stream) {
-    const int slices = (rows + 15) / 16;
-    if (head_dim == 256) return launch_verify_d<256>(slices, tk, tv, p, grid, stream, 16);
-    if (head_dim == 128) return launch_verify_d<128>(slices, tk, tv, p, grid, stream, 24);
+                          const CUtensorMap &tk64, const CUtensorMap &tv64, const VerifyParams &p, dim3 grid,
+                          cudaStream_t stream) {
+    (void)rows;  // every row count up to 128 runs as one M = 128 block
+    if (head_dim == 256) return launch_verify_tc<256, 2>(tk, tv, tk64, tv64, p, grid, stream, 32);
+    if (head_dim == 128) return launch_verify_tc<128, 4>(tk, tv, tk64, tv64, p, grid, stream, 33);
     return cudaErrorInvalidValue;
 }
 

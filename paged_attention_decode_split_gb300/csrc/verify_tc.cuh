@@ -1,0 +1,505 @@
+// verify_tc.cuh -- multi-row (speculative verify) paged attention on the
+// sm_100-family tensor cores: tcgen05 MMAs with accumulators in tensor memory.
+//
+// What it computes ("Qwen3.8 on MI350P", Lektion 3: verify rows share K/V
+// tiles, a causal mask applies per row, partial softmax statistics merge;
+// "DCU page832 attention", Sec.5/7 for the paged walk): for the q_len new rows
+// of a sequence, row r attends to keys 0 .. L - q_len + r.  All G * q_len query
+// rows of one KV head form one M = 128 MMA block (row rho = r * G + g; rows
+// past G * q_len are zero padding), so each K/V chunk is read from HBM once
+// per CTA and consumed once by the tensor core for all rows.  The context is
+// split across CTAs like decode; the same partition reduce merges the splits.
+//
+// Per 64-token tile i (four 16-token TMA chunks landing side by side):
+//   S_i = Q K_i^T     M=128, N=64, K=D: D/16 MMAs into a tensor-memory buffer
+//                     (two S buffers alternate, so tile i+1's scores are
+//                     formed while the softmax warps work on tile i; N=64
+//                     amortises each read of Q from shared memory over 64 keys)
+//   softmax           4 warps, one query row per thread (tensor-memory lane =
+//                     row): scale, causal mask, running max and sum, P = 2^(s-m)
+//   O += P V_i        M=128, N=D, K=16 per step (4 steps), P carried as a bf16
+//                     head plus a bf16 residual (two MMAs) so it keeps ~16
+//                     significant bits
+// The running max used for the exponentials is only raised when the row's
+// max grows by more than 2^8 (then O and l are rescaled in place); otherwise
+// P may exceed 1 by at most 2^8, which fp32 and the bf16 pair hold exactly
+// enough, and the final division by l uses the same reference max.
+//
+// Operand layouts in shared memory (tcgen05 matrix descriptors):
+//   Q   [D/64 blocks][128 rows][128 B], 128-byte swizzle, K-major
+//   K_i [D/64 blocks][64 tokens][128 B], 128-byte swizzle, K-major: one 5-D TMA
+//       box of 64 tokens when the tile lies in one page, else 64-dim x 16-token
+//       boxes per chunk
+//   V_i same layout as K_i, read as the MN-major (N = d) B operand
+//   P   [16 row groups][8 k cores][8 rows][16 B], no swizzle, K-major
+// Warp roles: 0-3 softmax, 4 MMA issue (and tensor-memory allocation), 5 TMA.
+#pragma once
+
+#include "decode_split.cuh"
+
+namespace pa {
+
+namespace tc {
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrives on the mbarrier when every MMA issued so far by this thread is done.
+__device__ __forceinline__ void commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets, descriptor version 1, layout (0: no swizzle, 2: 128-byte swizzle).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)(layout & 7u) << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
+// B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+}  // namespace tc
+
+template <int D, int NS>
+struct VerifyTcCfg {
+    static constexpr int M = 128;                      // MMA rows (query rows, zero padded)
+    static constexpr int TT = 64;                      // tokens per tile (4 TMA chunks)
+    static constexpr int CPT = TT / kChunk;            // chunks per tile
+    static constexpr int DB = D / 64;                  // 128-byte column blocks
+    static constexpr int TILE_BYTES = TT * D * 2;      // K or V of one tile
+    static constexpr int CHUNK_BYTES = kChunk * D * 2;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile, then V tile
+    static constexpr int Q_BYTES = M * D * 2;
+    static constexpr int P_BYTES = M * TT * 2;         // one bf16 P matrix, 128 x 64
+    static constexpr int OFF_Q = NS * STAGE_BYTES;
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;      // [head, residual]
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    // full[NS], empty[NS], s_full[2], s_free[2], p_full, o_done, mma_fin
+    static constexpr int OFF_TMEM = OFF_BAR + (2 * NS + 7) * 8;
+    static constexpr int OFF_FLAGS = OFF_TMEM + 16;
+    static constexpr int SMEM_BYTES = OFF_FLAGS + 16 + 1024;
+    static constexpr int TMEM_COLS = 512;              // O: D columns, S: 2 x 64 columns
+    static constexpr int S_COL = D;
+    static constexpr int THREADS = 6 * 32;
+    static_assert(D == 256 || D == 128, "head_dim 256 or 128");
+    static_assert(D + 2 * TT <= TMEM_COLS, "tensor-memory columns");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
+
+template <int D, int NS>
+__global__ void __launch_bounds__(6 * 32, 1)
+    pa_verify_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
+                        const VerifyParams p) {
+    using C = VerifyTcCfg<D, NS>;
+    constexpr int TT = C::TT, CPT = C::CPT;
+    constexpr float kLazy = 8.f;  // raise the reference max only when it grows by more than 2^8
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    uint8_t *qs = smem + C::OFF_Q;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *empty = full + NS;
+    uint64_t *s_full = empty + NS;
+    uint64_t *s_free = s_full + 2;
+    uint64_t *p_full = s_free + 2;
+    uint64_t *o_done = p_full + 1;
+    uint64_t *mma_fin = o_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM);
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + C::OFF_FLAGS);  // [0] abort, [1] bad page
+
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.group, R = p.q_len * G;
+
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&s_full[j], 1);
+            mbar_init(&s_free[j], 128);
+        }
+        mbar_init(p_full, 128);
+        mbar_init(o_done, 1);
+        mbar_init(mma_fin, 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5 && lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_k64);
+        prefetch_tensormap(&tm_v64);
+    }
+    pdl_wait_primary();
+
+    int L = p.seq_lens[b];
+    const bool bad_len = L < 0 || L > p.max_seq_len || L < p.q_len;
+    if (bad_len) {
+        if (threadIdx.x == 0 && split == 0 && kvh == 0) set_status(p.status, PA_DEV_BAD_SEQLEN);
+        L = 0;
+    }
+    const int n_chunks = (L + kChunk - 1) / kChunk;
+    const int c_begin = split * p.chunks_per_split;
+    const int n_my = min(n_chunks - c_begin, p.chunks_per_split);
+    if (n_my <= 0) {
+        if (p.num_splits == 1) {
+            for (int idx = threadIdx.x; idx < R * D; idx += C::THREADS) {
+                const int rho = idx / D, d = idx - rho * D;
+                const size_t row = (size_t)b * p.q_len + rho / G;
+                store_out(p.out, (row * p.num_q_heads + kvh * G + rho % G) * D + d, 0.f, p.out_bf16);
+            }
+        }
+        return;
+    }
+    const int n_tiles = (n_my + CPT - 1) / CPT;
+
+    // Q block -> shared memory (swizzled, K-major); padding rows are zero.
+    for (int idx = threadIdx.x; idx < C::M * (D / 8); idx += C::THREADS) {
+        const int rho = idx / (D / 8), c = idx - rho * (D / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (rho < R) {
+            const size_t row = (size_t)b * p.q_len + rho / G;
+            v = *reinterpret_cast<const uint4 *>(p.q + (row * p.num_q_heads + kvh * G + rho % G) * D + c * 8);
+        }
+        *reinterpret_cast<uint4 *>(qs + swz_off(rho, c, C::M)) = v;
+    }
+    tc::fence_async_smem();  // generic-proxy writes of Q become visible to the tensor core
+    if (warp == 4) {
+        tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 5) {
+        // ---------------- producer: TMA copies of K and V, 4 chunks per tile ----------------
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
+            int cur_lp = -1, page = 0, issued = 0;
+            for (int i = 0; i < n_tiles; ++i) {
+                const int s = i % NS;
+                if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, &flags[0])) {
+                    flags[0] = 1;
+                    break;
+                }
+                const int nc = min(CPT, n_my - i * CPT);  // chunks in this tile
+                uint8_t *kt = smem + s * C::STAGE_BYTES;
+                uint8_t *vt = kt + C::TILE_BYTES;
+                mbar_arrive_expect_tx(&full[s], 2 * nc * C::CHUNK_BYTES);
+                for (int c = 0; c < nc; ++c) {
+                    const int t0 = (c_begin + i * CPT + c) * kChunk;
+                    const int lp = t0 / p.block_size;
+                    if (lp != cur_lp) {
+                        cur_lp = lp;
+                        page = bt[lp];
+                        if (page < 0 || (int64_t)page >= p.num_pages) {
+                            flags[1] = 1;
+                            set_status(p.status, PA_DEV_BAD_PAGE);
+                        }
+                    }
+                    const int off = t0 - lp * p.block_size;
+                    if (c == 0 && nc == CPT && off + TT <= p.block_size) {
+                        // the whole tile lies in one page: one copy per tensor lands it as
+                        // [D/64 blocks][64 tokens][128 B]
+                        tma_load_5d(kt, &tm_k64, &full[s], 0, off, 0, kvh, page, policy);
+                        tma_load_5d(vt, &tm_v64, &full[s], 0, off, 0, kvh, page, policy);
+                        break;
+                    }
+#pragma unroll
+                    for (int db = 0; db < C::DB; ++db) {
+                        const int dst = db * TT * 128 + c * kChunk * 128;
+                        tma_load_4d(kt + dst, &tm_k, &full[s], db * 64, kvh, off, page, policy);
+                        tma_load_4d(vt + dst, &tm_v, &full[s], db * 64, kvh, off, page, policy);
+                    }
+                }
+                issued = i + 1;
+            }
+            if (flags[0]) {
+                for (int i = max(0, issued - NS); i < issued; ++i) {
+                    uint64_t *bar = &full[i % NS];
+                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(bar, (i / NS) & 1); ++n) {
+                    }
+                }
+                set_status(p.status, PA_DEV_TIMEOUT);
+            }
+        }
+    } else if (warp == 4) {
+        // ---------------- MMA issue: one lane ----------------
+        if (lane == 0) {
+            constexpr uint32_t kIdQK = tc::idesc_bf16(128, TT, 0);
+            constexpr uint32_t kIdPV = tc::idesc_bf16(128, D, 1);
+            const uint32_t q_base = smem_addr(qs);
+            const uint32_t p_base = smem_addr(smem + C::OFF_P);
+            // Event loop: each product is issued as soon as its own inputs are
+            // ready -- O += P_i V_i when the softmax warps have released P_i,
+            // S_i = Q K_i^T when tile i has landed and an S buffer is free --
+            // so a P.V product never waits behind the next tile's copy (which
+            // would hold its stage, and with it the copy two tiles ahead).
+            int next_qk = 0, next_pv = 0;
+            uint32_t idle = 0;
+            bool ok = true;
+            while (next_pv < n_tiles) {
+                bool progress = false;
+                if (next_pv < next_qk && mbar_test_wait(p_full, next_pv & 1)) {
+                    const int i = next_pv;
+                    tc::fence_after();
+                    const uint32_t v_addr = smem_addr(smem + (i % NS) * C::STAGE_BYTES + C::TILE_BYTES);
+#pragma unroll
+                    for (int ks = 0; ks < TT / 16; ++ks) {
+                        // V: MN-major; 64-dim blocks TT x 128 B apart (LBO), 8-token groups 1 KiB apart (SBO)
+                        const uint64_t bdesc = tc::sdesc(v_addr + ks * 16 * 128, TT * 128, 1024, 2);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            // P: K-major, no swizzle; 8x16 B cores, k cores 128 B apart (LBO),
+                            // row groups TT x 16 B apart (SBO)
+                            const uint64_t adesc = tc::sdesc(p_base + h * C::P_BYTES + ks * 256, 128, TT * 16, 0);
+                            tc::mma_bf16(tmem, adesc, bdesc, kIdPV, (i > 0 || ks > 0 || h > 0) ? 1u : 0u);
+                        }
+                    }
+                    tc::commit(&empty[i % NS]);
+                    tc::commit(o_done);
+                    ++next_pv;
+                    progress = true;
+                }
+                if (next_qk < n_tiles && next_qk - next_pv < 2) {
+                    const int i = next_qk, s = i % NS, j = i & 1;
+                    if (mbar_test_wait(&full[s], (i / NS) & 1) &&
+                        (i < 2 || mbar_test_wait(&s_free[j], ((i - 2) >> 1) & 1))) {
+                        tc::fence_after();
+                        const uint32_t k_addr = smem_addr(smem + s * C::STAGE_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            // 16-element k steps: +32 B inside a 128-byte swizzle row, next 64-dim block further on
+                            const uint32_t koff = (kk >> 2) * (TT * 128) + (kk & 3) * 32;
+                            const uint32_t qoff = (kk >> 2) * (C::M * 128) + (kk & 3) * 32;
+                            tc::mma_bf16(tmem + C::S_COL + j * TT, tc::sdesc(q_base + qoff, 16, 1024, 2),
+                                         tc::sdesc(k_addr + koff, 16, 1024, 2), kIdQK, kk > 0 ? 1u : 0u);
+                        }
+                        tc::commit(&s_full[j]);
+                        ++next_qk;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    idle = 0;
+                } else if (++idle > kWaitPollLimit || flags[0]) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) {
+                flags[0] = 1;
+                set_status(p.status, PA_DEV_TIMEOUT);
+            }
+            // Whatever happened, let every issued MMA finish before tensor
+            // memory is released at the end of the CTA.
+            tc::commit(mma_fin);
+            for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(mma_fin, 0); ++n) {
+            }
+        }
+    } else {
+        // ---------------- softmax: thread = query row = tensor-memory lane ----------------
+        const int rho = threadIdx.x;  // 0..127
+        const bool live = rho < R;
+        // last visible key: the causal limit of the row, and never past this
+        // split's last chunk (a tile may reach into the next split's tokens)
+        const int t_end = min(L, (c_begin + n_my) * kChunk);
+        const int lim = live ? min(L - p.q_len + rho / G, t_end - 1) : -1;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        uint8_t *p_smem = smem + C::OFF_P;
+        // byte offset of this row's first 16-byte core-matrix row in a P matrix
+        const uint32_t prow = (rho >> 3) * (TT * 16) + (rho & 7) * 16;
+        float m_ref = -INFINITY, l_sum = 0.f;
+        bool ok = true;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int j = i & 1;
+            // waits ahead of a warp-collective tensor-memory access end the same way for the whole warp
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j], (i >> 1) & 1, &flags[0]))) {
+                ok = false;
+                break;
+            }
+            tc::fence_after();
+            float sv[TT];
+#pragma unroll
+            for (int c0 = 0; c0 < TT; c0 += 16) {
+                float t16[16];
+                tc::ld16(lane_base + C::S_COL + j * TT + c0, t16);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) sv[c0 + c] = t16[c];
+            }
+            tc::fence_before();
+            mbar_arrive(&s_free[j]);
+
+            const int t0 = (c_begin + i * CPT) * kChunk;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < TT; ++c) {
+                sv[c] = (t0 + c <= lim) ? sv[c] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, sv[c]);
+            }
+            // O (rescale) and the P buffer are touched only after the previous
+            // tile's P.V product has finished.
+            if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(o_done, (i - 1) & 1, &flags[0]))) {
+                ok = false;
+                break;
+            }
+            tc::fence_after();
+            // lazy rescale: only when the max grows by more than 2^kLazy
+            const bool raise = mx > m_ref + kLazy;
+            const bool need_rescale = raise && m_ref != -INFINITY;
+            if (__any_sync(0xffffffffu, need_rescale)) {
+                const float alpha = need_rescale ? fast_exp2(m_ref - mx) : 1.f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    float ov[16];
+                    tc::ld16(lane_base + c0, ov);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) ov[c] *= alpha;
+                    tc::st16(lane_base + c0, ov);
+                }
+                if (need_rescale) l_sum *= alpha;
+            }
+            if (raise) m_ref = mx;
+            // The tile may be short or end in a partial chunk: V rows past the
+            // end hold stale data (even NaN), and 0 * NaN would reach O through
+            // the tensor core, so zero them before the P.V product reads them.
+            const int nv = min(TT, t_end - t0);
+            if (nv < TT) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[i % NS], (i / NS) & 1, &flags[0]))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *vst = smem + (i % NS) * C::STAGE_BYTES + C::TILE_BYTES;
+                for (int idx = threadIdx.x; idx < (TT - nv) * C::DB * 8; idx += 128) {
+                    const int t = nv + idx / (C::DB * 8), rem = idx % (C::DB * 8);
+                    *reinterpret_cast<uint4 *>(vst + (rem >> 3) * (TT * 128) + t * 128 + (rem & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            float ps = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < TT / 8; ++c8) {
+                float pv[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    pv[c] = (m_ref == -INFINITY) ? 0.f : fast_exp2(sv[c8 * 8 + c] - m_ref);
+                    ps += pv[c];
+                }
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) split_bf16(pv[2 * c], pv[2 * c + 1], hw[c], lw[c]);
+                *reinterpret_cast<uint4 *>(p_smem + prow + c8 * 128) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(p_smem + C::P_BYTES + prow + c8 * 128) =
+                    make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            l_sum += ps;
+            tc::fence_async_smem();  // P (and zeroed V rows) are read by the tensor core
+            tc::fence_before();
+            mbar_arrive(p_full);
+        }
+        // Epilogue: wait for the last P.V MMA, normalise and write this row.
+        if (ok && !mbar_wait(o_done, (n_tiles - 1) & 1, &flags[0])) ok = false;
+        ok = __all_sync(0xffffffffu, ok);  // the loads below are warp-collective
+        if (!ok) flags[0] = 1;
+        tc::fence_after();
+        const bool poisoned = !ok || flags[1] != 0;
+        const float inv = (poisoned || !(l_sum > 0.f)) ? 0.f : 1.f / l_sum;
+        const size_t orow = live ? ((size_t)b * p.q_len + rho / G) * p.num_q_heads + kvh * G + rho % G : 0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 16) {
+            float ov[16];
+            if (ok) tc::ld16(lane_base + c0, ov);  // ok is warp-uniform
+            if (live) {
+#pragma unroll
+                for (int c = 0; c < 16; c += 4) {
+                    const float4 v = ok ? make_float4(ov[c] * inv, ov[c + 1] * inv, ov[c + 2] * inv, ov[c + 3] * inv)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (p.num_splits == 1) {
+                        store_out(p.out, orow * D + c0 + c, v.x, p.out_bf16);
+                        store_out(p.out, orow * D + c0 + c + 1, v.y, p.out_bf16);
+                        store_out(p.out, orow * D + c0 + c + 2, v.z, p.out_bf16);
+                        store_out(p.out, orow * D + c0 + c + 3, v.w, p.out_bf16);
+                    } else {
+                        *reinterpret_cast<float4 *>(p.part_o + (orow * p.num_splits + split) * D + c0 + c) = v;
+                    }
+                }
+            }
+        }
+        if (live && p.num_splits > 1)
+            p.part_ml[orow * p.num_splits + split] = make_float2(m_ref, poisoned ? -1.f : l_sum);
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace pa

@@ -220,6 +220,17 @@ def test_verify_small(oracle_mod, q_len, lens, bs):
     assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"verify q_len={q_len}")
 
 
+@pytest.mark.parametrize("splits", [2, 5, 13])
+def test_verify_forced_splits_tiles_cross_split_ends(oracle_mod, splits):
+    """Split sizes that are not whole 64-token tiles: a tile reaches into the
+    next split's tokens, which must be masked out (and the ends zero-filled)."""
+    prob = hybrid(141 + splits, [1700, 900, 37], 784, q_len=16, poison_unused=True)
+    write_new_rows(prob, 11)
+    out, status, plan = run_attention(prob, num_splits=splits)
+    assert status == 0 and plan["num_splits"] > 1
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"verify splits={splits}")
+
+
 @pytest.mark.parametrize("splits", [1, 3])
 def test_verify_dense_shape_d128(oracle_mod, splits):
     prob = make_problem(121, num_seqs=2, seq_lens=[300, 77], num_q_heads=32, num_kv_heads=8, head_dim=128,
