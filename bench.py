@@ -451,12 +451,27 @@ def _layers_beyond_l2(bytes_per_layer, minimum, l2_bytes=256 << 20):
     return max(minimum, -(-l2_bytes // max(1, bytes_per_layer)))
 
 
-def secondary_workloads(args, dev, stream, peak):
+SECONDARY = ("decode_l512_bs16", "context_sweep", "batch32_uniform_bs784", "verify_b8_q16_l8192_bs832")
+
+
+def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
     import torch
     import paged_attention_decode_split_gb300 as pa
     from paged_attention_decode_split_gb300.inputs import SWEEP_DEPTHS, WORKLOADS, make_problem, sweep_workload
     res = {}
 
+    if "decode_l512_bs16" in names:
+        _short_context(pa, torch, dev, stream, res, WORKLOADS, make_problem)
+    if "context_sweep" in names:
+        res["context_sweep"] = _context_sweep(pa, dev, stream, SWEEP_DEPTHS, make_problem, sweep_workload)
+    if "batch32_uniform_bs784" in names:
+        _batch32(pa, dev, stream, peak, res, WORKLOADS, make_problem)
+    if "verify_b8_q16_l8192_bs832" in names:
+        _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem)
+    return res
+
+
+def _short_context(pa, torch, dev, stream, res, WORKLOADS, make_problem):
     # 512-token decode on 16-token pages: 2 MiB of KV, launch-bound.  Timed with
     # the caches L2-resident, and again after writing a 256 MiB buffer each call.
     prob = make_problem(1001, **dict(WORKLOADS["decode_l512_bs16"], num_layers=16), device=dev)
@@ -477,6 +492,8 @@ def secondary_workloads(args, dev, stream, peak):
                                "GBps_l2_flushed": kv / (flushed[25] * 1e-6) / 1e9, "plan": pa.last_plan()}
     del prob, calls, flush
 
+
+def _context_sweep(pa, dev, stream, SWEEP_DEPTHS, make_problem, sweep_workload):
     # Context sweep: a 16-layer step at 11 depths, hybrid (832-token pages) and
     # dense control (32Q/8KV, head_dim 128, 16-token pages).  Enough distinct
     # layer copies are cycled to keep the caches out of L2.
@@ -502,8 +519,10 @@ def secondary_workloads(args, dev, stream, peak):
             "rows": rows, "fit_us_per_context_token_16_layers": slope, "fit_intercept_us": icpt,
             "max_abs_deviation_pct_depth_ge_4k": max(abs(d) for d in dev_pct),
             "flat_within_15pct": all(abs(d) <= 15.0 for d in dev_pct)}
-    res["context_sweep"] = sweep
+    return sweep
 
+
+def _batch32(pa, dev, stream, peak, res, WORKLOADS, make_problem):
     # Batched decode: 32 sequences, lengths uniform in [1024, 32768].
     prob = make_problem(1004, **dict(WORKLOADS["batch32_uniform_bs784"], num_layers=2), device=dev)
     calls = _attention_calls(pa, prob, dev)
@@ -512,8 +531,9 @@ def secondary_workloads(args, dev, stream, peak):
     res["batch32_uniform_bs784"] = {"us_per_call": us, "context_tokens": prob.context_tokens(),
                                     "GBps": kv / (us * 1e-6) / 1e9, "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak,
                                     "plan": pa.last_plan()}
-    del prob, calls
 
+
+def _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem):
     # Speculative verify: 8 sequences x 16 new rows, 8192 prior tokens.
     prob = make_problem(1005, **dict(WORKLOADS["verify_b8_q16_l8192_bs832"], num_layers=4), device=dev)
     calls = _attention_calls(pa, prob, dev)
@@ -523,7 +543,20 @@ def secondary_workloads(args, dev, stream, peak):
     res["verify_b8_q16_l8192_bs832"] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
                                         "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak,
                                         "TFLOPs": flops / (us * 1e-6) / 1e12, "plan": pa.last_plan()}
-    return res
+
+
+def only_workload(args):
+    """Times one secondary workload on cuda:0 (used for small profiling runs)."""
+    import torch
+    import paged_attention_decode_split_gb300 as pa
+    from paged_attention_decode_split_gb300 import _build
+    _build.build()
+    pa.load_library()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    peak, _ = load_peaks()
+    res = secondary_workloads(args, dev, stream, peak, names=(args.only,))
+    print(json.dumps({"workloads": res}), flush=True)
 
 
 def main():
@@ -539,8 +572,13 @@ def main():
     ap.add_argument("--no-suite", action="store_true", help="skip the other workloads (sweep, batch 32, verify)")
     ap.add_argument("--reference-budget", type=float, default=60.0,
                     help="wall seconds after which --impl reference stops taking steps")
+    ap.add_argument("--only", choices=SECONDARY, default=None,
+                    help="time one of the other workloads alone and print its record (no headline line)")
     args = ap.parse_args()
     import torch  # noqa: F401
+    if args.only is not None:
+        only_workload(args)
+        return
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":

@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "decode_split.cuh"
-#include "verify_mma.cuh"
+#include "verify_tc.cuh"
 
 namespace pa {
 

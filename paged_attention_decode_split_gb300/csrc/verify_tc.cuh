@@ -39,6 +39,45 @@
 
 namespace pa {
 
+struct VerifyParams {
+    const __nv_bfloat16 *q;  // [B * q_len, Hq, D]
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    void *out;
+    float *part_o;
+    float2 *part_ml;
+    int32_t *status;
+    int64_t num_pages;
+    int num_q_heads;
+    int q_len;
+    int group;  // G
+    int max_pages_per_seq;
+    int max_seq_len;
+    int block_size;
+    int chunks_per_split;
+    int num_splits;
+    float scale_log2;
+    int out_bf16;
+};
+
+// Byte offset of 16-byte column chunk c of row t in a [D/64][rows][128 B]
+// tile written with the 128-byte swizzle (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t swz_off(int t, int c, int rows) {
+    return (uint32_t)((c >> 3) * rows * 128 + t * 128 + (((c & 7) ^ (t & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// x = head + residual with both parts in bf16 (packed pairs for elements a, b).
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t &head, uint32_t &resid) {
+    head = pack_bf16(a, b);
+    const float ha = __uint_as_float(head << 16), hb = __uint_as_float(head & 0xffff0000u);
+    resid = pack_bf16(a - ha, b - hb);
+}
+
 namespace tc {
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
