@@ -74,6 +74,7 @@ typedef enum { PA_OUT_F32 = 0, PA_OUT_BF16 = 1 } pa_out_dtype;
  *   out_dtype         pa_out_dtype
  *   num_splits        0 = automatic; > 0 forces the split count (benchmarks, tests)
  *   num_sms           0 = query the current device; > 0 plans for that SM count
+ *   flags             0, or PA_FLAG_EARLY_KV_READ (below)
  */
 typedef struct {
     int32_t num_seqs;
@@ -89,7 +90,28 @@ typedef struct {
     int32_t out_dtype;
     int32_t num_splits;
     int32_t num_sms;
+    int32_t flags;
 } pa_attn_desc;
+
+/* desc->flags bits.
+ *
+ * Every kernel of this library is launched as a programmatic dependent of the
+ * work before it on the stream: it may be scheduled while that work is still
+ * running and overlap its own set-up with it.  By default each kernel then
+ * waits for that work to finish before it reads or writes global memory.
+ *
+ * PA_FLAG_EARLY_KV_READ lets a decode or verify call start streaming cached
+ * K/V before that wait.  Before the preceding work has finished it reads only
+ * block_table, seq_lens and the cached K/V rows of positions 0 .. L_b - q_len - 1
+ * (the context before the new rows); q, the new rows' cache slots, the
+ * workspace and the output are touched only after the wait.  The caller
+ * guarantees that no work that may still be running when the call starts
+ * writes any of those early-read inputs.  Kernels of this library honour that
+ * on their own (reshape_and_cache writes only the new rows' slots; the
+ * attention kernels write only workspaces and outputs).  The guarantee is
+ * broken by, for example, a kernel just before the call that fills the block
+ * table or seq_lens on the device. */
+#define PA_FLAG_EARLY_KV_READ 1
 
 /* What the last successful attention call on this host thread ran: the path
  * marker the tests and benchmarks record. */

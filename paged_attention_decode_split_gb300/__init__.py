@@ -28,6 +28,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0
 PA_OUT_F32, PA_OUT_BF16 = 0, 1
 PA_DEV_BAD_SEQLEN, PA_DEV_BAD_PAGE, PA_DEV_BAD_SLOT, PA_DEV_TIMEOUT = 1, 2, 4, 8
 PA_PATH_DECODE_CUDA_CORE, PA_PATH_VERIFY_MMA, PA_PATH_VERIFY_TCGEN05 = 1, 2, 3
+PA_FLAG_EARLY_KV_READ = 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libpagedattn.so")
@@ -39,7 +40,7 @@ class AttnDesc(ctypes.Structure):
         ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("max_pages_per_seq", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("num_pages", ctypes.c_int64),
         ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int32), ("num_splits", ctypes.c_int32),
-        ("num_sms", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32), ("flags", ctypes.c_int32),
     ]
 
 
@@ -99,9 +100,9 @@ def status_string(status: int) -> str:
 
 def make_desc(*, num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
               max_pages_per_seq: int, max_seq_len: int, num_pages: int, scale: float, q_len: int = 1,
-              out_dtype: int = PA_OUT_F32, num_splits: int = 0, num_sms: int = 0) -> AttnDesc:
+              out_dtype: int = PA_OUT_F32, num_splits: int = 0, num_sms: int = 0, flags: int = 0) -> AttnDesc:
     return AttnDesc(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_pages_per_seq,
-                    max_seq_len, num_pages, scale, out_dtype, num_splits, num_sms)
+                    max_seq_len, num_pages, scale, out_dtype, num_splits, num_sms, flags)
 
 
 def workspace_bytes(desc: AttnDesc) -> int:

@@ -7,11 +7,11 @@ namespace pa {
 
 namespace {
 
-template <int D, int G, int HS, int NST, int SPS>
+template <int D, int G, int TS, int NST, int SPS>
 cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, dim3 grid,
                             cudaStream_t stream, int slot) {
-    using C = DecodeCfg<D, G, HS, NST, SPS>;
-    auto kern = pa_decode_split_kernel<D, G, HS, NST, SPS>;
+    using C = DecodeCfg<D, G, TS, NST, SPS>;
+    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the kernel's set-up overlaps the previous
@@ -38,27 +38,27 @@ bool decode_supported(int head_dim, int group) {
     return false;
 }
 
-// Per (head_dim, group): warps per chunk (HS), chunk streams (NST), stages per
-// stream (SPS).  D = 256: 6 streams x 2 stages x 16 KiB; groups of 4 and 6
-// heads are split over 2 warps per chunk, giving 13 warps per CTA at up to
-// 128 registers per thread (more warps to hide latency).  D = 128: 12
-// streams x 2 x 8 KiB, or 6 streams x 4 with the heads split over 2 warps.
+// Per (head_dim, group): warps per chunk (TS), chunk streams (NST), stages
+// per stream (SPS).  D = 256: 6 streams x 2 stages x 16 KiB; groups of 4 and
+// 6 heads split each chunk's tokens over 2 warps, giving 13 warps per CTA.
+// D = 128: 12 streams x 2 x 8 KiB, or 6 streams x 4 with the tokens split
+// over 2 warps.
 cudaError_t launch_decode(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                           const DecodeParams &p, dim3 grid, cudaStream_t stream) {
     if (head_dim == 256) {
         switch (group) {
             case 1: return launch_decode_t<256, 1, 1, 6, 2>(tk, tv, p, grid, stream, 0);
             case 2: return launch_decode_t<256, 2, 1, 6, 2>(tk, tv, p, grid, stream, 1);
-            case 4: return launch_decode_t<256, 4, 2, 6, 2>(tk, tv, p, grid, stream, 2);
-            case 6: return launch_decode_t<256, 6, 2, 6, 2>(tk, tv, p, grid, stream, 3);
+            case 4: return launch_decode_t<256, 4, 2, 4, 3>(tk, tv, p, grid, stream, 2);
+            case 6: return launch_decode_t<256, 6, 2, 4, 3>(tk, tv, p, grid, stream, 3);
         }
     } else if (head_dim == 128) {
         switch (group) {
             case 1: return launch_decode_t<128, 1, 1, 12, 2>(tk, tv, p, grid, stream, 4);
             case 2: return launch_decode_t<128, 2, 1, 12, 2>(tk, tv, p, grid, stream, 5);
-            case 4: return launch_decode_t<128, 4, 1, 12, 2>(tk, tv, p, grid, stream, 6);
-            case 6: return launch_decode_t<128, 6, 2, 6, 4>(tk, tv, p, grid, stream, 7);
-            case 8: return launch_decode_t<128, 8, 2, 6, 4>(tk, tv, p, grid, stream, 8);
+            case 4: return launch_decode_t<128, 4, 2, 6, 4>(tk, tv, p, grid, stream, 6);
+            case 6: return launch_decode_t<128, 6, 2, 4, 6>(tk, tv, p, grid, stream, 7);
+            case 8: return launch_decode_t<128, 8, 2, 4, 6>(tk, tv, p, grid, stream, 8);
         }
     }
     return cudaErrorInvalidValue;

@@ -19,22 +19,25 @@
 //    once (the page-contiguous walk of Sec.7 reads the table once per page).  Only the last chunk of a sequence
 //    can be partial; its rows past the end are masked (scores) and skipped (PV).
 //  * One producer lane issues the copies into NS stages; NST chunk streams
-//    take chunks round-robin, each with its own online softmax and its own
-//    SPS stages, refilled as soon as the stream frees one.  A chunk is shared
-//    by HS warps that split the G heads of the group among them.
-//  * A K/V row is read from shared memory once per warp and used by all of
-//    that warp's query heads (GQA reuse).  A lane owns E = D/32 consecutive
-//    elements of d: q (pre-scaled to log2 units) and the output accumulator
-//    for its heads stay in registers.  Arithmetic runs on packed fp32 pairs
-//    (FFMA2).
-//  * Scores: per micro-batch of 8 tokens a lane forms 8 x GW partial dot
+//    take chunks round-robin, each owning SPS stages that are refilled as
+//    soon as the stream frees one.  A chunk is shared by TS warps that split
+//    its 16 tokens (8 each when TS = 2); every warp keeps its own online
+//    softmax state over the tokens it sees, and the CTA merges the states.
+//  * Every warp handles all G query heads of the group, so each K/V element
+//    is read from shared memory and widened to fp32 once per CTA and used by
+//    the G heads (GQA reuse).  A lane owns E = D/32 consecutive elements of
+//    d: q (pre-scaled to log2 units) and the output accumulators of the G
+//    heads stay in registers.  Arithmetic runs on packed fp32 pairs (FFMA2).
+//  * Scores: per micro-batch of 8 tokens a lane forms 8 x G partial dot
 //    products over its d slice, and a transposing butterfly sums them across
 //    the 32 lanes.  Lane l computes token (slot XOR ((l >> 2) & 7)) in slot, so
 //    at every halving step each lane keeps its low slots and sends its high
 //    ones (no selects); afterwards lane l holds all scores of token
 //    (l >> 2) & 7 of the micro-batch.
-//  * Probabilities go through a per-warp shared buffer so every lane can
-//    broadcast-read p for each token of the PV accumulation.
+//  * Softmax is lazy: a head's reference max is raised (and its O and l
+//    rescaled) only when the chunk max exceeds it by more than 2^8, so most
+//    chunks skip the rescale.  Probabilities go through a per-warp shared
+//    buffer as (p, p) pairs that every lane broadcast-reads for P.V.
 #pragma once
 
 #include "pa_device.cuh"
@@ -43,6 +46,7 @@ namespace pa {
 
 constexpr int kChunk = 16;    // tokens per TMA copy and per pipeline stage
 constexpr int kPageTab = 512;  // block-table entries a CTA stages in shared memory
+constexpr float kLazyLog2 = 8.f;  // a head's reference max is raised only when it grows by more than 2^8
 
 struct DecodeParams {
     const __nv_bfloat16 *q;  // [B, Hq, D]
@@ -61,39 +65,39 @@ struct DecodeParams {
     int num_splits;
     float scale_log2;     // scale * log2(e)
     int out_bf16;
+    int early_kv;         // stream the context before the new row ahead of the dependency wait
 };
 
-// D: head_dim.  G: query heads per KV head.  HS: warps sharing one chunk,
-// each taking G / HS of the heads (fewer registers per thread, so more warps
-// per SM).  NST: chunk streams (consumer warps = HS * NST).  SPS: stages owned
-// by each stream (NS = NST * SPS in all).
+// D: head_dim.  G: query heads per KV head.  TS: warps sharing one chunk,
+// each taking 16 / TS of its tokens.  NST: chunk streams (consumer warps =
+// TS * NST).  SPS: stages owned by each stream (NS = NST * SPS in all).
 //
 // Stage ownership matters for correctness: an mbarrier wait tests the parity
 // of a phase, so a waiter must never run two phases ahead of the barrier.
 // Each stream therefore owns SPS stages and cycles through them in order; it
 // has consumed every earlier phase of a stage before it waits on the next,
 // and the producer waits on every phase of a stage's empty barrier in order.
-template <int D, int G, int HS, int NST, int SPS>
+template <int D, int G, int TS, int NST, int SPS>
 struct DecodeCfg {
     static constexpr int NS = NST * SPS;
     static constexpr int E = D / 32;
-    static constexpr int GW = G / HS;                    // heads per consumer warp
-    static constexpr int NWC = HS * NST;                 // consumer warps
+    static constexpr int MB = 2 / TS;                    // micro-batches of 8 tokens per warp and chunk
+    static constexpr int NWC = TS * NST;                 // consumer warps
     static constexpr int ROW_BYTES = D * 2;
     static constexpr int CHUNK_BYTES = kChunk * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;  // K chunk, then V chunk
-    static constexpr int GP2 = (GW + 1) & ~1;            // (p, p) pairs per P row (16-byte rows)
+    static constexpr int GP2 = (G + 1) & ~1;             // (p, p) pairs per P row (16-byte rows)
     static constexpr int STAGES_BYTES = NS * STAGE_BYTES;
-    static constexpr int MERGE_BYTES = NST * G * D * 4;
+    static constexpr int MERGE_BYTES = NWC * G * D * 4;
     static constexpr int OFF_P = STAGES_BYTES;
-    static constexpr int OFF_ML = OFF_P + NWC * kChunk * GP2 * 8;
-    static constexpr int OFF_BAR = OFF_ML + NST * G * 12;  // (m, l) pairs, then the merge weights
+    static constexpr int OFF_ML = OFF_P + NWC * 8 * MB * GP2 * 8;
+    static constexpr int OFF_BAR = OFF_ML + NWC * G * 12;  // (m, l) pairs, then the merge weights
     static constexpr int OFF_FLAGS = OFF_BAR + 2 * NS * 8;
     static constexpr int OFF_PT = OFF_FLAGS + 16;
     static constexpr int SMEM_BYTES = OFF_PT + kPageTab * 4 + 1024;  // + slack to align the base to 1 KiB
     static constexpr int THREADS = (NWC + 1) * 32;
     static_assert(D % 32 == 0 && (E == 8 || E == 4), "head_dim 256 or 128");
-    static_assert(G % HS == 0, "heads split evenly across the warps of a chunk");
+    static_assert(TS == 1 || TS == 2, "a chunk is consumed by one warp or split in token halves");
     static_assert(MERGE_BYTES <= STAGES_BYTES, "the CTA merge reuses the stage buffers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
@@ -121,12 +125,12 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
         reinterpret_cast<float *>(out)[idx] = v;
 }
 
-template <int D, int G, int HS, int NST, int SPS>
-__global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
+template <int D, int G, int TS, int NST, int SPS>
+__global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
     pa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecodeParams p) {
-    using C = DecodeCfg<D, G, HS, NST, SPS>;
-    constexpr int E = C::E, GW = C::GW, NWC = C::NWC, NS = C::NS;
+    using C = DecodeCfg<D, G, TS, NST, SPS>;
+    constexpr int E = C::E, MB = C::MB, NWC = C::NWC, NS = C::NS;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     float2 *pbuf_all = reinterpret_cast<float2 *>(smem + C::OFF_P);
@@ -141,13 +145,17 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
     const int hq0 = kvh * G;
 
     // Programmatic dependent launch: the reduce grid may be scheduled now, and
-    // this grid's set-up overlaps the kernel before it in the stream (which
-    // may be writing the cache); every global read waits for that kernel.
+    // this grid's set-up overlaps the work before it in the stream (which may
+    // be writing the cache).  By default every global access waits for that
+    // work.  With early_kv, the block table, seq_lens and the K/V chunks that
+    // lie wholly before the new row are read first; q, the new row, the
+    // workspace and the output wait.  Every thread passes the wait before it
+    // exits, so this grid completes only after the work before it.
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], HS);
+            mbar_init(&empty[s], TS);
         }
         flags[0] = 0;
         flags[1] = 0;
@@ -157,7 +165,7 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
-    pdl_wait_primary();
+    if (!p.early_kv) pdl_wait_primary();
 
     // The pages this split may touch are staged in shared memory once, so the
     // producer resolves every chunk's page without a dependent global load.
@@ -182,6 +190,7 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
     if (n_my <= 0) {
         // Nothing of this sequence falls in this split.  The merge reads only
         // non-empty splits; an unsplit call owns its output rows and zeroes them.
+        if (p.early_kv) pdl_wait_primary();
         if (p.num_splits == 1)
             for (int idx = threadIdx.x; idx < G * D; idx += C::THREADS)
                 store_out(p.out, ((size_t)b * p.num_q_heads + hq0) * D + idx, 0.f, p.out_bf16);
@@ -189,10 +198,9 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
     }
     __syncthreads();  // barrier initialisation and the page table are visible to every thread
 
-    const int hg = warp % HS, stream = warp / HS;  // consumer warps: head group, chunk stream
-    const int gbase = hg * GW;
-    float m_run[GW], l_run[GW];
-    float2 acc[GW][E / 2];
+    const int wh = warp % TS, stream = warp / TS;  // consumer warps: token half, chunk stream
+    float m_run[G], l_run[G];
+    float2 acc[G][E / 2];
     if (warp == NWC) {
         // ---------------- producer: one lane issues every copy ----------------
         // Streams are refilled independently: the lane probes each stream's
@@ -205,6 +213,31 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
 #pragma unroll
             for (int c = 0; c < NST; ++c) next[c] = 0;
             int remaining = n_my;
+            auto issue = [&](int c, int k) {  // chunk c + k * NST into stream c's stage k % SPS
+                const int i = c + k * NST, s = c * SPS + k % SPS;
+                const int t0 = (c_begin + i) * kChunk;
+                const int lp = t0 / p.block_size;
+                const int page = staged ? page_tab[lp - lp_first] : bt[lp];
+                if (page < 0 || (int64_t)page >= p.num_pages) {
+                    flags[1] = 1;  // the copy below reads zeros (box outside the tensor)
+                    set_status(p.status, PA_DEV_BAD_PAGE);
+                }
+                const int off = t0 - lp * p.block_size;
+                uint8_t *st = smem + s * C::STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+                tma_load_4d(st, &tm_k, &full[s], 0, kvh, off, page, policy);
+                tma_load_4d(st + C::CHUNK_BYTES, &tm_v, &full[s], 0, kvh, off, page, policy);
+            };
+            if (p.early_kv) {
+                // First use of every stage: the chunks that end before the new
+                // row (token L - 1) go out before the dependency wait.
+                for (int i = 0; i < min(NS, n_my) && (c_begin + i + 1) * kChunk <= L - 1; ++i) {
+                    issue(i % NST, i / NST);
+                    ++next[i % NST];
+                    --remaining;
+                }
+                pdl_wait_primary();
+            }
             uint32_t idle = 0;
             while (remaining > 0) {
                 bool progress = false;
@@ -214,18 +247,7 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
                     if (i >= n_my) continue;
                     const int s = c * SPS + k % SPS, ph = k / SPS;
                     if (ph > 0 && !mbar_test_wait(&empty[s], (ph - 1) & 1)) continue;
-                    const int t0 = (c_begin + i) * kChunk;
-                    const int lp = t0 / p.block_size;
-                    const int page = staged ? page_tab[lp - lp_first] : bt[lp];
-                    if (page < 0 || (int64_t)page >= p.num_pages) {
-                        flags[1] = 1;  // the copy below reads zeros (box outside the tensor)
-                        set_status(p.status, PA_DEV_BAD_PAGE);
-                    }
-                    const int off = t0 - lp * p.block_size;
-                    uint8_t *st = smem + s * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-                    tma_load_4d(st, &tm_k, &full[s], 0, kvh, off, page, policy);
-                    tma_load_4d(st + C::CHUNK_BYTES, &tm_v, &full[s], 0, kvh, off, page, policy);
+                    issue(c, k);
                     next[c] = k + 1;
                     --remaining;
                     progress = true;
@@ -256,22 +278,22 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
         // adjacent dims (even/odd partial sums), the P.V update pairs adjacent
         // output dims with the probability duplicated in both halves.
         const int cg = (lane >> 2) & 7;
-        float2 *pbuf = pbuf_all + warp * (kChunk * C::GP2);
-        float2 q2[GW][E / 2];
+        float2 *pbuf = pbuf_all + warp * (8 * MB * C::GP2);
+        float2 q2[G][E / 2];
+        if (p.early_kv) pdl_wait_primary();  // q may come from the work before this call
         {
-            const uint8_t *qrow = reinterpret_cast<const uint8_t *>(
-                                      p.q + ((size_t)b * p.num_q_heads + hq0 + gbase) * D) +
-                                  lane * E * 2;
+            const uint8_t *qrow =
+                reinterpret_cast<const uint8_t *>(p.q + ((size_t)b * p.num_q_heads + hq0) * D) + lane * E * 2;
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-            for (int g = 0; g < GW; ++g) {
+            for (int g = 0; g < G; ++g) {
                 load_bf16_pairs<E>(qrow + g * D * 2, q2[g]);
 #pragma unroll
                 for (int j = 0; j < E / 2; ++j) q2[g][j] = __fmul2_rn(q2[g][j], sc2);
             }
         }
 #pragma unroll
-        for (int g = 0; g < GW; ++g) {
+        for (int g = 0; g < G; ++g) {
             m_run[g] = -INFINITY;
             l_run[g] = 0.f;
 #pragma unroll
@@ -280,30 +302,32 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
 
         for (int i = stream, k = 0; i < n_my; i += NST, ++k) {
             const int s = stream * SPS + k % SPS;
-            if (!mbar_wait(&full[s], (k / SPS) & 1, &flags[0])) {
+            // the loop body holds full-warp shuffles: every lane leaves together
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / SPS) & 1, &flags[0]))) {
                 flags[0] = 1;
                 break;
             }
-            const uint8_t *kst = smem + s * C::STAGE_BYTES;
+            const uint8_t *kst = smem + s * C::STAGE_BYTES + wh * 8 * C::ROW_BYTES + lane * E * 2;
             const uint8_t *vst = kst + C::CHUNK_BYTES;
-            const int nv = min(kChunk, L - (c_begin + i) * kChunk);  // valid rows, >= 1
+            // valid rows of this warp's part of the chunk (may be <= 0 in the last chunk)
+            const int nv = min(8 * MB, L - (c_begin + i) * kChunk - wh * 8);
 
-            float sc[2][GW];
+            float sc[MB][G];
 #pragma unroll
-            for (int mb = 0; mb < 2; ++mb) {
+            for (int mb = 0; mb < MB; ++mb) {
                 // Slots j and j + 4 are formed together and the first butterfly
                 // step (lane XOR 16) folds the high one into the low one at once.
-                float part[4][GW];
+                float part[4][G];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    float hi[GW];
+                    float hi[G];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int slot = j + 4 * h;
                         float2 k2[E / 2];
-                        load_bf16_pairs<E>(kst + (mb * 8 + (slot ^ cg)) * C::ROW_BYTES + lane * E * 2, k2);
+                        load_bf16_pairs<E>(kst + (mb * 8 + (slot ^ cg)) * C::ROW_BYTES, k2);
 #pragma unroll
-                        for (int g = 0; g < GW; ++g) {
+                        for (int g = 0; g < G; ++g) {
                             float2 a = __fmul2_rn(q2[g][0], k2[0]);
 #pragma unroll
                             for (int jj = 1; jj < E / 2; ++jj) a = __ffma2_rn(q2[g][jj], k2[jj], a);
@@ -314,11 +338,11 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
                         }
                     }
 #pragma unroll
-                    for (int g = 0; g < GW; ++g) part[j][g] += __shfl_xor_sync(0xffffffffu, hi[g], 16);
+                    for (int g = 0; g < G; ++g) part[j][g] += __shfl_xor_sync(0xffffffffu, hi[g], 16);
                 }
-                // Rest of the transposing butterfly: 4 slots x GW -> 1 slot x GW.
+                // Rest of the transposing butterfly: 4 slots x G -> 1 slot x G.
 #pragma unroll
-                for (int g = 0; g < GW; ++g) {
+                for (int g = 0; g < G; ++g) {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) part[j][g] += __shfl_xor_sync(0xffffffffu, part[j + 2][g], 8);
                     part[0][g] += __shfl_xor_sync(0xffffffffu, part[1][g], 4);
@@ -327,67 +351,84 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
                 }
                 const bool valid = (mb * 8 + cg) < nv;
 #pragma unroll
-                for (int g = 0; g < GW; ++g) sc[mb][g] = valid ? part[0][g] : -INFINITY;
+                for (int g = 0; g < G; ++g) sc[mb][g] = valid ? part[0][g] : -INFINITY;
             }
 
-            // Online softmax update (log2 domain); every chunk has >= 1 valid row,
-            // so the chunk max is finite.
-            float alpha[GW];
+            if (nv > 0) {  // warp-uniform
+                // Lazy online softmax (log2 domain): the chunk max of a head is
+                // finite because this part has >= 1 valid row.
+                float mx[G];
+                bool raise_any = false;
 #pragma unroll
-            for (int g = 0; g < GW; ++g) {
-                const float mx = warp_max(fmaxf(sc[0][g], sc[1][g]));
-                const float m_new = fmaxf(m_run[g], mx);
-                alpha[g] = fast_exp2(m_run[g] - m_new);
-                const float p0 = fast_exp2(sc[0][g] - m_new);
-                const float p1 = fast_exp2(sc[1][g] - m_new);
-                l_run[g] = fmaf(l_run[g], alpha[g], p0 + p1);
-                m_run[g] = m_new;
-                sc[0][g] = p0;
-                sc[1][g] = p1;
-            }
-            if ((lane & 3) == 0) {
+                for (int g = 0; g < G; ++g) {
+                    float v = sc[0][g];
 #pragma unroll
-                for (int g = 0; g < GW; ++g) {
-                    pbuf[cg * C::GP2 + g] = make_float2(sc[0][g], sc[0][g]);
-                    pbuf[(8 + cg) * C::GP2 + g] = make_float2(sc[1][g], sc[1][g]);
+                    for (int mb = 1; mb < MB; ++mb) v = fmaxf(v, sc[mb][g]);
+                    mx[g] = warp_max(v);
+                    raise_any |= mx[g] > m_run[g] + kLazyLog2;
                 }
-            }
-            __syncwarp();
+                if (raise_any) {
 #pragma unroll
-            for (int g = 0; g < GW; ++g) {
-                const float2 a2 = make_float2(alpha[g], alpha[g]);
+                    for (int g = 0; g < G; ++g) {
+                        if (mx[g] > m_run[g] + kLazyLog2) {
+                            const float alpha = fast_exp2(m_run[g] - mx[g]);  // 0 on the first chunk
+                            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                for (int j = 0; j < E / 2; ++j) acc[g][j] = __fmul2_rn(acc[g][j], a2);
-            }
+                            for (int j = 0; j < E / 2; ++j) acc[g][j] = __fmul2_rn(acc[g][j], a2);
+                            l_run[g] *= alpha;
+                            m_run[g] = mx[g];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float ps = 0.f;
+#pragma unroll
+                    for (int mb = 0; mb < MB; ++mb) {
+                        const float pv = fast_exp2(sc[mb][g] - m_run[g]);  // 0 for rows past the end
+                        ps += pv;
+                        sc[mb][g] = pv;
+                    }
+                    l_run[g] += ps;
+                }
+                if ((lane & 3) == 0) {
+#pragma unroll
+                    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+                        for (int g = 0; g < G; ++g) pbuf[(mb * 8 + cg) * C::GP2 + g] = make_float2(sc[mb][g], sc[mb][g]);
+                }
+                __syncwarp();
 
-            auto pv_row = [&](int t) {
-                float2 v2[E / 2];
-                load_bf16_pairs<E>(vst + t * C::ROW_BYTES + lane * E * 2, v2);
-                float2 pp[C::GP2];
+                auto pv_row = [&](int t) {
+                    float2 v2[E / 2];
+                    load_bf16_pairs<E>(vst + t * C::ROW_BYTES, v2);
+                    float2 pp[C::GP2];
 #pragma unroll
-                for (int j = 0; j < C::GP2; j += 2) {
-                    const float4 x = *reinterpret_cast<const float4 *>(pbuf + t * C::GP2 + j);
-                    pp[j] = make_float2(x.x, x.y);
-                    pp[j + 1] = make_float2(x.z, x.w);
-                }
+                    for (int j = 0; j < C::GP2; j += 2) {
+                        const float4 x = *reinterpret_cast<const float4 *>(pbuf + t * C::GP2 + j);
+                        pp[j] = make_float2(x.x, x.y);
+                        pp[j + 1] = make_float2(x.z, x.w);
+                    }
 #pragma unroll
-                for (int g = 0; g < GW; ++g)
+                    for (int g = 0; g < G; ++g)
 #pragma unroll
-                    for (int j = 0; j < E / 2; ++j) acc[g][j] = __ffma2_rn(pp[g], v2[j], acc[g][j]);
-            };
-            if (nv == kChunk) {
+                        for (int j = 0; j < E / 2; ++j) acc[g][j] = __ffma2_rn(pp[g], v2[j], acc[g][j]);
+                };
+                if (nv == 8 * MB) {
 #pragma unroll 4
-                for (int t = 0; t < kChunk; ++t) pv_row(t);
-            } else {
+                    for (int t = 0; t < 8 * MB; ++t) pv_row(t);
+                } else {
 #pragma unroll 1
-                for (int t = 0; t < nv; ++t) pv_row(t);
+                    for (int t = 0; t < nv; ++t) pv_row(t);
+                }
+                __syncwarp();
             }
-            __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
-        // l_run is replicated across lane bits 0-1 and split across bits 2-4.
+        // l_run counts each token once per 4 lanes (bits 0-1 replicate) and is
+        // split across lane bits 2-4.
 #pragma unroll
-        for (int g = 0; g < GW; ++g) {
+        for (int g = 0; g < G; ++g) {
             float l = l_run[g];
             l += __shfl_xor_sync(0xffffffffu, l, 4);
             l += __shfl_xor_sync(0xffffffffu, l, 8);
@@ -398,43 +439,43 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
 
     __syncthreads();  // every chunk is consumed: the stage buffers become the merge area
     const bool aborted = flags[0] != 0;
-    float *merge_acc = reinterpret_cast<float *>(smem);  // [NST][G][D]
+    float *merge_acc = reinterpret_cast<float *>(smem);  // [NWC][G][D]
     if (warp < NWC) {
 #pragma unroll
-        for (int g = 0; g < GW; ++g) {
-            float *dst = merge_acc + (stream * G + gbase + g) * D + lane * E;
+        for (int g = 0; g < G; ++g) {
+            float *dst = merge_acc + (warp * G + g) * D + lane * E;
 #pragma unroll
             for (int j = 0; j < E / 2; j += 2)
                 *reinterpret_cast<float4 *>(dst + 2 * j) =
                     make_float4(acc[g][j].x, acc[g][j].y, acc[g][j + 1].x, acc[g][j + 1].y);
-            if (lane == 0) merge_ml[stream * G + gbase + g] = make_float2(m_run[g], l_run[g]);
+            if (lane == 0) merge_ml[warp * G + g] = make_float2(m_run[g], l_run[g]);
         }
     }
     __syncthreads();
 
-    // Merge the NST stream states of this split (same log-sum-exp rule as the
-    // split reduce) and write the split result.  The per-(stream, head)
+    // Merge the NWC warp states of this split (same log-sum-exp rule as the
+    // split reduce) and write the split result.  The per-(warp, head)
     // weights 2^(m_w - M) / sum are formed once, then every output element is
-    // a short weighted sum over the streams.
+    // a short weighted sum over the warps.
     const bool poisoned = aborted || flags[1] != 0;
-    float *wgt = reinterpret_cast<float *>(merge_ml + NST * G);  // [NST][G] after (m, l)
+    float *wgt = reinterpret_cast<float *>(merge_ml + NWC * G);  // [NWC][G] after (m, l)
     if (threadIdx.x < G) {
         const int g = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NST; ++w) M = fmaxf(M, merge_ml[w * G + g].x);
+        for (int w = 0; w < NWC; ++w) M = fmaxf(M, merge_ml[w * G + g].x);
         float lsum = 0.f;
 #pragma unroll
-        for (int w = 0; w < NST; ++w) {
+        for (int w = 0; w < NWC; ++w) {
             const float2 ml = merge_ml[w * G + g];
-            const float e = fast_exp2(ml.x - M);  // 0 for a stream without chunks (m = -inf)
+            const float e = fast_exp2(ml.x - M);  // 0 for a warp without rows (m = -inf)
             lsum = fmaf(ml.y, e, lsum);
             wgt[w * G + g] = e;
         }
         const bool zero = poisoned || !(lsum > 0.f);
         const float inv = zero ? 0.f : 1.f / lsum;
 #pragma unroll
-        for (int w = 0; w < NST; ++w) wgt[w * G + g] *= inv;
+        for (int w = 0; w < NWC; ++w) wgt[w * G + g] *= inv;
         if (p.num_splits > 1)
             p.part_ml[((size_t)b * p.num_q_heads + hq0 + g) * p.num_splits + split] =
                 make_float2(M, poisoned ? -1.f : lsum);
@@ -444,7 +485,7 @@ __global__ void __launch_bounds__((HS * NST + 1) * 32, 1)
         const int g = idx / D, d = idx - (idx / D) * D;
         float o = 0.f;
 #pragma unroll
-        for (int w = 0; w < NST; ++w) o = fmaf(merge_acc[(w * G + g) * D + d], wgt[w * G + g], o);
+        for (int w = 0; w < NWC; ++w) o = fmaf(merge_acc[(w * G + g) * D + d], wgt[w * G + g], o);
         const size_t row = (size_t)b * p.num_q_heads + hq0 + g;
         if (p.num_splits == 1)
             store_out(p.out, row * D + d, o, p.out_bf16);

@@ -60,7 +60,7 @@ pa_status check_desc(const pa_attn_desc *d, bool verify) {
     if (!d) return PA_ERR_INVALID_ARG;
     if (d->num_seqs < 0 || d->q_len < 1 || d->num_q_heads < 1 || d->num_kv_heads < 1 || d->head_dim < 1 ||
         d->block_size < 1 || d->max_pages_per_seq < 0 || d->max_seq_len < 0 || d->num_pages < 1 ||
-        d->num_splits < 0 || d->num_sms < 0)
+        d->num_splits < 0 || d->num_sms < 0 || (d->flags & ~PA_FLAG_EARLY_KV_READ) != 0)
         return PA_ERR_INVALID_ARG;
     if (!verify && d->q_len != 1) return PA_ERR_INVALID_ARG;
     if (d->num_q_heads % d->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(128) pa_reshape_and_cache_kernel(const uint4 *
                                                                    const int64_t *__restrict__ slots, int row_vecs,
                                                                    int64_t num_slots, int32_t *status) {
     pdl_launch_dependents();  // the attention kernel behind may start its set-up
+    pdl_wait_primary();       // the work before it on the stream has finished
     const int i = blockIdx.x;
     const int64_t s = slots[i];
     if (s < 0) return;  // padding token
@@ -287,11 +288,21 @@ pa_status pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cac
         return PA_ERR_INVALID_ARG;
     const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * 2;
     if (row_bytes % 16 != 0 || row_bytes / 16 > INT32_MAX) return PA_ERR_UNSUPPORTED;
-    pa_reshape_and_cache_kernel<<<num_tokens, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_cache),
-        static_cast<uint4 *>(v_cache), slot_mapping, static_cast<int>(row_bytes / 16), num_pages * block_size,
-        device_status);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    // programmatic dependent launch: scheduled early, waits before any access
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_tokens));
+    cfg.blockDim = dim3(128);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, pa_reshape_and_cache_kernel, static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, static_cast<int>(row_bytes / 16),
+        num_pages * block_size, device_status);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
@@ -332,6 +343,7 @@ pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const vo
     p.num_splits = pl.num_splits;
     p.scale_log2 = desc->scale * 1.4426950408889634f;
     p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
+    p.early_kv = (desc->flags & PA_FLAG_EARLY_KV_READ) != 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);
@@ -403,6 +415,7 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
     p.num_splits = pl.num_splits;
     p.scale_log2 = desc->scale * 1.4426950408889634f;
     p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
+    p.early_kv = (desc->flags & PA_FLAG_EARLY_KV_READ) != 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);

@@ -58,6 +58,7 @@ struct VerifyParams {
     int num_splits;
     float scale_log2;
     int out_bf16;
+    int early_kv;  // stream the context before the new rows ahead of the dependency wait
 };
 
 // Byte offset of 16-byte column chunk c of row t in a [D/64][rows][128 B]
@@ -231,7 +232,10 @@ __global__ void __launch_bounds__(6 * 32, 1)
         prefetch_tensormap(&tm_k64);
         prefetch_tensormap(&tm_v64);
     }
-    pdl_wait_primary();
+    // Every global access waits for the work before this call on the stream,
+    // except with early_kv: then the block table, seq_lens and the tiles that
+    // end before the new rows are read first (see the producer below).
+    if (!p.early_kv) pdl_wait_primary();
 
     int L = p.seq_lens[b];
     const bool bad_len = L < 0 || L > p.max_seq_len || L < p.q_len;
@@ -243,6 +247,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
     const int c_begin = split * p.chunks_per_split;
     const int n_my = min(n_chunks - c_begin, p.chunks_per_split);
     if (n_my <= 0) {
+        if (p.early_kv) pdl_wait_primary();
         if (p.num_splits == 1) {
             for (int idx = threadIdx.x; idx < R * D; idx += C::THREADS) {
                 const int rho = idx / D, d = idx - rho * D;
@@ -253,6 +258,56 @@ __global__ void __launch_bounds__(6 * 32, 1)
         return;
     }
     const int n_tiles = (n_my + CPT - 1) / CPT;
+
+    // TMA copies of one tile of K and V (4 chunks); state of the producer lane.
+    const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
+    int cur_lp = -1, page = 0, issued = 0;
+    auto issue_tile = [&](int i, uint64_t policy) {
+        const int s = i % NS;
+        const int nc = min(CPT, n_my - i * CPT);  // chunks in this tile
+        uint8_t *kt = smem + s * C::STAGE_BYTES;
+        uint8_t *vt = kt + C::TILE_BYTES;
+        mbar_arrive_expect_tx(&full[s], 2 * nc * C::CHUNK_BYTES);
+        for (int c = 0; c < nc; ++c) {
+            const int t0 = (c_begin + i * CPT + c) * kChunk;
+            const int lp = t0 / p.block_size;
+            if (lp != cur_lp) {
+                cur_lp = lp;
+                page = bt[lp];
+                if (page < 0 || (int64_t)page >= p.num_pages) {
+                    flags[1] = 1;
+                    set_status(p.status, PA_DEV_BAD_PAGE);
+                }
+            }
+            const int off = t0 - lp * p.block_size;
+            if (c == 0 && nc == CPT && off + TT <= p.block_size) {
+                // the whole tile lies in one page: one copy per tensor lands it as
+                // [D/64 blocks][64 tokens][128 B]
+                tma_load_5d(kt, &tm_k64, &full[s], 0, off, 0, kvh, page, policy);
+                tma_load_5d(vt, &tm_v64, &full[s], 0, off, 0, kvh, page, policy);
+                break;
+            }
+#pragma unroll
+            for (int db = 0; db < C::DB; ++db) {
+                const int dst = db * TT * 128 + c * kChunk * 128;
+                tma_load_4d(kt + dst, &tm_k, &full[s], db * 64, kvh, off, page, policy);
+                tma_load_4d(vt + dst, &tm_v, &full[s], db * 64, kvh, off, page, policy);
+            }
+        }
+    };
+    if (p.early_kv) {
+        __syncthreads();  // barrier initialisation is visible to the producer lane
+        if (warp == 5 && lane == 0) {
+            // first use of each stage: tiles that end before the new rows
+            const uint64_t policy = l2_policy_evict_first();
+            while (issued < min(NS, n_tiles) &&
+                   (c_begin + issued * CPT + min(CPT, n_my - issued * CPT)) * kChunk <= L - p.q_len) {
+                issue_tile(issued, policy);
+                ++issued;
+            }
+        }
+        pdl_wait_primary();
+    }
 
     // Q block -> shared memory (swizzled, K-major); padding rows are zero.
     for (int idx = threadIdx.x; idx < C::M * (D / 8); idx += C::THREADS) {
@@ -278,44 +333,13 @@ __global__ void __launch_bounds__(6 * 32, 1)
         // ---------------- producer: TMA copies of K and V, 4 chunks per tile ----------------
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
-            const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
-            int cur_lp = -1, page = 0, issued = 0;
-            for (int i = 0; i < n_tiles; ++i) {
+            for (int i = issued; i < n_tiles; ++i) {
                 const int s = i % NS;
                 if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, &flags[0])) {
                     flags[0] = 1;
                     break;
                 }
-                const int nc = min(CPT, n_my - i * CPT);  // chunks in this tile
-                uint8_t *kt = smem + s * C::STAGE_BYTES;
-                uint8_t *vt = kt + C::TILE_BYTES;
-                mbar_arrive_expect_tx(&full[s], 2 * nc * C::CHUNK_BYTES);
-                for (int c = 0; c < nc; ++c) {
-                    const int t0 = (c_begin + i * CPT + c) * kChunk;
-                    const int lp = t0 / p.block_size;
-                    if (lp != cur_lp) {
-                        cur_lp = lp;
-                        page = bt[lp];
-                        if (page < 0 || (int64_t)page >= p.num_pages) {
-                            flags[1] = 1;
-                            set_status(p.status, PA_DEV_BAD_PAGE);
-                        }
-                    }
-                    const int off = t0 - lp * p.block_size;
-                    if (c == 0 && nc == CPT && off + TT <= p.block_size) {
-                        // the whole tile lies in one page: one copy per tensor lands it as
-                        // [D/64 blocks][64 tokens][128 B]
-                        tma_load_5d(kt, &tm_k64, &full[s], 0, off, 0, kvh, page, policy);
-                        tma_load_5d(vt, &tm_v64, &full[s], 0, off, 0, kvh, page, policy);
-                        break;
-                    }
-#pragma unroll
-                    for (int db = 0; db < C::DB; ++db) {
-                        const int dst = db * TT * 128 + c * kChunk * 128;
-                        tma_load_4d(kt + dst, &tm_k, &full[s], db * 64, kvh, off, page, policy);
-                        tma_load_4d(vt + dst, &tm_v, &full[s], db * 64, kvh, off, page, policy);
-                    }
-                }
+                issue_tile(i, policy);
                 issued = i + 1;
             }
             if (flags[0]) {

@@ -80,6 +80,7 @@ def test_workspace_plan_rules(lib):
     (dict(scale=float("nan")), pa.PA_ERR_INVALID_ARG),
     (dict(q_len=2), pa.PA_ERR_INVALID_ARG),              # decode takes one row per sequence
     (dict(num_q_heads=40, num_kv_heads=4), pa.PA_ERR_UNSUPPORTED),  # G = 10 not compiled
+    (dict(flags=2), pa.PA_ERR_INVALID_ARG),               # unknown flag bit
 ])
 def test_decode_rejects_bad_descriptions(lib, kw, code):
     desc = hybrid_desc(**kw)
@@ -98,6 +99,20 @@ def test_decode_rejects_bad_pointers_and_workspace(lib):
     assert call(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(desc), FAKE, FAKE, need - 1, None, None) == pa.PA_ERR_WORKSPACE
     assert call(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(desc), FAKE, None, need, None, None) == pa.PA_ERR_WORKSPACE
     assert call(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, need, None, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_desc_layout_matches_header(lib):
+    # the binding's mirror of pa_attn_desc: same fields, same order, 64 bytes
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct {", text.index("Shape and launch description")):text.index("} pa_attn_desc;")]
+    fields = re.findall(r"^\s*(?:int32_t|int64_t|float)\s+(\w+);", body, flags=re.M)
+    assert fields == [name for name, _ in pa.AttnDesc._fields_]
+    assert ctypes.sizeof(pa.AttnDesc) == 64
+
+
+def test_early_kv_flag_accepted(lib):
+    desc = hybrid_desc(flags=pa.PA_FLAG_EARLY_KV_READ)
+    assert pa.workspace_bytes(desc) == pa.workspace_bytes(hybrid_desc())
 
 
 def test_empty_batch_is_a_noop(lib):
