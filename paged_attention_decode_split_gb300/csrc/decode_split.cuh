@@ -188,12 +188,18 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
     const int n_chunks = (L + kChunk - 1) / kChunk;
     const int n_my = min(n_chunks - c_begin, p.chunks_per_split);
     if (n_my <= 0) {
-        // Nothing of this sequence falls in this split.  The merge reads only
-        // non-empty splits; an unsplit call owns its output rows and zeroes them.
+        // Nothing of this sequence falls in this split: its record says "no
+        // keys" (m = -inf, l = 0) so the reduce can read every split without
+        // knowing the sequence length; an unsplit call owns its output rows
+        // and zeroes them.
         if (p.early_kv) pdl_wait_primary();
-        if (p.num_splits == 1)
+        if (p.num_splits == 1) {
             for (int idx = threadIdx.x; idx < G * D; idx += C::THREADS)
                 store_out(p.out, ((size_t)b * p.num_q_heads + hq0) * D + idx, 0.f, p.out_bf16);
+        } else if (threadIdx.x < G) {
+            p.part_ml[((size_t)b * p.num_q_heads + hq0 + threadIdx.x) * p.num_splits + split] =
+                make_float2(-INFINITY, 0.f);
+        }
         return;
     }
     __syncthreads();  // barrier initialisation and the page table are visible to every thread
@@ -503,16 +509,11 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
 struct ReduceParams {
     const float *part_o;
     const float2 *part_ml;
-    const int32_t *seq_lens;
     void *out;
     int num_q_heads;
-    int q_len;
-    int max_seq_len;
-    int chunks_per_split;
     int num_splits;
     int out_bf16;
 };
-
 
 
 // Grid (Hq, rows, D / 64), 128 threads: each CTA merges a 64-wide slice of
@@ -533,11 +534,9 @@ __global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams
     pdl_wait_primary();       // partials of the split kernel are complete and visible
 
     const int hq = blockIdx.x, row = blockIdx.y, slice = blockIdx.z;
-    const int b = row / p.q_len;
-    int L = p.seq_lens[b];
-    if (L < 0 || L > p.max_seq_len || L < p.q_len) L = 0;  // same rule as the split kernels
-    const int n_chunks = (L + kChunk - 1) / kChunk;
-    const int S_b = min(p.num_splits, (n_chunks + p.chunks_per_split - 1) / p.chunks_per_split);
+    // Every split wrote its record (an empty one as m = -inf, l = 0), so all
+    // of them are read and the sequence length is not needed here.
+    const int S_b = p.num_splits;
     const size_t r = (size_t)row * p.num_q_heads + hq;
     const float2 *ml = p.part_ml + r * p.num_splits;
     const int qd = threadIdx.x % QD, sg = threadIdx.x / QD;

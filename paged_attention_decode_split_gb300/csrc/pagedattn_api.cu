@@ -352,12 +352,8 @@ pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const vo
         ReduceParams r;
         r.part_o = p.part_o;
         r.part_ml = p.part_ml;
-        r.seq_lens = seq_lens;
         r.out = out;
         r.num_q_heads = desc->num_q_heads;
-        r.q_len = 1;
-        r.max_seq_len = desc->max_seq_len;
-        r.chunks_per_split = pl.chunks_per_split;
         r.num_splits = pl.num_splits;
         r.out_bf16 = p.out_bf16;
         if (launch_reduce(desc->head_dim, r, dim3(desc->num_q_heads, desc->num_seqs, desc->head_dim / 64), s) !=
@@ -425,12 +421,8 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
         ReduceParams r;
         r.part_o = p.part_o;
         r.part_ml = p.part_ml;
-        r.seq_lens = seq_lens;
         r.out = out;
         r.num_q_heads = desc->num_q_heads;
-        r.q_len = desc->q_len;
-        r.max_seq_len = desc->max_seq_len;
-        r.chunks_per_split = pl.chunks_per_split;
         r.num_splits = pl.num_splits;
         r.out_bf16 = p.out_bf16;
         if (launch_reduce(desc->head_dim, r,

@@ -247,12 +247,20 @@ __global__ void __launch_bounds__(6 * 32, 1)
     const int c_begin = split * p.chunks_per_split;
     const int n_my = min(n_chunks - c_begin, p.chunks_per_split);
     if (n_my <= 0) {
+        // No key of this sequence in this split: an empty record (m = -inf,
+        // l = 0) for the reduce, or zero rows when the call is unsplit.
         if (p.early_kv) pdl_wait_primary();
         if (p.num_splits == 1) {
             for (int idx = threadIdx.x; idx < R * D; idx += C::THREADS) {
                 const int rho = idx / D, d = idx - rho * D;
                 const size_t row = (size_t)b * p.q_len + rho / G;
                 store_out(p.out, (row * p.num_q_heads + kvh * G + rho % G) * D + d, 0.f, p.out_bf16);
+            }
+        } else {
+            for (int rho = threadIdx.x; rho < R; rho += C::THREADS) {
+                const size_t row = (size_t)b * p.q_len + rho / G;
+                p.part_ml[(row * p.num_q_heads + kvh * G + rho % G) * p.num_splits + split] =
+                    make_float2(-INFINITY, 0.f);
             }
         }
         return;
