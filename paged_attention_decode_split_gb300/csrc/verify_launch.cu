@@ -28,8 +28,8 @@ cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const C
                           const CUtensorMap &tk64, const CUtensorMap &tv64, const VerifyParams &p, dim3 grid,
                           cudaStream_t stream) {
     (void)rows;  // every row count up to 128 runs as one M = 128 block
-    if (head_dim == 256) return launch_verify_tc<256, 2>(tk, tv, tk64, tv64, p, grid, stream, 32);
-    if (head_dim == 128) return launch_verify_tc<128, 4>(tk, tv, tk64, tv64, p, grid, stream, 33);
+    if (head_dim == 256) return launch_verify_tc<256, 3>(tk, tv, tk64, tv64, p, grid, stream, 32);
+    if (head_dim == 128) return launch_verify_tc<128, 6>(tk, tv, tk64, tv64, p, grid, stream, 33);
     return cudaErrorInvalidValue;
 }
 

@@ -11,27 +11,30 @@
 // split across CTAs like decode; the same partition reduce merges the splits.
 //
 // Per 64-token tile i (four 16-token TMA chunks landing side by side):
-//   S_i = Q K_i^T     M=128, N=64, K=D: D/16 MMAs into a tensor-memory buffer
-//                     (two S buffers alternate, so tile i+1's scores are
-//                     formed while the softmax warps work on tile i; N=64
-//                     amortises each read of Q from shared memory over 64 keys)
+//   S_i = Q K_i^T     M=128, N=64, K=D: D/16 MMAs with A = Q read from tensor
+//                     memory, into one of two tensor-memory S buffers (tile
+//                     i+1's scores are formed while the softmax warps work on
+//                     tile i)
 //   softmax           4 warps, one query row per thread (tensor-memory lane =
-//                     row): scale, causal mask, running max and sum, P = 2^(s-m)
-//   O += P V_i        M=128, N=D, K=16 per step (4 steps), P carried as a bf16
-//                     head plus a bf16 residual (two MMAs) so it keeps ~16
-//                     significant bits
+//                     row): scale, causal mask, running max and sum, P = 2^(s-m),
+//                     written back over S_i in tensor memory
+//   O += P_i V_i      M=128, N=D, K=16 per step (4 steps), A = P_i from tensor
+//                     memory, carried as a bf16 head plus a bf16 residual (two
+//                     MMAs) so it keeps ~16 significant bits
 // The running max used for the exponentials is only raised when the row's
-// max grows by more than 2^8 (then O and l are rescaled in place); otherwise
-// P may exceed 1 by at most 2^8, which fp32 and the bf16 pair hold exactly
-// enough, and the final division by l uses the same reference max.
+// max grows by more than 2^8 (then O and l are rescaled in place, after the
+// previous tile's P.V product); otherwise P may exceed 1 by at most 2^8, which
+// fp32 and the bf16 pair hold exactly enough, and the final division by l uses
+// the same reference max.  Because O is touched only then, the softmax of tile
+// i+1 overlaps the P.V product of tile i.
 //
-// Operand layouts in shared memory (tcgen05 matrix descriptors):
-//   Q   [D/64 blocks][128 rows][128 B], 128-byte swizzle, K-major
+// Tensor memory (512 columns x 128 lanes): O fp32 in columns [0, D), S/P
+// buffers in [D, D + 128), Q as bf16 pairs in [D + 128, D + 128 + D/2).
+// Shared memory holds only the K/V stages (three of 64 KiB for D = 256):
 //   K_i [D/64 blocks][64 tokens][128 B], 128-byte swizzle, K-major: one 5-D TMA
 //       box of 64 tokens when the tile lies in one page, else 64-dim x 16-token
 //       boxes per chunk
 //   V_i same layout as K_i, read as the MN-major (N = d) B operand
-//   P   [16 row groups][8 k cores][8 rows][16 B], no swizzle, K-major
 // Warp roles: 0-3 softmax, 4 MMA issue (and tensor-memory allocation), 5 TMA.
 #pragma once
 
@@ -106,6 +109,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]: A's M = 128 rows are the tensor-memory
+// lanes, its K elements packed two per 32-bit column.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrives on the mbarrier when every MMA issued so far by this thread is done.
 __device__ __forceinline__ void commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
@@ -142,6 +156,18 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
@@ -167,20 +193,19 @@ struct VerifyTcCfg {
     static constexpr int TILE_BYTES = TT * D * 2;      // K or V of one tile
     static constexpr int CHUNK_BYTES = kChunk * D * 2;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile, then V tile
-    static constexpr int Q_BYTES = M * D * 2;
-    static constexpr int P_BYTES = M * TT * 2;         // one bf16 P matrix, 128 x 64
-    static constexpr int OFF_Q = NS * STAGE_BYTES;
-    static constexpr int OFF_P = OFF_Q + Q_BYTES;      // [head, residual]
-    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-    // full[NS], empty[NS], s_full[2], s_free[2], p_full, o_done, mma_fin
+    static constexpr int OFF_BAR = NS * STAGE_BYTES;
+    // full[NS], empty[NS], s_full[2], p_full[2], o_done[2], mma_fin
     static constexpr int OFF_TMEM = OFF_BAR + (2 * NS + 7) * 8;
     static constexpr int OFF_FLAGS = OFF_TMEM + 16;
     static constexpr int SMEM_BYTES = OFF_FLAGS + 16 + 1024;
-    static constexpr int TMEM_COLS = 512;              // O: D columns, S: 2 x 64 columns
+    // tensor-memory columns: O (fp32, D), two S/P buffers (64 each), Q (bf16 pairs, D / 2)
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int O_COL = 0;
     static constexpr int S_COL = D;
+    static constexpr int Q_COL = D + 2 * TT;
     static constexpr int THREADS = 6 * 32;
     static_assert(D == 256 || D == 128, "head_dim 256 or 128");
-    static_assert(D + 2 * TT <= TMEM_COLS, "tensor-memory columns");
+    static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor-memory columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -194,14 +219,12 @@ __global__ void __launch_bounds__(6 * 32, 1)
     constexpr float kLazy = 8.f;  // raise the reference max only when it grows by more than 2^8
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    uint8_t *qs = smem + C::OFF_Q;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *empty = full + NS;
-    uint64_t *s_full = empty + NS;
-    uint64_t *s_free = s_full + 2;
-    uint64_t *p_full = s_free + 2;
-    uint64_t *o_done = p_full + 1;
-    uint64_t *mma_fin = o_done + 1;
+    uint64_t *s_full = empty + NS;   // [2]: S_i written (tile parity)
+    uint64_t *p_full = s_full + 2;   // [2]: P_i written by the softmax warps
+    uint64_t *o_done = p_full + 2;   // [2]: O += P_i V_i finished
+    uint64_t *mma_fin = o_done + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::OFF_FLAGS);  // [0] abort, [1] bad page
 
@@ -217,10 +240,9 @@ __global__ void __launch_bounds__(6 * 32, 1)
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(&s_full[j], 1);
-            mbar_init(&s_free[j], 128);
+            mbar_init(&p_full[j], 128);
+            mbar_init(&o_done[j], 1);
         }
-        mbar_init(p_full, 128);
-        mbar_init(o_done, 1);
         mbar_init(mma_fin, 1);
         flags[0] = 0;
         flags[1] = 0;
@@ -317,17 +339,6 @@ __global__ void __launch_bounds__(6 * 32, 1)
         pdl_wait_primary();
     }
 
-    // Q block -> shared memory (swizzled, K-major); padding rows are zero.
-    for (int idx = threadIdx.x; idx < C::M * (D / 8); idx += C::THREADS) {
-        const int rho = idx / (D / 8), c = idx - rho * (D / 8);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (rho < R) {
-            const size_t row = (size_t)b * p.q_len + rho / G;
-            v = *reinterpret_cast<const uint4 *>(p.q + (row * p.num_q_heads + kvh * G + rho % G) * D + c * 8);
-        }
-        *reinterpret_cast<uint4 *>(qs + swz_off(rho, c, C::M)) = v;
-    }
-    tc::fence_async_smem();  // generic-proxy writes of Q become visible to the tensor core
     if (warp == 4) {
         tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
         tc::tmem_relinquish();
@@ -336,6 +347,33 @@ __global__ void __launch_bounds__(6 * 32, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's tensor-memory lanes
+
+    // Q block -> tensor memory, the A operand of S = Q K^T: row rho in lane
+    // rho, dims packed two per column; padding rows are zero.
+    if (warp < 4) {
+        const int rho = threadIdx.x;
+        const __nv_bfloat16 *qrow =
+            p.q + (((size_t)b * p.q_len + rho / G) * p.num_q_heads + kvh * G + rho % G) * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            uint32_t r[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 w = rho < R ? *reinterpret_cast<const uint4 *>(qrow + 2 * c0 + 8 * v)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+                r[4 * v] = w.x;
+                r[4 * v + 1] = w.y;
+                r[4 * v + 2] = w.z;
+                r[4 * v + 3] = w.w;
+            }
+            tc::st32(lane_base + C::Q_COL + c0, r);
+        }
+        tc::wait_st();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
 
     if (warp == 5) {
         // ---------------- producer: TMA copies of K and V, 4 chunks per tile ----------------
@@ -364,20 +402,19 @@ __global__ void __launch_bounds__(6 * 32, 1)
         if (lane == 0) {
             constexpr uint32_t kIdQK = tc::idesc_bf16(128, TT, 0);
             constexpr uint32_t kIdPV = tc::idesc_bf16(128, D, 1);
-            const uint32_t q_base = smem_addr(qs);
-            const uint32_t p_base = smem_addr(smem + C::OFF_P);
             // Event loop: each product is issued as soon as its own inputs are
-            // ready -- O += P_i V_i when the softmax warps have released P_i,
-            // S_i = Q K_i^T when tile i has landed and an S buffer is free --
-            // so a P.V product never waits behind the next tile's copy (which
-            // would hold its stage, and with it the copy two tiles ahead).
+            // ready -- O += P_i V_i when the softmax warps have written P_i,
+            // S_i = Q K_i^T when tile i has landed and P_{i-2}, which shares
+            // S_i's columns, has been consumed.  The tensor core runs this
+            // thread's MMAs in issue order, so S_i never overwrites P_{i-2}
+            // before O += P_{i-2} V_{i-2} has read it.
             int next_qk = 0, next_pv = 0;
             uint32_t idle = 0;
             bool ok = true;
             while (next_pv < n_tiles) {
                 bool progress = false;
-                if (next_pv < next_qk && mbar_test_wait(p_full, next_pv & 1)) {
-                    const int i = next_pv;
+                if (next_pv < next_qk && mbar_test_wait(&p_full[next_pv & 1], (next_pv >> 1) & 1)) {
+                    const int i = next_pv, j = i & 1;
                     tc::fence_after();
                     const uint32_t v_addr = smem_addr(smem + (i % NS) * C::STAGE_BYTES + C::TILE_BYTES);
 #pragma unroll
@@ -386,30 +423,27 @@ __global__ void __launch_bounds__(6 * 32, 1)
                         const uint64_t bdesc = tc::sdesc(v_addr + ks * 16 * 128, TT * 128, 1024, 2);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            // P: K-major, no swizzle; 8x16 B cores, k cores 128 B apart (LBO),
-                            // row groups TT x 16 B apart (SBO)
-                            const uint64_t adesc = tc::sdesc(p_base + h * C::P_BYTES + ks * 256, 128, TT * 16, 0);
-                            tc::mma_bf16(tmem, adesc, bdesc, kIdPV, (i > 0 || ks > 0 || h > 0) ? 1u : 0u);
+                            // P (head, then residual): 16 tokens = 8 columns per step
+                            const uint32_t a_tm = tmem + C::S_COL + j * TT + h * (TT / 2) + ks * 8;
+                            tc::mma_bf16_ta(tmem + C::O_COL, a_tm, bdesc, kIdPV, (i > 0 || ks > 0 || h > 0) ? 1u : 0u);
                         }
                     }
                     tc::commit(&empty[i % NS]);
-                    tc::commit(o_done);
+                    tc::commit(&o_done[j]);
                     ++next_pv;
                     progress = true;
                 }
                 if (next_qk < n_tiles && next_qk - next_pv < 2) {
                     const int i = next_qk, s = i % NS, j = i & 1;
-                    if (mbar_test_wait(&full[s], (i / NS) & 1) &&
-                        (i < 2 || mbar_test_wait(&s_free[j], ((i - 2) >> 1) & 1))) {
+                    if (mbar_test_wait(&full[s], (i / NS) & 1)) {
                         tc::fence_after();
                         const uint32_t k_addr = smem_addr(smem + s * C::STAGE_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             // 16-element k steps: +32 B inside a 128-byte swizzle row, next 64-dim block further on
                             const uint32_t koff = (kk >> 2) * (TT * 128) + (kk & 3) * 32;
-                            const uint32_t qoff = (kk >> 2) * (C::M * 128) + (kk & 3) * 32;
-                            tc::mma_bf16(tmem + C::S_COL + j * TT, tc::sdesc(q_base + qoff, 16, 1024, 2),
-                                         tc::sdesc(k_addr + koff, 16, 1024, 2), kIdQK, kk > 0 ? 1u : 0u);
+                            tc::mma_bf16_ta(tmem + C::S_COL + j * TT, tmem + C::Q_COL + kk * 8,
+                                            tc::sdesc(k_addr + koff, 16, 1024, 2), kIdQK, kk > 0 ? 1u : 0u);
                         }
                         tc::commit(&s_full[j]);
                         ++next_qk;
@@ -441,12 +475,14 @@ __global__ void __launch_bounds__(6 * 32, 1)
         // split's last chunk (a tile may reach into the next split's tokens)
         const int t_end = min(L, (c_begin + n_my) * kChunk);
         const int lim = live ? min(L - p.q_len + rho / G, t_end - 1) : -1;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        uint8_t *p_smem = smem + C::OFF_P;
-        // byte offset of this row's first 16-byte core-matrix row in a P matrix
-        const uint32_t prow = (rho >> 3) * (TT * 16) + (rho & 7) * 16;
         float m_ref = -INFINITY, l_sum = 0.f;
         bool ok = true;
+        // O += P_k V_k of tile k is waited for in order per barrier (tile k + 2,
+        // where it is long finished), so no wait ever tests a phase parity
+        // two phases behind the barrier.
+        auto wait_pv = [&](int k) {
+            return __all_sync(0xffffffffu, mbar_wait(&o_done[k & 1], (k >> 1) & 1, &flags[0]));
+        };
         for (int i = 0; i < n_tiles; ++i) {
             const int j = i & 1;
             // waits ahead of a warp-collective tensor-memory access end the same way for the whole warp
@@ -463,8 +499,10 @@ __global__ void __launch_bounds__(6 * 32, 1)
 #pragma unroll
                 for (int c = 0; c < 16; ++c) sv[c0 + c] = t16[c];
             }
-            tc::fence_before();
-            mbar_arrive(&s_free[j]);
+            if (i >= 2 && !wait_pv(i - 2)) {
+                ok = false;
+                break;
+            }
 
             const int t0 = (c_begin + i * CPT) * kChunk;
             float mx = -INFINITY;
@@ -473,25 +511,24 @@ __global__ void __launch_bounds__(6 * 32, 1)
                 sv[c] = (t0 + c <= lim) ? sv[c] * p.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, sv[c]);
             }
-            // O (rescale) and the P buffer are touched only after the previous
-            // tile's P.V product has finished.
-            if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(o_done, (i - 1) & 1, &flags[0]))) {
-                ok = false;
-                break;
-            }
-            tc::fence_after();
-            // lazy rescale: only when the max grows by more than 2^kLazy
+            // lazy rescale: only when the max grows by more than 2^kLazy, and
+            // then only after the previous tile's P.V product has finished
             const bool raise = mx > m_ref + kLazy;
             const bool need_rescale = raise && m_ref != -INFINITY;
             if (__any_sync(0xffffffffu, need_rescale)) {
+                if (!wait_pv(i - 1)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after();
                 const float alpha = need_rescale ? fast_exp2(m_ref - mx) : 1.f;
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 16) {
                     float ov[16];
-                    tc::ld16(lane_base + c0, ov);
+                    tc::ld16(lane_base + C::O_COL + c0, ov);
 #pragma unroll
                     for (int c = 0; c < 16; ++c) ov[c] *= alpha;
-                    tc::st16(lane_base + c0, ov);
+                    tc::st16(lane_base + C::O_COL + c0, ov);
                 }
                 if (need_rescale) l_sum *= alpha;
             }
@@ -511,30 +548,28 @@ __global__ void __launch_bounds__(6 * 32, 1)
                     *reinterpret_cast<uint4 *>(vst + (rem >> 3) * (TT * 128) + t * 128 + (rem & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
+                tc::fence_async_smem();  // zeroed V rows are read by the tensor core
             }
+            // P = 2^(s - m) as a bf16 head and a bf16 residual, written over S_i
+            // (tokens packed two per column: head in the first 32 columns)
             float ps = 0.f;
+            uint32_t hw[TT / 2], lw[TT / 2];
 #pragma unroll
-            for (int c8 = 0; c8 < TT / 8; ++c8) {
-                float pv[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    pv[c] = (m_ref == -INFINITY) ? 0.f : fast_exp2(sv[c8 * 8 + c] - m_ref);
-                    ps += pv[c];
-                }
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) split_bf16(pv[2 * c], pv[2 * c + 1], hw[c], lw[c]);
-                *reinterpret_cast<uint4 *>(p_smem + prow + c8 * 128) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(p_smem + C::P_BYTES + prow + c8 * 128) =
-                    make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            for (int c = 0; c < TT / 2; ++c) {
+                const float p0 = (m_ref == -INFINITY) ? 0.f : fast_exp2(sv[2 * c] - m_ref);
+                const float p1 = (m_ref == -INFINITY) ? 0.f : fast_exp2(sv[2 * c + 1] - m_ref);
+                ps += p0 + p1;
+                split_bf16(p0, p1, hw[c], lw[c]);
             }
             l_sum += ps;
-            tc::fence_async_smem();  // P (and zeroed V rows) are read by the tensor core
+            tc::st32(lane_base + C::S_COL + j * TT, hw);
+            tc::st32(lane_base + C::S_COL + j * TT + TT / 2, lw);
+            tc::wait_st();
             tc::fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[j]);
         }
         // Epilogue: wait for the last P.V MMA, normalise and write this row.
-        if (ok && !mbar_wait(o_done, (n_tiles - 1) & 1, &flags[0])) ok = false;
+        if (ok && !wait_pv(n_tiles - 1)) ok = false;
         ok = __all_sync(0xffffffffu, ok);  // the loads below are warp-collective
         if (!ok) flags[0] = 1;
         tc::fence_after();
@@ -544,7 +579,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 16) {
             float ov[16];
-            if (ok) tc::ld16(lane_base + c0, ov);  // ok is warp-uniform
+            if (ok) tc::ld16(lane_base + C::O_COL + c0, ov);  // ok is warp-uniform
             if (live) {
 #pragma unroll
                 for (int c = 0; c < 16; c += 4) {
