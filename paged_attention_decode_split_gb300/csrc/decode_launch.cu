@@ -64,10 +64,11 @@ cudaError_t launch_decode(int head_dim, int group, const CUtensorMap &tk, const 
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_reduce(int head_dim, const ReduceParams &p, dim3 grid, cudaStream_t stream) {
+// rows = sequences x query rows per sequence.  Few splits: one warp per
+// (row, head); many splits: a CTA per (head, row, 64-dim slice) whose threads
+// split the splits.
+cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -75,6 +76,16 @@ cudaError_t launch_reduce(int head_dim, const ReduceParams &p, dim3 grid, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.num_splits <= kReduceSmallMaxSplits) {
+        const int pairs = rows * p.num_q_heads;
+        cfg.gridDim = dim3((pairs + 7) / 8);
+        cfg.blockDim = dim3(256);
+        if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_split_reduce_small_kernel<256>, p, pairs);
+        if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_split_reduce_small_kernel<128>, p, pairs);
+        return cudaErrorInvalidValue;
+    }
+    cfg.gridDim = dim3(p.num_q_heads, rows, head_dim / 64);
+    cfg.blockDim = dim3(128);
     if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_split_reduce_kernel<256>, p);
     if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_split_reduce_kernel<128>, p);
     return cudaErrorInvalidValue;

@@ -356,8 +356,7 @@ pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const vo
         r.num_q_heads = desc->num_q_heads;
         r.num_splits = pl.num_splits;
         r.out_bf16 = p.out_bf16;
-        if (launch_reduce(desc->head_dim, r, dim3(desc->num_q_heads, desc->num_seqs, desc->head_dim / 64), s) !=
-            cudaSuccess)
+        if (launch_reduce(desc->head_dim, r, desc->num_seqs, s) != cudaSuccess)
             return PA_ERR_CUDA;
     }
     record_plan(PA_PATH_DECODE_CUDA_CORE, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
@@ -425,9 +424,7 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
         r.num_q_heads = desc->num_q_heads;
         r.num_splits = pl.num_splits;
         r.out_bf16 = p.out_bf16;
-        if (launch_reduce(desc->head_dim, r,
-                          dim3(desc->num_q_heads, desc->num_seqs * desc->q_len, desc->head_dim / 64), s) !=
-            cudaSuccess)
+        if (launch_reduce(desc->head_dim, r, desc->num_seqs * desc->q_len, s) != cudaSuccess)
             return PA_ERR_CUDA;
     }
     record_plan(PA_PATH_VERIFY_TCGEN05, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);

@@ -30,7 +30,8 @@
 //
 // Tensor memory (512 columns x 128 lanes): O fp32 in columns [0, D), S/P
 // buffers in [D, D + 128), Q as bf16 pairs in [D + 128, D + 128 + D/2).
-// Shared memory holds only the K/V stages (three of 64 KiB for D = 256):
+// Shared memory holds only K and V tiles, in two rings (4 K and 3 V slots of
+// 32 KiB for D = 256); a K slot is refilled once S_i is done:
 //   K_i [D/64 blocks][64 tokens][128 B], 128-byte swizzle, K-major: one 5-D TMA
 //       box of 64 tokens when the tile lies in one page, else 64-dim x 16-token
 //       boxes per chunk
@@ -184,7 +185,7 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
 
 }  // namespace tc
 
-template <int D, int NS>
+template <int D, int NK, int NV>
 struct VerifyTcCfg {
     static constexpr int M = 128;                      // MMA rows (query rows, zero padded)
     static constexpr int TT = 64;                      // tokens per tile (4 TMA chunks)
@@ -192,10 +193,10 @@ struct VerifyTcCfg {
     static constexpr int DB = D / 64;                  // 128-byte column blocks
     static constexpr int TILE_BYTES = TT * D * 2;      // K or V of one tile
     static constexpr int CHUNK_BYTES = kChunk * D * 2;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile, then V tile
-    static constexpr int OFF_BAR = NS * STAGE_BYTES;
-    // full[NS], empty[NS], s_full[2], p_full[2], o_done[2], mma_fin
-    static constexpr int OFF_TMEM = OFF_BAR + (2 * NS + 7) * 8;
+    static constexpr int OFF_V = NK * TILE_BYTES;       // K ring, then V ring
+    static constexpr int OFF_BAR = OFF_V + NV * TILE_BYTES;
+    // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done[2], mma_fin
+    static constexpr int OFF_TMEM = OFF_BAR + (2 * NK + 2 * NV + 7) * 8;
     static constexpr int OFF_FLAGS = OFF_TMEM + 16;
     static constexpr int SMEM_BYTES = OFF_FLAGS + 16 + 1024;
     // tensor-memory columns: O (fp32, D), two S/P buffers (64 each), Q (bf16 pairs, D / 2)
@@ -209,19 +210,23 @@ struct VerifyTcCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-template <int D, int NS>
+template <int D, int NK, int NV>
 __global__ void __launch_bounds__(6 * 32, 1)
     pa_verify_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
                         const VerifyParams p) {
-    using C = VerifyTcCfg<D, NS>;
+    using C = VerifyTcCfg<D, NK, NV>;
     constexpr int TT = C::TT, CPT = C::CPT;
     constexpr float kLazy = 8.f;  // raise the reference max only when it grows by more than 2^8
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *empty = full + NS;
-    uint64_t *s_full = empty + NS;   // [2]: S_i written (tile parity)
+    // K and V tiles have their own rings: a K slot is free again as soon as
+    // S_i = Q K_i^T is done, long before O += P_i V_i releases the V slot.
+    uint64_t *k_full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *k_empty = k_full + NK;
+    uint64_t *v_full = k_empty + NK;
+    uint64_t *v_empty = v_full + NV;
+    uint64_t *s_full = v_empty + NV; // [2]: S_i written (tile parity)
     uint64_t *p_full = s_full + 2;   // [2]: P_i written by the softmax warps
     uint64_t *o_done = p_full + 2;   // [2]: O += P_i V_i finished
     uint64_t *mma_fin = o_done + 2;
@@ -234,9 +239,13 @@ __global__ void __launch_bounds__(6 * 32, 1)
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(&s_full[j], 1);
@@ -289,52 +298,53 @@ __global__ void __launch_bounds__(6 * 32, 1)
     }
     const int n_tiles = (n_my + CPT - 1) / CPT;
 
-    // TMA copies of one tile of K and V (4 chunks); state of the producer lane.
+    // TMA copies of one tile (4 chunks) of K or of V; state of the producer lane.
     const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
-    int cur_lp = -1, page = 0, issued = 0;
-    auto issue_tile = [&](int i, uint64_t policy) {
-        const int s = i % NS;
+    int lp_cache[2] = {-1, -1}, page_cache[2] = {0, 0};  // per tensor: last page looked up
+    int issued_k = 0, issued_v = 0;
+    auto issue_tile = [&](int i, int tensor, uint64_t policy) {
+        const int s = tensor == 0 ? i % NK : i % NV;
+        uint64_t *bar = tensor == 0 ? &k_full[s] : &v_full[s];
+        uint8_t *dst0 = smem + (tensor == 0 ? s * C::TILE_BYTES : C::OFF_V + s * C::TILE_BYTES);
+        const CUtensorMap *m4 = tensor == 0 ? &tm_k : &tm_v;
+        const CUtensorMap *m5 = tensor == 0 ? &tm_k64 : &tm_v64;
         const int nc = min(CPT, n_my - i * CPT);  // chunks in this tile
-        uint8_t *kt = smem + s * C::STAGE_BYTES;
-        uint8_t *vt = kt + C::TILE_BYTES;
-        mbar_arrive_expect_tx(&full[s], 2 * nc * C::CHUNK_BYTES);
+        mbar_arrive_expect_tx(bar, nc * C::CHUNK_BYTES);
         for (int c = 0; c < nc; ++c) {
             const int t0 = (c_begin + i * CPT + c) * kChunk;
             const int lp = t0 / p.block_size;
-            if (lp != cur_lp) {
-                cur_lp = lp;
-                page = bt[lp];
-                if (page < 0 || (int64_t)page >= p.num_pages) {
+            if (lp != lp_cache[tensor]) {
+                lp_cache[tensor] = lp;
+                page_cache[tensor] = bt[lp];
+                if (page_cache[tensor] < 0 || (int64_t)page_cache[tensor] >= p.num_pages) {
                     flags[1] = 1;
                     set_status(p.status, PA_DEV_BAD_PAGE);
                 }
             }
+            const int page = page_cache[tensor];
             const int off = t0 - lp * p.block_size;
             if (c == 0 && nc == CPT && off + TT <= p.block_size) {
-                // the whole tile lies in one page: one copy per tensor lands it as
+                // the whole tile lies in one page: one copy lands it as
                 // [D/64 blocks][64 tokens][128 B]
-                tma_load_5d(kt, &tm_k64, &full[s], 0, off, 0, kvh, page, policy);
-                tma_load_5d(vt, &tm_v64, &full[s], 0, off, 0, kvh, page, policy);
+                tma_load_5d(dst0, m5, bar, 0, off, 0, kvh, page, policy);
                 break;
             }
 #pragma unroll
-            for (int db = 0; db < C::DB; ++db) {
-                const int dst = db * TT * 128 + c * kChunk * 128;
-                tma_load_4d(kt + dst, &tm_k, &full[s], db * 64, kvh, off, page, policy);
-                tma_load_4d(vt + dst, &tm_v, &full[s], db * 64, kvh, off, page, policy);
-            }
+            for (int db = 0; db < C::DB; ++db)
+                tma_load_4d(dst0 + db * TT * 128 + c * kChunk * 128, m4, bar, db * 64, kvh, off, page, policy);
         }
+    };
+    // tiles that end before the new rows (early_kv reads only those before the wait)
+    auto before_new_rows = [&](int i) {
+        return (c_begin + i * CPT + min(CPT, n_my - i * CPT)) * kChunk <= L - p.q_len;
     };
     if (p.early_kv) {
         __syncthreads();  // barrier initialisation is visible to the producer lane
         if (warp == 5 && lane == 0) {
-            // first use of each stage: tiles that end before the new rows
+            // first use of each slot: tiles that end before the new rows
             const uint64_t policy = l2_policy_evict_first();
-            while (issued < min(NS, n_tiles) &&
-                   (c_begin + issued * CPT + min(CPT, n_my - issued * CPT)) * kChunk <= L - p.q_len) {
-                issue_tile(issued, policy);
-                ++issued;
-            }
+            while (issued_k < min(NK, n_tiles) && before_new_rows(issued_k)) issue_tile(issued_k++, 0, policy);
+            while (issued_v < min(NV, n_tiles) && before_new_rows(issued_v)) issue_tile(issued_v++, 1, policy);
         }
         pdl_wait_primary();
     }
@@ -350,50 +360,70 @@ __global__ void __launch_bounds__(6 * 32, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's tensor-memory lanes
 
     // Q block -> tensor memory, the A operand of S = Q K^T: row rho in lane
-    // rho, dims packed two per column; padding rows are zero.
+    // rho, dims packed two per column; padding rows are zero.  The softmax
+    // warps store it while the producer already streams K and V; only the
+    // MMA warp waits for it (named barrier 1: warps 0-4).
     if (warp < 4) {
         const int rho = threadIdx.x;
         const __nv_bfloat16 *qrow =
             p.q + (((size_t)b * p.q_len + rho / G) * p.num_q_heads + kvh * G + rho % G) * D;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-            uint32_t r[32];
+        for (int c0 = 0; c0 < D / 2; c0 += 64) {
+            uint32_t r[2][32];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
+            for (int v = 0; v < 16; ++v) {
                 const uint4 w = rho < R ? *reinterpret_cast<const uint4 *>(qrow + 2 * c0 + 8 * v)
                                         : make_uint4(0u, 0u, 0u, 0u);
-                r[4 * v] = w.x;
-                r[4 * v + 1] = w.y;
-                r[4 * v + 2] = w.z;
-                r[4 * v + 3] = w.w;
+                r[v >> 3][4 * (v & 7)] = w.x;
+                r[v >> 3][4 * (v & 7) + 1] = w.y;
+                r[v >> 3][4 * (v & 7) + 2] = w.z;
+                r[v >> 3][4 * (v & 7) + 3] = w.w;
             }
-            tc::st32(lane_base + C::Q_COL + c0, r);
+            tc::st32(lane_base + C::Q_COL + c0, r[0]);
+            if (c0 + 32 < D / 2) tc::st32(lane_base + C::Q_COL + c0 + 32, r[1]);
         }
         tc::wait_st();
+        tc::fence_before();
+        asm volatile("bar.arrive 1, 160;" ::: "memory");
+    } else if (warp == 4) {
+        asm volatile("bar.sync 1, 160;" ::: "memory");
+        tc::fence_after();
     }
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
 
     if (warp == 5) {
         // ---------------- producer: TMA copies of K and V, 4 chunks per tile ----------------
+        // Two rings refilled independently: the lane probes the next slot of
+        // each without blocking, and within a ring issues tiles in order.
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
-            for (int i = issued; i < n_tiles; ++i) {
-                const int s = i % NS;
-                if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, &flags[0])) {
+            uint32_t idle = 0;
+            while (issued_k < n_tiles || issued_v < n_tiles) {
+                bool progress = false;
+                if (issued_k < n_tiles &&
+                    (issued_k < NK || mbar_test_wait(&k_empty[issued_k % NK], ((issued_k / NK) - 1) & 1))) {
+                    issue_tile(issued_k++, 0, policy);
+                    progress = true;
+                }
+                if (issued_v < n_tiles &&
+                    (issued_v < NV || mbar_test_wait(&v_empty[issued_v % NV], ((issued_v / NV) - 1) & 1))) {
+                    issue_tile(issued_v++, 1, policy);
+                    progress = true;
+                }
+                if (progress) {
+                    idle = 0;
+                } else if (++idle > kWaitPollLimit || flags[0]) {
                     flags[0] = 1;
                     break;
                 }
-                issue_tile(i, policy);
-                issued = i + 1;
             }
             if (flags[0]) {
-                for (int i = max(0, issued - NS); i < issued; ++i) {
-                    uint64_t *bar = &full[i % NS];
-                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(bar, (i / NS) & 1); ++n) {
+                // let the copies in flight land before the CTA ends
+                for (int i = max(0, issued_k - NK); i < issued_k; ++i)
+                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&k_full[i % NK], (i / NK) & 1); ++n) {
                     }
-                }
+                for (int i = max(0, issued_v - NV); i < issued_v; ++i)
+                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&v_full[i % NV], (i / NV) & 1); ++n) {
+                    }
                 set_status(p.status, PA_DEV_TIMEOUT);
             }
         }
@@ -413,10 +443,11 @@ __global__ void __launch_bounds__(6 * 32, 1)
             bool ok = true;
             while (next_pv < n_tiles) {
                 bool progress = false;
-                if (next_pv < next_qk && mbar_test_wait(&p_full[next_pv & 1], (next_pv >> 1) & 1)) {
+                if (next_pv < next_qk && mbar_test_wait(&p_full[next_pv & 1], (next_pv >> 1) & 1) &&
+                    mbar_test_wait(&v_full[next_pv % NV], (next_pv / NV) & 1)) {
                     const int i = next_pv, j = i & 1;
                     tc::fence_after();
-                    const uint32_t v_addr = smem_addr(smem + (i % NS) * C::STAGE_BYTES + C::TILE_BYTES);
+                    const uint32_t v_addr = smem_addr(smem + C::OFF_V + (i % NV) * C::TILE_BYTES);
 #pragma unroll
                     for (int ks = 0; ks < TT / 16; ++ks) {
                         // V: MN-major; 64-dim blocks TT x 128 B apart (LBO), 8-token groups 1 KiB apart (SBO)
@@ -428,16 +459,16 @@ __global__ void __launch_bounds__(6 * 32, 1)
                             tc::mma_bf16_ta(tmem + C::O_COL, a_tm, bdesc, kIdPV, (i > 0 || ks > 0 || h > 0) ? 1u : 0u);
                         }
                     }
-                    tc::commit(&empty[i % NS]);
+                    tc::commit(&v_empty[i % NV]);
                     tc::commit(&o_done[j]);
                     ++next_pv;
                     progress = true;
                 }
                 if (next_qk < n_tiles && next_qk - next_pv < 2) {
-                    const int i = next_qk, s = i % NS, j = i & 1;
-                    if (mbar_test_wait(&full[s], (i / NS) & 1)) {
+                    const int i = next_qk, s = i % NK, j = i & 1;
+                    if (mbar_test_wait(&k_full[s], (i / NK) & 1)) {
                         tc::fence_after();
-                        const uint32_t k_addr = smem_addr(smem + s * C::STAGE_BYTES);
+                        const uint32_t k_addr = smem_addr(smem + s * C::TILE_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             // 16-element k steps: +32 B inside a 128-byte swizzle row, next 64-dim block further on
@@ -445,6 +476,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
                             tc::mma_bf16_ta(tmem + C::S_COL + j * TT, tmem + C::Q_COL + kk * 8,
                                             tc::sdesc(k_addr + koff, 16, 1024, 2), kIdQK, kk > 0 ? 1u : 0u);
                         }
+                        tc::commit(&k_empty[s]);
                         tc::commit(&s_full[j]);
                         ++next_qk;
                         progress = true;
@@ -538,11 +570,11 @@ __global__ void __launch_bounds__(6 * 32, 1)
             // the tensor core, so zero them before the P.V product reads them.
             const int nv = min(TT, t_end - t0);
             if (nv < TT) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&full[i % NS], (i / NS) & 1, &flags[0]))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&v_full[i % NV], (i / NV) & 1, &flags[0]))) {
                     ok = false;
                     break;
                 }
-                uint8_t *vst = smem + (i % NS) * C::STAGE_BYTES + C::TILE_BYTES;
+                uint8_t *vst = smem + C::OFF_V + (i % NV) * C::TILE_BYTES;
                 for (int idx = threadIdx.x; idx < (TT - nv) * C::DB * 8; idx += 128) {
                     const int t = nv + idx / (C::DB * 8), rem = idx % (C::DB * 8);
                     *reinterpret_cast<uint4 *>(vst + (rem >> 3) * (TT * 128) + t * 128 + (rem & 7) * 16) =
