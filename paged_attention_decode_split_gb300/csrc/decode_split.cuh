@@ -235,13 +235,15 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
                 tma_load_4d(st + C::CHUNK_BYTES, &tm_v, &full[s], 0, kvh, off, page, policy);
             };
             if (p.early_kv) {
-                // First use of every stage: the chunks that end before the new
-                // row (token L - 1) go out before the dependency wait.
-                for (int i = 0; i < min(NS, n_my) && (c_begin + i + 1) * kChunk <= L - 1; ++i) {
-                    issue(i % NST, i / NST);
-                    ++next[i % NST];
-                    --remaining;
-                }
+                // First use of every stage: the chunks i < n_pre (those that
+                // end before the new row, token L - 1) go out before the
+                // dependency wait; chunk i is stream i % NST's (i / NST)-th.
+                const int n_pre = max(0, min(min(NS, n_my), (L - 1) / kChunk - c_begin));
+#pragma unroll 1
+                for (int i = 0; i < n_pre; ++i) issue(i % NST, i / NST);
+#pragma unroll
+                for (int c = 0; c < NST; ++c) next[c] = c < n_pre ? (n_pre - c + NST - 1) / NST : 0;
+                remaining -= n_pre;
                 pdl_wait_primary();
             }
             uint32_t idle = 0;
@@ -445,7 +447,14 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
 
     __syncthreads();  // every chunk is consumed: the stage buffers become the merge area
     const bool aborted = flags[0] != 0;
+    // Merge the NWC warp states of this split (same log-sum-exp rule as the
+    // split reduce) and write the split result: the warps store their states,
+    // warp 0 forms the weights 2^(m_w - M) / sum_w l_w 2^(m_w - M) with
+    // shuffles, and every output is a weighted sum over the warps read with
+    // 16-byte shared loads.
     float *merge_acc = reinterpret_cast<float *>(smem);  // [NWC][G][D]
+    float *wgt = reinterpret_cast<float *>(merge_ml + NWC * G);  // [NWC][G] after (m, l)
+    const bool poisoned = aborted || flags[1] != 0;
     if (warp < NWC) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -458,45 +467,54 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
         }
     }
     __syncthreads();
-
-    // Merge the NWC warp states of this split (same log-sum-exp rule as the
-    // split reduce) and write the split result.  The per-(warp, head)
-    // weights 2^(m_w - M) / sum are formed once, then every output element is
-    // a short weighted sum over the warps.
-    const bool poisoned = aborted || flags[1] != 0;
-    float *wgt = reinterpret_cast<float *>(merge_ml + NWC * G);  // [NWC][G] after (m, l)
-    if (threadIdx.x < G) {
-        const int g = threadIdx.x;
-        float M = -INFINITY;
+    if (warp == 0) {
+        // lane groups of NWP >= NWC lanes, one group per head; surplus lanes hold empty states
+        constexpr int NWP = NWC <= 8 ? 8 : (NWC <= 16 ? 16 : 32);
+        static_assert(NWC <= 32, "warp states fit one warp");
+        constexpr int HPP = 32 / NWP;  // heads per pass
 #pragma unroll
-        for (int w = 0; w < NWC; ++w) M = fmaxf(M, merge_ml[w * G + g].x);
-        float lsum = 0.f;
+        for (int g0 = 0; g0 < G; g0 += HPP) {
+            const int w = lane % NWP, g = g0 + lane / NWP;
+            const bool mine = w < NWC && g < G;
+            const float2 ml = mine ? merge_ml[w * G + g] : make_float2(-INFINITY, 0.f);
+            float M = ml.x;
 #pragma unroll
-        for (int w = 0; w < NWC; ++w) {
-            const float2 ml = merge_ml[w * G + g];
-            const float e = fast_exp2(ml.x - M);  // 0 for a warp without rows (m = -inf)
-            lsum = fmaf(ml.y, e, lsum);
-            wgt[w * G + g] = e;
+            for (int o = 1; o < NWP; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float e = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;  // 0 for a warp without rows
+            float lsum = ml.y * e;
+#pragma unroll
+            for (int o = 1; o < NWP; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+            const bool zero = poisoned || !(lsum > 0.f);
+            if (mine) {
+                wgt[w * G + g] = zero ? 0.f : e / lsum;
+                if (w == 0 && p.num_splits > 1)
+                    p.part_ml[((size_t)b * p.num_q_heads + hq0 + g) * p.num_splits + split] =
+                        make_float2(M, poisoned ? -1.f : lsum);
+            }
         }
-        const bool zero = poisoned || !(lsum > 0.f);
-        const float inv = zero ? 0.f : 1.f / lsum;
-#pragma unroll
-        for (int w = 0; w < NWC; ++w) wgt[w * G + g] *= inv;
-        if (p.num_splits > 1)
-            p.part_ml[((size_t)b * p.num_q_heads + hq0 + g) * p.num_splits + split] =
-                make_float2(M, poisoned ? -1.f : lsum);
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < G * D; idx += C::THREADS) {
-        const int g = idx / D, d = idx - (idx / D) * D;
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < NWC; ++w) o = fmaf(merge_acc[(w * G + g) * D + d], wgt[w * G + g], o);
+    for (int idx = threadIdx.x; idx < G * D / 4; idx += C::THREADS) {
+        const int g = (4 * idx) / D, d = 4 * idx - g * D;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+        for (int w = 0; w < NWC; ++w) {
+            const float4 x = *reinterpret_cast<const float4 *>(merge_acc + w * G * D + 4 * idx);
+            const float wg = wgt[w * G + g];
+            o.x = fmaf(x.x, wg, o.x);
+            o.y = fmaf(x.y, wg, o.y);
+            o.z = fmaf(x.z, wg, o.z);
+            o.w = fmaf(x.w, wg, o.w);
+        }
         const size_t row = (size_t)b * p.num_q_heads + hq0 + g;
-        if (p.num_splits == 1)
-            store_out(p.out, row * D + d, o, p.out_bf16);
-        else
-            p.part_o[(row * p.num_splits + split) * D + d] = o;
+        if (p.num_splits == 1) {
+            store_out(p.out, row * D + d, o.x, p.out_bf16);
+            store_out(p.out, row * D + d + 1, o.y, p.out_bf16);
+            store_out(p.out, row * D + d + 2, o.z, p.out_bf16);
+            store_out(p.out, row * D + d + 3, o.w, p.out_bf16);
+        } else {
+            *reinterpret_cast<float4 *>(p.part_o + (row * p.num_splits + split) * D + d) = o;
+        }
     }
 }
 
@@ -549,16 +567,14 @@ __global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams
         float2 v[UNROLL];
         float4 o[UNROLL];
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {  // all loads first
-            const int i = i0 + u * SG;
-            if (i < S_b) {
-                v[u] = ml[i];
-                o[u] = *reinterpret_cast<const float4 *>(po + (size_t)i * D);
-            } else {
-                v[u] = make_float2(-INFINITY, 0.f);
-                o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        for (int u = 0; u < UNROLL; ++u) {  // all loads first, none behind a branch
+            const int i = min(i0 + u * SG, S_b - 1);
+            v[u] = ml[i];
+            o[u] = *reinterpret_cast<const float4 *>(po + (size_t)i * D);
         }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (i0 + u * SG >= S_b) v[u] = make_float2(-INFINITY, 0.f);  // a repeated load: ignore it
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             bad |= v[u].y < 0.f;
@@ -619,12 +635,11 @@ __global__ void __launch_bounds__(256) pa_split_reduce_small_kernel(const Reduce
     float2 v[kReduceSmallMaxSplits];
     float4 o[kReduceSmallMaxSplits][E / 4];
 #pragma unroll
-    for (int u = 0; u < kReduceSmallMaxSplits; ++u) {  // all loads first
-        if (u < S) {
-            v[u] = ml[u];
+    for (int u = 0; u < kReduceSmallMaxSplits; ++u) {  // all loads first, none behind a branch
+        const int i = min(u, S - 1);
+        v[u] = ml[i];
 #pragma unroll
-            for (int e = 0; e < E / 4; ++e) o[u][e] = *reinterpret_cast<const float4 *>(po + (size_t)u * D + 4 * e);
-        }
+        for (int e = 0; e < E / 4; ++e) o[u][e] = *reinterpret_cast<const float4 *>(po + (size_t)i * D + 4 * e);
     }
     float M = -INFINITY, W = 0.f;
     float4 a[E / 4];
