@@ -14,8 +14,18 @@ cudaError_t launch_verify_tc(const CUtensorMap &tk, const CUtensorMap &tv, const
     auto kern = pa_verify_tc_kernel<D, NK, NV>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, tk64, tv64, p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the set-up overlaps the work before it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, tk64, tv64, p);
 }
 
 }  // namespace
