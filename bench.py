@@ -451,7 +451,8 @@ def _layers_beyond_l2(bytes_per_layer, minimum, l2_bytes=256 << 20):
     return max(minimum, -(-l2_bytes // max(1, bytes_per_layer)))
 
 
-SECONDARY = ("decode_l512_bs16", "context_sweep", "batch32_uniform_bs784", "verify_b8_q16_l8192_bs832")
+SECONDARY = ("decode_l512_bs16", "context_sweep", "batch32_uniform_bs784", "verify_b8_q16_l8192_bs832",
+             "prefill_q2048_l16384_bs832")
 
 
 def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
@@ -468,6 +469,8 @@ def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
         _batch32(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "verify_b8_q16_l8192_bs832" in names:
         _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem)
+    if "prefill_q2048_l16384_bs832" in names:
+        _prefill(pa, dev, stream, res, WORKLOADS, make_problem)
     return res
 
 
@@ -539,10 +542,43 @@ def _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem):
     calls = _attention_calls(pa, prob, dev)
     us = _time_graph(calls, stream, 100) * 1e3 / len(calls)
     kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER
-    flops = sum(4 * 256 * 24 * (int(L) - 16 + r + 1) for L in prob.seq_lens.tolist() for r in range(16))
+    flops = _causal_flops(prob)
     res["verify_b8_q16_l8192_bs832"] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
                                         "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak,
                                         "TFLOPs": flops / (us * 1e-6) / 1e12, "plan": pa.last_plan()}
+
+
+def _causal_flops(prob):
+    """Useful flops of a q_len-row call: 4 D per (row, head, visible key)."""
+    total = 0
+    for L in prob.seq_lens.tolist():
+        q = prob.q_len
+        total += prob.num_q_heads * 4 * prob.head_dim * (q * (int(L) - q) + q * (q + 1) // 2)
+    return total
+
+
+def _prefill(pa, dev, stream, res, WORKLOADS, make_problem):
+    # Chunked-prefill step: 2048 new rows of one sequence (L = 16384) on the
+    # tensor cores, 96 row blocks per KV head, each reading only the keys its
+    # rows can see.  Compute-bound: reported against the bf16 tensor peak.
+    prob = make_problem(1006, **dict(WORKLOADS["prefill_q2048_l16384_bs832"], num_layers=2), device=dev)
+    calls = _attention_calls(pa, prob, dev)
+    us = _time_graph(calls, stream, 20) * 1e3 / len(calls)
+    flops = _causal_flops(prob)
+    tf_peak = load_tensor_peak()
+    res["prefill_q2048_l16384_bs832"] = {
+        "us_per_call": us, "TFLOPs": flops / (us * 1e-6) / 1e12, "useful_flops": flops,
+        "bf16_peak_TFLOPs": tf_peak, "frac_of_bf16_peak": flops / (us * 1e-6) / 1e12 / tf_peak,
+        "note": "useful flops (4 D per row, head and visible key); the kernel also runs the P residual MMA "
+                "and pads each 128-row block's causal edge", "plan": pa.last_plan()}
+
+
+def load_tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
 
 
 def only_workload(args):

@@ -175,9 +175,13 @@ pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const vo
  * them (speculative verify).  Rows are ordered (sequence, new row): q and out
  * are [B * q_len, Hq, D].  Row r (0-based) of sequence b attends to keys
  * 0 .. L_b - q_len + r inclusive; the q_len new rows must already be in the
- * cache (L_b >= q_len, else PA_DEV_BAD_SEQLEN and zero rows).  All G * q_len
- * rows of one KV head share every K/V tile on the tensor cores.  Supported:
- * G * q_len <= 128.  Other arguments as for decode. */
+ * cache (L_b >= q_len, else PA_DEV_BAD_SEQLEN and zero rows).  The G * q_len
+ * rows of one KV head are processed in blocks of 128 that share every K/V tile
+ * on the tensor cores; a block reads only the keys its last row can see, so a
+ * large q_len (a chunked-prefill step) skips the masked upper triangle tile by
+ * tile.  Supported:
+ * G * q_len <= 32768 and num_kv_heads * ceil(G * q_len / 128) <= 65535.  Other
+ * arguments as for decode. */
 pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const void *v_cache,
                                     const int32_t *block_table, const int32_t *seq_lens,
                                     const pa_attn_desc *desc, void *out, void *workspace,

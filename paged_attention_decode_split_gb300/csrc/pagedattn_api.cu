@@ -69,8 +69,12 @@ pa_status check_desc(const pa_attn_desc *d, bool verify) {
     const int64_t need_pages = (static_cast<int64_t>(d->max_seq_len) + d->block_size - 1) / d->block_size;
     if (need_pages > d->max_pages_per_seq) return PA_ERR_INVALID_ARG;
     if (d->num_pages > INT32_MAX) return PA_ERR_UNSUPPORTED;  // TMA coordinates are 32-bit
-    // grid.z = num_seqs (split kernels), grid.y = num_seqs * q_len (reduce), grid.y = Hkv
+    // grid.z = num_seqs (split kernels), grid.y = num_seqs * q_len (reduce), grid.y = Hkv x row blocks
     if (static_cast<int64_t>(d->num_seqs) * d->q_len > 65535 || d->num_kv_heads > 65535)
+        return PA_ERR_UNSUPPORTED;
+    if (verify && static_cast<int64_t>(d->num_kv_heads) *
+                          ((static_cast<int64_t>(d->q_len) * (d->num_q_heads / d->num_kv_heads) + 127) / 128) >
+                      65535)
         return PA_ERR_UNSUPPORTED;
     if (d->block_size % kChunk != 0) return PA_ERR_UNSUPPORTED;
     const int group = d->num_q_heads / d->num_kv_heads;
@@ -88,7 +92,10 @@ pa_status make_plan(const pa_attn_desc *d, bool verify, Plan *pl) {
     int sms = d->num_sms;
     if (sms <= 0 && device_sm_count(&sms) != 0) return PA_ERR_CUDA;
     const int n_chunks = (d->max_seq_len + kChunk - 1) / kChunk;
-    const int64_t units = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads;
+    // verify: each (sequence, KV head) unit has ceil(q_len G / 128) row blocks of its own
+    const int64_t row_blocks =
+        verify ? (static_cast<int64_t>(d->q_len) * (d->num_q_heads / d->num_kv_heads) + 127) / 128 : 1;
+    const int64_t units = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * row_blocks;
     int splits;
     if (d->num_splits > 0) {
         splits = d->num_splits;
@@ -99,7 +106,9 @@ pa_status make_plan(const pa_attn_desc *d, bool verify, Plan *pl) {
         // never spills a few CTAs into a second wave
         splits = static_cast<int>(std::max<int64_t>(1, sms / units));
         splits = std::min(splits, std::max(1, n_chunks / kMinChunksPerSplit));
-        splits = std::max(splits, (n_chunks + kMaxChunksPerSplit - 1) / kMaxChunksPerSplit);
+        // long contexts are cut further to bound the longest CTA -- unless the
+        // units alone already fill the SMs (a verify with many row blocks)
+        if (units < sms) splits = std::max(splits, (n_chunks + kMaxChunksPerSplit - 1) / kMaxChunksPerSplit);
     }
     splits = std::max(1, std::min(splits, std::max(1, n_chunks)));
     int cps = std::max(1, (n_chunks + splits - 1) / splits);
@@ -411,9 +420,11 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
     p.scale_log2 = desc->scale * 1.4426950408889634f;
     p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
     p.early_kv = (desc->flags & PA_FLAG_EARLY_KV_READ) != 0;
+    p.num_kv_heads = desc->num_kv_heads;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);
+    const int row_blocks = (desc->q_len * group + 127) / 128;
+    const dim3 grid(pl.num_splits, desc->num_kv_heads * row_blocks, desc->num_seqs);
     if (launch_verify(desc->head_dim, desc->q_len * group, tk, tv, tk64, tv64, p, grid, s) != cudaSuccess)
         return PA_ERR_CUDA;
     if (pl.num_splits > 1) {
@@ -427,7 +438,7 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
         if (launch_reduce(desc->head_dim, r, desc->num_seqs * desc->q_len, s) != cudaSuccess)
             return PA_ERR_CUDA;
     }
-    record_plan(PA_PATH_VERIFY_TCGEN05, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
+    record_plan(PA_PATH_VERIFY_TCGEN05, pl, desc, pl.num_splits * desc->num_kv_heads * row_blocks * desc->num_seqs);
     return PA_OK;
 }
 

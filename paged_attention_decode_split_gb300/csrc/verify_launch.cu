@@ -30,14 +30,16 @@ cudaError_t launch_verify_tc(const CUtensorMap &tk, const CUtensorMap &tv, const
 
 }  // namespace
 
+// Rows beyond 128 run as several 128-row blocks (grid y = Hkv x blocks), up
+// to q_len 4096 x G 8 = 32768 rows.
 bool verify_supported(int head_dim, int rows) {
-    return (head_dim == 256 || head_dim == 128) && rows >= 1 && rows <= 128;
+    return (head_dim == 256 || head_dim == 128) && rows >= 1 && rows <= 32768;
 }
 
 cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const CUtensorMap &tv,
                           const CUtensorMap &tk64, const CUtensorMap &tv64, const VerifyParams &p, dim3 grid,
                           cudaStream_t stream) {
-    (void)rows;  // every row count up to 128 runs as one M = 128 block
+    (void)rows;  // each CTA runs one M = 128 block of rows
     if (head_dim == 256) return launch_verify_tc<256, 4, 3>(tk, tv, tk64, tv64, p, grid, stream, 32);
     if (head_dim == 128) return launch_verify_tc<128, 6, 6>(tk, tv, tk64, tv64, p, grid, stream, 33);
     return cudaErrorInvalidValue;

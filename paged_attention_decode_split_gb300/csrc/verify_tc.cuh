@@ -63,6 +63,7 @@ struct VerifyParams {
     float scale_log2;
     int out_bf16;
     int early_kv;  // stream the context before the new rows ahead of the dependency wait
+    int num_kv_heads;  // grid y = num_kv_heads x 128-row blocks
 };
 
 // Byte offset of 16-byte column chunk c of row t in a [D/64][rows][128 B]
@@ -233,9 +234,11 @@ __global__ void __launch_bounds__(6 * 32, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::OFF_FLAGS);  // [0] abort, [1] bad page
 
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, b = blockIdx.z;
+    const int kvh = blockIdx.y % p.num_kv_heads;
+    const int row0 = (blockIdx.y / p.num_kv_heads) * C::M;  // first row (rho = r G + g) of this block
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = p.group, R = p.q_len * G;
+    const int G = p.group, R = min(C::M, p.q_len * G - row0);  // rows of this block
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -276,19 +279,21 @@ __global__ void __launch_bounds__(6 * 32, 1)
     }
     const int n_chunks = (L + kChunk - 1) / kChunk;
     const int c_begin = split * p.chunks_per_split;
-    const int n_my = min(n_chunks - c_begin, p.chunks_per_split);
+    // keys past the block's last row's causal limit are never read
+    const int k_last = L - p.q_len + (row0 + R - 1) / G;
+    const int n_my = min(min(n_chunks, k_last / kChunk + 1) - c_begin, p.chunks_per_split);
     if (n_my <= 0) {
         // No key of this sequence in this split: an empty record (m = -inf,
         // l = 0) for the reduce, or zero rows when the call is unsplit.
         if (p.early_kv) pdl_wait_primary();
         if (p.num_splits == 1) {
             for (int idx = threadIdx.x; idx < R * D; idx += C::THREADS) {
-                const int rho = idx / D, d = idx - rho * D;
+                const int rho = row0 + idx / D, d = idx % D;
                 const size_t row = (size_t)b * p.q_len + rho / G;
                 store_out(p.out, (row * p.num_q_heads + kvh * G + rho % G) * D + d, 0.f, p.out_bf16);
             }
         } else {
-            for (int rho = threadIdx.x; rho < R; rho += C::THREADS) {
+            for (int rho = row0 + threadIdx.x; rho < row0 + R; rho += C::THREADS) {
                 const size_t row = (size_t)b * p.q_len + rho / G;
                 p.part_ml[(row * p.num_q_heads + kvh * G + rho % G) * p.num_splits + split] =
                     make_float2(-INFINITY, 0.f);
@@ -364,7 +369,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
     // warps store it while the producer already streams K and V; only the
     // MMA warp waits for it (named barrier 1: warps 0-4).
     if (warp < 4) {
-        const int rho = threadIdx.x;
+        const int rho = row0 + threadIdx.x;  // rows past R are zero padding
         const __nv_bfloat16 *qrow =
             p.q + (((size_t)b * p.q_len + rho / G) * p.num_q_heads + kvh * G + rho % G) * D;
 #pragma unroll 1
@@ -372,8 +377,8 @@ __global__ void __launch_bounds__(6 * 32, 1)
             uint32_t r[2][32];
 #pragma unroll
             for (int v = 0; v < 16; ++v) {
-                const uint4 w = rho < R ? *reinterpret_cast<const uint4 *>(qrow + 2 * c0 + 8 * v)
-                                        : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 w = (int)threadIdx.x < R ? *reinterpret_cast<const uint4 *>(qrow + 2 * c0 + 8 * v)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
                 r[v >> 3][4 * (v & 7)] = w.x;
                 r[v >> 3][4 * (v & 7) + 1] = w.y;
                 r[v >> 3][4 * (v & 7) + 2] = w.z;
@@ -501,8 +506,8 @@ __global__ void __launch_bounds__(6 * 32, 1)
         }
     } else {
         // ---------------- softmax: thread = query row = tensor-memory lane ----------------
-        const int rho = threadIdx.x;  // 0..127
-        const bool live = rho < R;
+        const int rho = row0 + threadIdx.x;  // this thread's row (tensor-memory lane threadIdx.x)
+        const bool live = (int)threadIdx.x < R;
         // last visible key: the causal limit of the row, and never past this
         // split's last chunk (a tile may reach into the next split's tokens)
         const int t_end = min(L, (c_begin + n_my) * kChunk);

@@ -121,9 +121,19 @@ def test_empty_batch_is_a_noop(lib):
                                          None, None) == pa.PA_OK
 
 
+def test_verify_row_blocks_plan(lib):
+    # 2048 rows x 6 heads = 96 blocks of 128 rows per KV head: 384 CTAs fill the
+    # SMs without splitting the context, so no workspace is needed
+    prefill = hybrid_desc(q_len=2048, block_size=832, max_pages_per_seq=20, max_seq_len=16384, num_pages=22)
+    assert pa.workspace_bytes(prefill) == 0
+    # a 16-row verify of 8 sequences splits each (sequence, KV head) context 4 ways
+    small = hybrid_desc(num_seqs=8, q_len=16, block_size=832, max_pages_per_seq=10, max_seq_len=8208, num_pages=88)
+    assert pa.workspace_bytes(small) == ((8 * 16 * 24 * 4 * 256 * 4 + 255) // 256 * 256) + 8 * 16 * 24 * 4 * 8
+
+
 def test_verify_rejects_bad_descriptions(lib):
     call = lib.pa_paged_attention_verify
-    too_many_rows = hybrid_desc(q_len=32)  # 32 * 6 = 192 rows > 128
+    too_many_rows = hybrid_desc(q_len=8192, max_seq_len=16384, max_pages_per_seq=21, num_pages=22)  # 49152 rows
     assert call(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(too_many_rows), FAKE, FAKE, 1 << 30, None,
                 None) == pa.PA_ERR_UNSUPPORTED
     bad_dim = hybrid_desc(q_len=16, head_dim=96)

@@ -240,6 +240,27 @@ def test_verify_dense_shape_d128(oracle_mod, splits):
     assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what="verify d128")
 
 
+@pytest.mark.parametrize("q_len,lens,bs,splits", [(48, [1000, 48], 784, 0), (48, [1000, 300], 16, 3),
+                                                  (512, [2048], 832, 0), (200, [200, 1500], 784, 0)])
+def test_verify_row_blocks(oracle_mod, q_len, lens, bs, splits):
+    """More than 128 rows (q_len x 6 heads): blocks of 128 rows, the last one
+    partial, each reading only the keys its rows can see (chunked prefill)."""
+    prob = hybrid(151 + q_len, lens, bs, q_len=q_len, poison_unused=True)
+    write_new_rows(prob, 13)
+    out, status, plan = run_attention(prob, num_splits=splits)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"verify rows q_len={q_len}")
+
+
+def test_verify_row_blocks_d128(oracle_mod):
+    prob = make_problem(161, num_seqs=1, seq_lens=[900], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, q_len=300, scale=1 / math.sqrt(128), poison_unused=True)
+    write_new_rows(prob, 17)
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what="verify rows d128")
+
+
 def test_verify_short_context_sets_status():
     prob = hybrid(131, [40, 40], 16, q_len=16)
     q, kc, vc, bt, sl = to_dev(prob)
