@@ -61,6 +61,8 @@ def _load():
                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_double]
             lib.oracle_paged_attention.restype = ctypes.c_int
             lib.oracle_paged_attention.argtypes = common + [_f64p, ctypes.c_int]
+            lib.oracle_paged_attention_window.restype = ctypes.c_int
+            lib.oracle_paged_attention_window.argtypes = common + [ctypes.c_int64, _f64p, ctypes.c_int]
             lib.oracle_attention_partial.restype = ctypes.c_int
             lib.oracle_attention_partial.argtypes = common + [
                 ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _f64p, _f64p, _f64p]
@@ -122,13 +124,17 @@ def _problem(q, k_cache, v_cache, block_table, seq_lens, scale, q_len):
 
 
 def paged_attention(q, k_cache, v_cache, block_table, seq_lens, scale: float, q_len: int = 1,
-                    num_threads: int | None = None) -> np.ndarray:
-    """Exact softmax attention through the block table; returns float64 [rows, Hq, D]."""
+                    num_threads: int | None = None, window: int = 0) -> np.ndarray:
+    """Exact softmax attention through the block table; returns float64 [rows, Hq, D].
+    window > 0: each row sees only its last `window` visible keys (sliding window)."""
     keep, args, shape = _problem(q, k_cache, v_cache, block_table, seq_lens, scale, q_len)
     out = np.zeros(shape, dtype=np.float64)
     if num_threads is None:
         num_threads = os.cpu_count() or 1
-    rc = _load().oracle_paged_attention(*args, _ptr(out, _f64p), int(num_threads))
+    if window:
+        rc = _load().oracle_paged_attention_window(*args, int(window), _ptr(out, _f64p), int(num_threads))
+    else:
+        rc = _load().oracle_paged_attention(*args, _ptr(out, _f64p), int(num_threads))
     del keep
     if rc != 0:
         raise ValueError(f"oracle_paged_attention failed ({rc})")

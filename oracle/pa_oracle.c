@@ -29,8 +29,11 @@
  *   - seq_lens[b] counts every cached token of sequence b, including the q_len
  *     rows just written; row r (0-based) of a q_len-row block sees keys
  *     0 .. seq_lens[b] - q_len + r inclusive;
- *   - plain softmax: no sliding window, ALiBi, sinks or soft-cap (the DCU page
- *     lists those as excluded conditions, Sec.6);
+ *   - plain softmax: no ALiBi, sinks or soft-cap (the DCU page lists those as
+ *     excluded conditions, Sec.6);
+ *   - sliding window (the RTX 3090 page's 2048-position window): with window
+ *     W > 0 a row sees only its last W visible keys, i.e. keys
+ *     (last visible key - W, last visible key]; W = 0 means no window;
  *   - a row that sees no key returns zeros;
  *   - a negative slot in reshape_and_cache is a padding slot and is skipped.
  *
@@ -105,6 +108,7 @@ typedef struct {
     int num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_pages_per_seq;
     int64_t num_pages;
     double scale;
+    int64_t window; /* 0: none; W > 0: each row sees only its last W visible keys */
 } problem;
 
 /* Number of keys query row r of sequence b may attend to (causal rule). */
@@ -136,6 +140,8 @@ static int attend_range(const problem *p, int64_t row, int h, int64_t t_begin, i
         t_end = n;
     if (t_begin < 0)
         t_begin = 0;
+    if (p->window > 0 && t_begin < n - p->window)
+        t_begin = n - p->window; /* the sliding window's first key */
     for (int d = 0; d < D; ++d)
         o[d] = 0.0;
     if (t_begin >= t_end) {
@@ -232,15 +238,35 @@ static void *attention_worker(void *varg)
  * the keys the row may see.  Rows are ordered (sequence, new-row), i.e. row =
  * b * q_len + r.  q_len == 1 is plain decode; q_len > 1 is the verify variant.
  * Work is spread over num_threads POSIX threads by (row, head) item. */
+int oracle_paged_attention_window(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                  const int32_t *block_table, const int32_t *seq_lens,
+                                  int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int max_pages_per_seq,
+                                  int64_t num_pages, double scale, int64_t window, double *out,
+                                  int num_threads);
+
 int oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                            const int32_t *block_table, const int32_t *seq_lens,
                            int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
                            int head_dim, int block_size, int max_pages_per_seq,
                            int64_t num_pages, double scale, double *out, int num_threads)
 {
+    return oracle_paged_attention_window(q, k_cache, v_cache, block_table, seq_lens, num_seqs, q_len,
+                                         num_q_heads, num_kv_heads, head_dim, block_size, max_pages_per_seq,
+                                         num_pages, scale, 0, out, num_threads);
+}
+
+/* The same with a sliding window of W keys per row (W = 0: none). */
+int oracle_paged_attention_window(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                  const int32_t *block_table, const int32_t *seq_lens,
+                                  int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int max_pages_per_seq,
+                                  int64_t num_pages, double scale, int64_t window, double *out,
+                                  int num_threads)
+{
     problem p = {q, k_cache, v_cache, block_table, seq_lens, num_seqs, q_len, num_q_heads,
-                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale};
-    if (!out || check_problem(&p) != 0)
+                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale, window};
+    if (!out || check_problem(&p) != 0 || window < 0)
         return -1;
     if (num_threads < 1)
         num_threads = 1;
@@ -285,7 +311,7 @@ int oracle_attention_partial(const uint16_t *q, const uint16_t *k_cache, const u
                              int64_t t_begin, int64_t t_end, double *o, double *m, double *l)
 {
     problem p = {q, k_cache, v_cache, block_table, seq_lens, num_seqs, q_len, num_q_heads,
-                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale};
+                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale, 0};
     if (!o || !m || !l || check_problem(&p) != 0)
         return -1;
     if (row < 0 || row >= (int64_t)num_seqs * q_len || head < 0 || head >= num_q_heads)

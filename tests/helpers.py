@@ -42,9 +42,11 @@ def place_in_pages(k_list, v_list, block_size: int, num_pages: int, seed: int, f
     return k_cache, v_cache, bt
 
 
-def dense_attention(q, k_list, v_list, scale: float, q_len: int, num_kv_heads: int) -> torch.Tensor:
+def dense_attention(q, k_list, v_list, scale: float, q_len: int, num_kv_heads: int,
+                    window: int = 0) -> torch.Tensor:
     """torch fp64 softmax(Q K^T scale) V per sequence with the causal rule for
-    the q_len new rows; query head h uses KV head h // (Hq / Hkv)."""
+    the q_len new rows; query head h uses KV head h // (Hq / Hkv).  window > 0
+    keeps only each row's last `window` visible keys."""
     rows, hq, d = q.shape
     g = hq // num_kv_heads
     out = torch.zeros(rows, hq, d, dtype=torch.float64)
@@ -56,11 +58,12 @@ def dense_attention(q, k_list, v_list, scale: float, q_len: int, num_kv_heads: i
             n = L - q_len + r + 1
             if n <= 0:
                 continue
+            a = max(0, n - window) if window > 0 else 0
             qr = q[b * q_len + r].double()  # [Hq, D]
             for h in range(hq):
-                s = (kf[:n, h // g, :] @ qr[h]) * scale
+                s = (kf[a:n, h // g, :] @ qr[h]) * scale
                 p = torch.softmax(s, dim=0)
-                out[b * q_len + r, h] = p @ vf[:n, h // g, :]
+                out[b * q_len + r, h] = p @ vf[a:n, h // g, :]
     return out
 
 

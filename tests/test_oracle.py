@@ -17,10 +17,10 @@ from tests.helpers import bits, dense_attention, place_in_pages, randn_bf16
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def _run(oracle_mod, q, k_cache, v_cache, bt, seq_lens, scale, q_len=1, threads=4):
+def _run(oracle_mod, q, k_cache, v_cache, bt, seq_lens, scale, q_len=1, threads=4, window=0):
     return oracle_mod.paged_attention(bits(q), bits(k_cache), bits(v_cache), bt.numpy(),
                                       np.asarray(seq_lens, dtype=np.int32), scale, q_len=q_len,
-                                      num_threads=threads)
+                                      num_threads=threads, window=window)
 
 
 def _contig(gen, lens, hkv, d):
@@ -276,6 +276,60 @@ def test_split_then_reduce_equals_whole(oracle_mod):
         o = np.stack([p[0] for p in parts])
         merged = oracle_mod.lse_combine(o, np.array([p[1] for p in parts]), np.array([p[2] for p in parts]))
         np.testing.assert_allclose(merged, full[0, 1], rtol=1e-12, atol=1e-14)
+
+
+# -- sliding window ("last 2048 positions" of the RTX 3090 page) ------------------------
+
+def _window_problem(seed, lens, q_len, hq=6, hkv=2, d=16, bs=16):
+    gen = torch.Generator().manual_seed(seed)
+    k, v = _contig(gen, lens, hkv, d)
+    q = randn_bf16((len(lens) * q_len, hq, d), gen)
+    pages = sum(math.ceil(L / bs) for L in lens) + 1
+    kc, vc, bt = place_in_pages(k, v, bs, pages, seed=seed + 1)
+    return k, v, q, kc, vc, bt
+
+
+@pytest.mark.parametrize("q_len", [1, 5])
+def test_window_wider_than_context_is_full_attention_bitwise(oracle_mod, q_len):
+    lens = [40, 77, 5]
+    k, v, q, kc, vc, bt = _window_problem(31, lens, q_len)
+    full = _run(oracle_mod, q, kc, vc, bt, lens, 0.25, q_len=q_len)
+    for w in (77, 78, 10**6):
+        assert np.array_equal(_run(oracle_mod, q, kc, vc, bt, lens, 0.25, q_len=q_len, window=w), full)
+
+
+@pytest.mark.parametrize("q_len", [1, 5])
+def test_window_of_one_returns_the_last_visible_v(oracle_mod, q_len):
+    lens = [40, 77, 9]
+    k, v, q, kc, vc, bt = _window_problem(32, lens, q_len)
+    out = _run(oracle_mod, q, kc, vc, bt, lens, 0.25, q_len=q_len, window=1)
+    for b, L in enumerate(lens):
+        for r in range(q_len):
+            t = L - q_len + r  # the row's own (last visible) key
+            for h in range(6):
+                np.testing.assert_array_equal(out[b * q_len + r, h], v[b][t, h // 3].double().numpy())
+
+
+@pytest.mark.parametrize("lens,q_len,window", [([200, 37], 1, 16), ([200, 37], 1, 50), ([150], 7, 33),
+                                               ([64, 90], 4, 17)])
+def test_window_bruteforce_dense_softmax(oracle_mod, lens, q_len, window):
+    k, v, q, kc, vc, bt = _window_problem(33 + window, lens, q_len)
+    out = _run(oracle_mod, q, kc, vc, bt, lens, 0.25, q_len=q_len, window=window)
+    ref = dense_attention(q, k, v, 0.25, q_len, 2, window=window).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+    # a wrong window edge (one key more or less) would be caught at this tolerance
+    assert not np.allclose(out, dense_attention(q, k, v, 0.25, q_len, 2, window=window + 1).numpy(),
+                           rtol=1e-9, atol=1e-9)
+
+
+def test_window_equals_the_split_over_its_keys_bitwise(oracle_mod):
+    lens, W = [500], 64
+    k, v, q, kc, vc, bt = _window_problem(34, lens, 1)
+    out = _run(oracle_mod, q, kc, vc, bt, lens, 0.3, window=W)
+    for h in range(6):
+        o, m, l = oracle_mod.attention_partial(bits(q), bits(kc), bits(vc), bt.numpy(), np.array(lens, np.int32),
+                                               0.3, 0, h, lens[0] - W, lens[0])
+        assert np.array_equal(out[0, h], o)
 
 
 # -- reshape_and_cache --------------------------------------------------------------
