@@ -59,7 +59,7 @@ def load_peaks():
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_attention_decode_split_gb300", "csrc")
-    for name in ("pa_device.cuh", "decode_split.cuh", "decode_launch.cu"):
+    for name in ("pa_device.cuh", "decode_split.cuh", "decode_launch.cuh", "decode_launch.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

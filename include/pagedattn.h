@@ -75,6 +75,9 @@ typedef enum { PA_OUT_F32 = 0, PA_OUT_BF16 = 1 } pa_out_dtype;
  *   num_splits        0 = automatic; > 0 forces the split count (benchmarks, tests)
  *   num_sms           0 = query the current device; > 0 plans for that SM count
  *   flags             0, or PA_FLAG_EARLY_KV_READ (below)
+ *   window            0 = full attention; W > 0 = sliding window: every query
+ *                     row sees only its last W visible keys (its own position
+ *                     included), as the RTX 3090 page's 2048-position window
  */
 typedef struct {
     int32_t num_seqs;
@@ -91,6 +94,7 @@ typedef struct {
     int32_t num_splits;
     int32_t num_sms;
     int32_t flags;
+    int32_t window;
 } pa_attn_desc;
 
 /* desc->flags bits.

@@ -40,7 +40,7 @@ class AttnDesc(ctypes.Structure):
         ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("max_pages_per_seq", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("num_pages", ctypes.c_int64),
         ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int32), ("num_splits", ctypes.c_int32),
-        ("num_sms", ctypes.c_int32), ("flags", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32), ("flags", ctypes.c_int32), ("window", ctypes.c_int32),
     ]
 
 
@@ -100,9 +100,10 @@ def status_string(status: int) -> str:
 
 def make_desc(*, num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
               max_pages_per_seq: int, max_seq_len: int, num_pages: int, scale: float, q_len: int = 1,
-              out_dtype: int = PA_OUT_F32, num_splits: int = 0, num_sms: int = 0, flags: int = 0) -> AttnDesc:
+              out_dtype: int = PA_OUT_F32, num_splits: int = 0, num_sms: int = 0, flags: int = 0,
+              window: int = 0) -> AttnDesc:
     return AttnDesc(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_pages_per_seq,
-                    max_seq_len, num_pages, scale, out_dtype, num_splits, num_sms, flags)
+                    max_seq_len, num_pages, scale, out_dtype, num_splits, num_sms, flags, window)
 
 
 def workspace_bytes(desc: AttnDesc) -> int:

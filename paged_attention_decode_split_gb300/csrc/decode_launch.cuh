@@ -1,0 +1,66 @@
+// decode_launch.cuh -- the decode kernel instantiations per (head_dim, GQA
+// group), shared by the full-attention and the sliding-window translation
+// units (compiled in parallel).
+#pragma once
+
+#include "pa_internal.h"
+
+namespace pa {
+
+template <int D, int G, int TS, int NST, int SPS, bool WIN>
+cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, dim3 grid,
+                            cudaStream_t stream, int slot) {
+    using C = DecodeCfg<D, G, TS, NST, SPS>;
+    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS, WIN>;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
+    if (e != cudaSuccess) return e;
+    // Programmatic dependent launch: the kernel's set-up overlaps the previous
+    // kernel in the stream (e.g. reshape_and_cache); it waits for that kernel
+    // before touching global memory.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+// Per (head_dim, group): warps per chunk (TS), chunk streams (NST), stages
+// per stream (SPS).  D = 256: groups of 4 and 6 heads run 4 streams x 3
+// stages x 16 KiB with each chunk's tokens split over 2 warps (9 warps, 168
+// registers); groups of 1 and 2 run 6 streams x 2 stages, one warp per chunk.
+// D = 128: 12 streams x 2 x 8 KiB for small groups, else the tokens split
+// over 2 warps.
+template <bool WIN>
+cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
+                              const DecodeParams &p, dim3 grid, cudaStream_t stream) {
+    constexpr int slot0 = WIN ? 16 : 0;  // shared-memory limit bookkeeping per kernel
+    if (head_dim == 256) {
+        switch (group) {
+            case 1: return launch_decode_t<256, 1, 1, 6, 2, WIN>(tk, tv, p, grid, stream, slot0 + 0);
+            case 2: return launch_decode_t<256, 2, 1, 6, 2, WIN>(tk, tv, p, grid, stream, slot0 + 1);
+            case 4: return launch_decode_t<256, 4, 2, 4, 3, WIN>(tk, tv, p, grid, stream, slot0 + 2);
+            case 6: return launch_decode_t<256, 6, 2, 4, 3, WIN>(tk, tv, p, grid, stream, slot0 + 3);
+        }
+    } else if (head_dim == 128) {
+        switch (group) {
+            case 1: return launch_decode_t<128, 1, 1, 12, 2, WIN>(tk, tv, p, grid, stream, slot0 + 4);
+            case 2: return launch_decode_t<128, 2, 1, 12, 2, WIN>(tk, tv, p, grid, stream, slot0 + 5);
+            case 4: return launch_decode_t<128, 4, 2, 6, 4, WIN>(tk, tv, p, grid, stream, slot0 + 6);
+            case 6: return launch_decode_t<128, 6, 2, 4, 6, WIN>(tk, tv, p, grid, stream, slot0 + 7);
+            case 8: return launch_decode_t<128, 8, 2, 4, 6, WIN>(tk, tv, p, grid, stream, slot0 + 8);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+// the sliding-window instantiations (decode_launch_window.cu)
+cudaError_t launch_decode_window(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const DecodeParams &p, dim3 grid, cudaStream_t stream);
+
+}  // namespace pa

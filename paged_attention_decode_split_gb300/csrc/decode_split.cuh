@@ -66,6 +66,7 @@ struct DecodeParams {
     float scale_log2;     // scale * log2(e)
     int out_bf16;
     int early_kv;         // stream the context before the new row ahead of the dependency wait
+    int window;           // 0: full attention; W > 0: only the last W keys
 };
 
 // D: head_dim.  G: query heads per KV head.  TS: warps sharing one chunk,
@@ -125,7 +126,9 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
         reinterpret_cast<float *>(out)[idx] = v;
 }
 
-template <int D, int G, int TS, int NST, int SPS>
+// WIN: the sliding-window variant (a separate instantiation, so the full-
+// attention kernel carries none of its bookkeeping).
+template <int D, int G, int TS, int NST, int SPS, bool WIN>
 __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
     pa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecodeParams p) {
@@ -172,13 +175,19 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
     // Their range depends only on the split (entries past the sequence's end
     // are staged but never used), so these loads are in flight together with
     // the seq_lens load instead of after it.
-    const int c_begin = split * p.chunks_per_split;
+    int L = p.seq_lens[b];
+    // With a sliding window the splits cover chunks from the window's first
+    // key s0 on (that start depends on the sequence length); without one
+    // they start at 0 and the page-table loads need not wait for seq_lens.
+    int c_begin = split * p.chunks_per_split;
+    if constexpr (WIN) {
+        if (L > p.window && L <= p.max_seq_len) c_begin += (L - p.window) / kChunk;
+    }
     const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
     const int lp_first = (c_begin * kChunk) / p.block_size;
     const int lp_last = min(((c_begin + p.chunks_per_split) * kChunk - 1) / p.block_size, p.max_pages_per_seq - 1);
     const int n_pt = lp_last - lp_first + 1;
     const bool staged = n_pt <= kPageTab;
-    int L = p.seq_lens[b];
     if (staged)
         for (int j = threadIdx.x; j < n_pt; j += C::THREADS) page_tab[j] = bt[lp_first + j];
     if (L < 0 || L > p.max_seq_len) {
@@ -317,8 +326,10 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
             }
             const uint8_t *kst = smem + s * C::STAGE_BYTES + wh * 8 * C::ROW_BYTES + lane * E * 2;
             const uint8_t *vst = kst + C::CHUNK_BYTES;
-            // valid rows of this warp's part of the chunk (may be <= 0 in the last chunk)
+            // valid rows [lead, nv) of this warp's part of the chunk: nv may be
+            // <= lead in the last chunk, lead > 0 only where the window starts
             const int nv = min(8 * MB, L - (c_begin + i) * kChunk - wh * 8);
+            const int lead = WIN ? max(0, L - p.window - (c_begin + i) * kChunk - wh * 8) : 0;
 
             float sc[MB][G];
 #pragma unroll
@@ -357,12 +368,12 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
                     part[0][g] += __shfl_xor_sync(0xffffffffu, part[0][g], 2);
                     part[0][g] += __shfl_xor_sync(0xffffffffu, part[0][g], 1);
                 }
-                const bool valid = (mb * 8 + cg) < nv;
+                const bool valid = (mb * 8 + cg) < nv && (mb * 8 + cg) >= lead;
 #pragma unroll
                 for (int g = 0; g < G; ++g) sc[mb][g] = valid ? part[0][g] : -INFINITY;
             }
 
-            if (nv > 0) {  // warp-uniform
+            if (nv > lead) {  // warp-uniform
                 // Lazy online softmax (log2 domain): the chunk max of a head is
                 // finite because this part has >= 1 valid row.
                 float mx[G];
@@ -422,6 +433,8 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
 #pragma unroll
                         for (int j = 0; j < E / 2; ++j) acc[g][j] = __ffma2_rn(pp[g], v2[j], acc[g][j]);
                 };
+                // rows before the window start have p = 0 and hold finite
+                // cached values, so they run through P.V like the others
                 if (nv == 8 * MB) {
 #pragma unroll 4
                     for (int t = 0; t < 8 * MB; ++t) pv_row(t);

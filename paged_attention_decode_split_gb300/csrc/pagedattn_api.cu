@@ -60,7 +60,7 @@ pa_status check_desc(const pa_attn_desc *d, bool verify) {
     if (!d) return PA_ERR_INVALID_ARG;
     if (d->num_seqs < 0 || d->q_len < 1 || d->num_q_heads < 1 || d->num_kv_heads < 1 || d->head_dim < 1 ||
         d->block_size < 1 || d->max_pages_per_seq < 0 || d->max_seq_len < 0 || d->num_pages < 1 ||
-        d->num_splits < 0 || d->num_sms < 0 || (d->flags & ~PA_FLAG_EARLY_KV_READ) != 0)
+        d->num_splits < 0 || d->num_sms < 0 || (d->flags & ~PA_FLAG_EARLY_KV_READ) != 0 || d->window < 0)
         return PA_ERR_INVALID_ARG;
     if (!verify && d->q_len != 1) return PA_ERR_INVALID_ARG;
     if (d->num_q_heads % d->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
@@ -91,7 +91,12 @@ pa_status make_plan(const pa_attn_desc *d, bool verify, Plan *pl) {
     if (st != PA_OK) return st;
     int sms = d->num_sms;
     if (sms <= 0 && device_sm_count(&sms) != 0) return PA_ERR_CUDA;
-    const int n_chunks = (d->max_seq_len + kChunk - 1) / kChunk;
+    int n_chunks = (d->max_seq_len + kChunk - 1) / kChunk;
+    // with a sliding window a unit reads at most window + q_len - 1 keys, from
+    // a chunk-aligned start: the splits cover that span only
+    if (d->window > 0)
+        n_chunks = static_cast<int>(std::min<int64_t>(
+            n_chunks, (static_cast<int64_t>(d->window) + d->q_len - 1 + kChunk - 1) / kChunk + 1));
     // verify: each (sequence, KV head) unit has ceil(q_len G / 128) row blocks of its own
     const int64_t row_blocks =
         verify ? (static_cast<int64_t>(d->q_len) * (d->num_q_heads / d->num_kv_heads) + 127) / 128 : 1;
@@ -353,6 +358,7 @@ pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const vo
     p.scale_log2 = desc->scale * 1.4426950408889634f;
     p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
     p.early_kv = (desc->flags & PA_FLAG_EARLY_KV_READ) != 0;
+    p.window = desc->window;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);
@@ -420,6 +426,7 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
     p.scale_log2 = desc->scale * 1.4426950408889634f;
     p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
     p.early_kv = (desc->flags & PA_FLAG_EARLY_KV_READ) != 0;
+    p.window = desc->window;
     p.num_kv_heads = desc->num_kv_heads;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);

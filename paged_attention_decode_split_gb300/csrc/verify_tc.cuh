@@ -64,6 +64,7 @@ struct VerifyParams {
     int out_bf16;
     int early_kv;  // stream the context before the new rows ahead of the dependency wait
     int num_kv_heads;  // grid y = num_kv_heads x 128-row blocks
+    int window;        // 0: full attention; W > 0: each row sees only its last W keys
 };
 
 // Byte offset of 16-byte column chunk c of row t in a [D/64][rows][128 B]
@@ -278,7 +279,10 @@ __global__ void __launch_bounds__(6 * 32, 1)
         L = 0;
     }
     const int n_chunks = (L + kChunk - 1) / kChunk;
-    const int c_begin = split * p.chunks_per_split;
+    // with a sliding window the splits start at the chunk of the block's first
+    // visible key (its first row's window start)
+    const int k_first = p.window > 0 ? max(0, L - p.q_len + row0 / G - p.window + 1) : 0;
+    const int c_begin = k_first / kChunk + split * p.chunks_per_split;
     // keys past the block's last row's causal limit are never read
     const int k_last = L - p.q_len + (row0 + R - 1) / G;
     const int n_my = min(min(n_chunks, k_last / kChunk + 1) - c_begin, p.chunks_per_split);
@@ -512,6 +516,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
         // split's last chunk (a tile may reach into the next split's tokens)
         const int t_end = min(L, (c_begin + n_my) * kChunk);
         const int lim = live ? min(L - p.q_len + rho / G, t_end - 1) : -1;
+        const int lo = p.window > 0 ? L - p.q_len + rho / G - p.window + 1 : 0;  // first key of the row's window
         float m_ref = -INFINITY, l_sum = 0.f;
         bool ok = true;
         // O += P_k V_k of tile k is waited for in order per barrier (tile k + 2,
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
             float mx = -INFINITY;
 #pragma unroll
             for (int c = 0; c < TT; ++c) {
-                sv[c] = (t0 + c <= lim) ? sv[c] * p.scale_log2 : -INFINITY;
+                sv[c] = (t0 + c <= lim && t0 + c >= lo) ? sv[c] * p.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, sv[c]);
             }
             // lazy rescale: only when the max grows by more than 2^kLazy, and

@@ -28,18 +28,21 @@ def to_dev(prob, layer=0, device="cuda"):
             prob.block_table.to(device), prob.seq_lens.to(device))
 
 
-def desc_for(prob, *, num_splits=0, out_dtype=pa.PA_OUT_F32, max_seq_len=None):
+def desc_for(prob, *, num_splits=0, out_dtype=pa.PA_OUT_F32, max_seq_len=None, window=0, flags=0):
     return pa.make_desc(num_seqs=prob.num_seqs, q_len=prob.q_len, num_q_heads=prob.num_q_heads,
                         num_kv_heads=prob.num_kv_heads, head_dim=prob.head_dim, block_size=prob.block_size,
                         max_pages_per_seq=prob.max_pages_per_seq,
                         max_seq_len=prob.max_seq_len if max_seq_len is None else max_seq_len,
-                        num_pages=prob.num_pages, scale=prob.scale, out_dtype=out_dtype, num_splits=num_splits)
+                        num_pages=prob.num_pages, scale=prob.scale, out_dtype=out_dtype, num_splits=num_splits,
+                        window=window, flags=flags)
 
 
-def run_attention(prob, layer=0, *, num_splits=0, out_dtype=pa.PA_OUT_F32, max_seq_len=None, tensors=None):
+def run_attention(prob, layer=0, *, num_splits=0, out_dtype=pa.PA_OUT_F32, max_seq_len=None, tensors=None,
+                  window=0, flags=0):
     """Runs decode (q_len 1) or verify through the C ABI; returns (out on CPU, status, plan)."""
     q, kc, vc, bt, sl = tensors if tensors is not None else to_dev(prob, layer)
-    desc = desc_for(prob, num_splits=num_splits, out_dtype=out_dtype, max_seq_len=max_seq_len)
+    desc = desc_for(prob, num_splits=num_splits, out_dtype=out_dtype, max_seq_len=max_seq_len, window=window,
+                    flags=flags)
     ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=q.device)
     dtype = torch.float32 if out_dtype == pa.PA_OUT_F32 else torch.bfloat16
     out = torch.full((prob.num_seqs * prob.q_len, prob.num_q_heads, prob.head_dim), float("nan"), dtype=dtype,
@@ -51,7 +54,7 @@ def run_attention(prob, layer=0, *, num_splits=0, out_dtype=pa.PA_OUT_F32, max_s
     return out.float().cpu(), int(status.item()), pa.last_plan()
 
 
-def oracle_out(oracle_mod, prob, layer=0, rows=None):
+def oracle_out(oracle_mod, prob, layer=0, rows=None, window=0):
     """Oracle output [rows, Hq, D] (float64); ``rows`` restricts to some sequences."""
     q, bt, sl = prob.q[layer].cpu(), prob.block_table.cpu(), prob.seq_lens.cpu()
     if rows is not None:
@@ -59,7 +62,7 @@ def oracle_out(oracle_mod, prob, layer=0, rows=None):
         qi = torch.cat([torch.arange(b * prob.q_len, (b + 1) * prob.q_len) for b in rows])
         q, bt, sl = q[qi].contiguous(), bt[idx].contiguous(), sl[idx].contiguous()
     return oracle_mod.paged_attention(q, prob.k_cache[layer].cpu(), prob.v_cache[layer].cpu(), bt.numpy(),
-                                      sl.numpy(), prob.scale, q_len=prob.q_len)
+                                      sl.numpy(), prob.scale, q_len=prob.q_len, window=window)
 
 
 def parity_report(gpu: torch.Tensor, ref: np.ndarray) -> dict:
