@@ -452,7 +452,7 @@ def _layers_beyond_l2(bytes_per_layer, minimum, l2_bytes=256 << 20):
 
 
 SECONDARY = ("decode_l512_bs16", "context_sweep", "batch32_uniform_bs784", "verify_b8_q16_l8192_bs832",
-             "prefill_q2048_l16384_bs832")
+             "prefill_q2048_l16384_bs832", "decode_window2048_l32768_bs784")
 
 
 def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
@@ -471,6 +471,8 @@ def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
         _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "prefill_q2048_l16384_bs832" in names:
         _prefill(pa, dev, stream, res, WORKLOADS, make_problem)
+    if "decode_window2048_l32768_bs784" in names:
+        _window(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     return res
 
 
@@ -546,6 +548,29 @@ def _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem):
     res["verify_b8_q16_l8192_bs832"] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
                                         "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak,
                                         "TFLOPs": flops / (us * 1e-6) / 1e12, "plan": pa.last_plan()}
+
+
+def _window(pa, dev, stream, peak, res, WORKLOADS, make_problem):
+    # Sliding-window decode: the 32K hybrid layer with a 2048-key window, so
+    # a call reads 2048 x 4096 B = 8 MiB of K+V.  32 distinct layer copies
+    # (256 MiB) keep the reads out of L2.
+    import torch
+    spec = dict(WORKLOADS["hybrid_step_l32768_bs784_x16"], num_layers=32)
+    prob = make_problem(1007, **spec, device=dev)
+    bt, sl = prob.block_table.to(dev), prob.seq_lens.to(dev)
+    desc = pa.make_desc(num_seqs=1, num_q_heads=24, num_kv_heads=4, head_dim=256, block_size=784,
+                        max_pages_per_seq=prob.max_pages_per_seq, max_seq_len=32768, num_pages=prob.num_pages,
+                        scale=1 / 16, window=2048)
+    ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=dev)
+    out = torch.empty((1, 24, 256), dtype=torch.float32, device=dev)
+    calls = [(lambda l=l: pa.paged_attention_decode(prob.q[l], prob.k_cache[l], prob.v_cache[l], bt, sl, desc,
+                                                     out, ws)) for l in range(prob.num_layers)]
+    us = _time_graph(calls, stream, 50) * 1e3 / len(calls)
+    kv = 2048 * KV_BYTES_PER_TOKEN_LAYER
+    res["decode_window2048_l32768_bs784"] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
+                                             "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak,
+                                             "plan": pa.last_plan()}
+    del prob, calls
 
 
 def _causal_flops(prob):
