@@ -452,7 +452,7 @@ def _layers_beyond_l2(bytes_per_layer, minimum, l2_bytes=256 << 20):
 
 
 SECONDARY = ("decode_l512_bs16", "context_sweep", "batch32_uniform_bs784", "verify_b8_q16_l8192_bs832",
-             "prefill_q2048_l16384_bs832", "decode_window2048_l32768_bs784")
+             "prefill_q2048_l16384_bs832", "decode_window2048_l32768_bs784", "decode_g12_l32768_bs784")
 
 
 def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
@@ -473,7 +473,21 @@ def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
         _prefill(pa, dev, stream, res, WORKLOADS, make_problem)
     if "decode_window2048_l32768_bs784" in names:
         _window(pa, dev, stream, peak, res, WORKLOADS, make_problem)
+    if "decode_g12_l32768_bs784" in names:
+        _wide_group(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     return res
+
+
+def _wide_group(pa, dev, stream, peak, res, WORKLOADS, make_problem):
+    # 12 query heads per KV head at 32K: the same 128 MiB of K+V per layer as
+    # the hybrid step with twice the arithmetic per byte; 16 layers (2 GiB).
+    prob = make_problem(1008, **WORKLOADS["decode_g12_l32768_bs784"], device=dev)
+    calls = _attention_calls(pa, prob, dev)
+    us = _time_graph(calls, stream, 50) * 1e3 / len(calls)
+    kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER
+    res["decode_g12_l32768_bs784"] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
+                                      "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak, "plan": pa.last_plan()}
+    del prob, calls
 
 
 def _short_context(pa, torch, dev, stream, res, WORKLOADS, make_problem):

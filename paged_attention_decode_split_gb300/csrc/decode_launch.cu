@@ -6,8 +6,8 @@
 namespace pa {
 
 bool decode_supported(int head_dim, int group) {
-    if (head_dim == 256) return group == 1 || group == 2 || group == 4 || group == 6;
-    if (head_dim == 128) return group == 1 || group == 2 || group == 4 || group == 6 || group == 8;
+    if (head_dim == 256) return group == 1 || group == 2 || group == 4 || group == 6 || group == 12;
+    if (head_dim == 128) return group == 1 || group == 2 || group == 4 || group == 6 || group == 8 || group == 12;
     return false;
 }
 

@@ -7,11 +7,11 @@
 
 namespace pa {
 
-template <int D, int G, int TS, int NST, int SPS, bool WIN>
+template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN>
 cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, dim3 grid,
                             cudaStream_t stream, int slot) {
-    using C = DecodeCfg<D, G, TS, NST, SPS>;
-    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS, WIN>;
+    using C = DecodeCfg<D, G, TS, NST, SPS, HG>;
+    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS, HG, WIN>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the kernel's set-up overlaps the previous
@@ -30,30 +30,33 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
     return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-// Per (head_dim, group): warps per chunk (TS), chunk streams (NST), stages
-// per stream (SPS).  D = 256: groups of 4 and 6 heads run 4 streams x 3
-// stages x 16 KiB with each chunk's tokens split over 2 warps (9 warps, 168
-// registers); groups of 1 and 2 run 6 streams x 2 stages, one warp per chunk.
-// D = 128: 12 streams x 2 x 8 KiB for small groups, else the tokens split
-// over 2 warps.
+// Per (head_dim, group): token halves (TS), chunk streams (NST), stages per
+// stream (SPS), head groups (HG).  D = 256: groups of 4 and 6 heads run 4
+// streams x 3 stages x 16 KiB with each chunk's tokens split over 2 warps (9
+// warps, 168 registers); groups of 1 and 2 run 6 streams x 2 stages, one
+// warp per chunk; 12 heads split into 2 head groups of 6 (4 warps per chunk,
+// 2 streams x 6 stages).  D = 128: 12 streams x 2 x 8 KiB for small groups,
+// else the tokens split over 2 warps.
 template <bool WIN>
 cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                               const DecodeParams &p, dim3 grid, cudaStream_t stream) {
     constexpr int slot0 = WIN ? 16 : 0;  // shared-memory limit bookkeeping per kernel
     if (head_dim == 256) {
         switch (group) {
-            case 1: return launch_decode_t<256, 1, 1, 6, 2, WIN>(tk, tv, p, grid, stream, slot0 + 0);
-            case 2: return launch_decode_t<256, 2, 1, 6, 2, WIN>(tk, tv, p, grid, stream, slot0 + 1);
-            case 4: return launch_decode_t<256, 4, 2, 4, 3, WIN>(tk, tv, p, grid, stream, slot0 + 2);
-            case 6: return launch_decode_t<256, 6, 2, 4, 3, WIN>(tk, tv, p, grid, stream, slot0 + 3);
+            case 1: return launch_decode_t<256, 1, 1, 6, 2, 1, WIN>(tk, tv, p, grid, stream, slot0 + 0);
+            case 2: return launch_decode_t<256, 2, 1, 6, 2, 1, WIN>(tk, tv, p, grid, stream, slot0 + 1);
+            case 4: return launch_decode_t<256, 4, 2, 4, 3, 1, WIN>(tk, tv, p, grid, stream, slot0 + 2);
+            case 6: return launch_decode_t<256, 6, 2, 4, 3, 1, WIN>(tk, tv, p, grid, stream, slot0 + 3);
+            case 12: return launch_decode_t<256, 12, 2, 2, 6, 2, WIN>(tk, tv, p, grid, stream, slot0 + 9);
         }
     } else if (head_dim == 128) {
         switch (group) {
-            case 1: return launch_decode_t<128, 1, 1, 12, 2, WIN>(tk, tv, p, grid, stream, slot0 + 4);
-            case 2: return launch_decode_t<128, 2, 1, 12, 2, WIN>(tk, tv, p, grid, stream, slot0 + 5);
-            case 4: return launch_decode_t<128, 4, 2, 6, 4, WIN>(tk, tv, p, grid, stream, slot0 + 6);
-            case 6: return launch_decode_t<128, 6, 2, 4, 6, WIN>(tk, tv, p, grid, stream, slot0 + 7);
-            case 8: return launch_decode_t<128, 8, 2, 4, 6, WIN>(tk, tv, p, grid, stream, slot0 + 8);
+            case 1: return launch_decode_t<128, 1, 1, 12, 2, 1, WIN>(tk, tv, p, grid, stream, slot0 + 4);
+            case 2: return launch_decode_t<128, 2, 1, 12, 2, 1, WIN>(tk, tv, p, grid, stream, slot0 + 5);
+            case 4: return launch_decode_t<128, 4, 2, 6, 4, 1, WIN>(tk, tv, p, grid, stream, slot0 + 6);
+            case 6: return launch_decode_t<128, 6, 2, 4, 6, 1, WIN>(tk, tv, p, grid, stream, slot0 + 7);
+            case 8: return launch_decode_t<128, 8, 2, 4, 6, 1, WIN>(tk, tv, p, grid, stream, slot0 + 8);
+            case 12: return launch_decode_t<128, 12, 2, 2, 12, 2, WIN>(tk, tv, p, grid, stream, slot0 + 10);
         }
     }
     return cudaErrorInvalidValue;

@@ -69,36 +69,42 @@ struct DecodeParams {
     int window;           // 0: full attention; W > 0: only the last W keys
 };
 
-// D: head_dim.  G: query heads per KV head.  TS: warps sharing one chunk,
-// each taking 16 / TS of its tokens.  NST: chunk streams (consumer warps =
-// TS * NST).  SPS: stages owned by each stream (NS = NST * SPS in all).
+// D: head_dim.  G: query heads per KV head.  TS x HG warps share one chunk,
+// each taking 16 / TS of its tokens and G / HG of the heads (HG > 1 only
+// for groups too wide for one warp's registers).  NST: chunk streams
+// (consumer warps = TS * HG * NST).  SPS: stages owned by each stream (NS =
+// NST * SPS in all).
 //
 // Stage ownership matters for correctness: an mbarrier wait tests the parity
 // of a phase, so a waiter must never run two phases ahead of the barrier.
 // Each stream therefore owns SPS stages and cycles through them in order; it
 // has consumed every earlier phase of a stage before it waits on the next,
 // and the producer waits on every phase of a stage's empty barrier in order.
-template <int D, int G, int TS, int NST, int SPS>
+template <int D, int G, int TS, int NST, int SPS, int HG>
 struct DecodeCfg {
     static constexpr int NS = NST * SPS;
     static constexpr int E = D / 32;
     static constexpr int MB = 2 / TS;                    // micro-batches of 8 tokens per warp and chunk
-    static constexpr int NWC = TS * NST;                 // consumer warps
+    static constexpr int GW = G / HG;                    // heads per warp
+    static constexpr int WPC = TS * HG;                  // warps per chunk
+    static constexpr int NWC = WPC * NST;                // consumer warps
+    static constexpr int NWH = TS * NST;                 // warps holding a given head
     static constexpr int ROW_BYTES = D * 2;
     static constexpr int CHUNK_BYTES = kChunk * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;  // K chunk, then V chunk
-    static constexpr int GP2 = (G + 1) & ~1;             // (p, p) pairs per P row (16-byte rows)
+    static constexpr int GP2 = (GW + 1) & ~1;            // (p, p) pairs per P row (16-byte rows)
     static constexpr int STAGES_BYTES = NS * STAGE_BYTES;
-    static constexpr int MERGE_BYTES = NWC * G * D * 4;
+    static constexpr int MERGE_BYTES = NWC * GW * D * 4;
     static constexpr int OFF_P = STAGES_BYTES;
     static constexpr int OFF_ML = OFF_P + NWC * 8 * MB * GP2 * 8;
-    static constexpr int OFF_BAR = OFF_ML + NWC * G * 12;  // (m, l) pairs, then the merge weights
+    static constexpr int OFF_BAR = OFF_ML + NWC * GW * 12;  // (m, l) pairs, then the merge weights
     static constexpr int OFF_FLAGS = OFF_BAR + 2 * NS * 8;
     static constexpr int OFF_PT = OFF_FLAGS + 16;
     static constexpr int SMEM_BYTES = OFF_PT + kPageTab * 4 + 1024;  // + slack to align the base to 1 KiB
     static constexpr int THREADS = (NWC + 1) * 32;
     static_assert(D % 32 == 0 && (E == 8 || E == 4), "head_dim 256 or 128");
     static_assert(TS == 1 || TS == 2, "a chunk is consumed by one warp or split in token halves");
+    static_assert(G % HG == 0, "heads split evenly over the head groups");
     static_assert(MERGE_BYTES <= STAGES_BYTES, "the CTA merge reuses the stage buffers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
@@ -128,12 +134,12 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
 
 // WIN: the sliding-window variant (a separate instantiation, so the full-
 // attention kernel carries none of its bookkeeping).
-template <int D, int G, int TS, int NST, int SPS, bool WIN>
-__global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
+template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN>
+__global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
     pa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecodeParams p) {
-    using C = DecodeCfg<D, G, TS, NST, SPS>;
-    constexpr int E = C::E, MB = C::MB, NWC = C::NWC, NS = C::NS;
+    using C = DecodeCfg<D, G, TS, NST, SPS, HG>;
+    constexpr int E = C::E, MB = C::MB, NWC = C::NWC, NS = C::NS, GW = C::GW, WPC = C::WPC, NWH = C::NWH;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     float2 *pbuf_all = reinterpret_cast<float2 *>(smem + C::OFF_P);
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], TS);
+            mbar_init(&empty[s], WPC);
         }
         flags[0] = 0;
         flags[1] = 0;
@@ -213,9 +219,10 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
     }
     __syncthreads();  // barrier initialisation and the page table are visible to every thread
 
-    const int wh = warp % TS, stream = warp / TS;  // consumer warps: token half, chunk stream
-    float m_run[G], l_run[G];
-    float2 acc[G][E / 2];
+    // consumer warps: chunk stream, token half, head group
+    const int stream = warp / WPC, wh = (warp % WPC) % TS, hg = (warp % WPC) / TS;
+    float m_run[GW], l_run[GW];
+    float2 acc[GW][E / 2];
     if (warp == NWC) {
         // ---------------- producer: one lane issues every copy ----------------
         // Streams are refilled independently: the lane probes each stream's
@@ -296,21 +303,21 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
         // output dims with the probability duplicated in both halves.
         const int cg = (lane >> 2) & 7;
         float2 *pbuf = pbuf_all + warp * (8 * MB * C::GP2);
-        float2 q2[G][E / 2];
+        float2 q2[GW][E / 2];
         if (p.early_kv) pdl_wait_primary();  // q may come from the work before this call
         {
             const uint8_t *qrow =
-                reinterpret_cast<const uint8_t *>(p.q + ((size_t)b * p.num_q_heads + hq0) * D) + lane * E * 2;
+                reinterpret_cast<const uint8_t *>(p.q + ((size_t)b * p.num_q_heads + hq0 + hg * GW) * D) + lane * E * 2;
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < GW; ++g) {
                 load_bf16_pairs<E>(qrow + g * D * 2, q2[g]);
 #pragma unroll
                 for (int j = 0; j < E / 2; ++j) q2[g][j] = __fmul2_rn(q2[g][j], sc2);
             }
         }
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < GW; ++g) {
             m_run[g] = -INFINITY;
             l_run[g] = 0.f;
 #pragma unroll
@@ -331,22 +338,22 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
             const int nv = min(8 * MB, L - (c_begin + i) * kChunk - wh * 8);
             const int lead = WIN ? max(0, L - p.window - (c_begin + i) * kChunk - wh * 8) : 0;
 
-            float sc[MB][G];
+            float sc[MB][GW];
 #pragma unroll
             for (int mb = 0; mb < MB; ++mb) {
                 // Slots j and j + 4 are formed together and the first butterfly
                 // step (lane XOR 16) folds the high one into the low one at once.
-                float part[4][G];
+                float part[4][GW];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    float hi[G];
+                    float hi[GW];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int slot = j + 4 * h;
                         float2 k2[E / 2];
                         load_bf16_pairs<E>(kst + (mb * 8 + (slot ^ cg)) * C::ROW_BYTES, k2);
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
+                        for (int g = 0; g < GW; ++g) {
                             float2 a = __fmul2_rn(q2[g][0], k2[0]);
 #pragma unroll
                             for (int jj = 1; jj < E / 2; ++jj) a = __ffma2_rn(q2[g][jj], k2[jj], a);
@@ -357,11 +364,11 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
                         }
                     }
 #pragma unroll
-                    for (int g = 0; g < G; ++g) part[j][g] += __shfl_xor_sync(0xffffffffu, hi[g], 16);
+                    for (int g = 0; g < GW; ++g) part[j][g] += __shfl_xor_sync(0xffffffffu, hi[g], 16);
                 }
-                // Rest of the transposing butterfly: 4 slots x G -> 1 slot x G.
+                // Rest of the transposing butterfly: 4 slots x GW -> 1 slot x GW.
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < GW; ++g) {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) part[j][g] += __shfl_xor_sync(0xffffffffu, part[j + 2][g], 8);
                     part[0][g] += __shfl_xor_sync(0xffffffffu, part[1][g], 4);
@@ -370,16 +377,16 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
                 }
                 const bool valid = (mb * 8 + cg) < nv && (mb * 8 + cg) >= lead;
 #pragma unroll
-                for (int g = 0; g < G; ++g) sc[mb][g] = valid ? part[0][g] : -INFINITY;
+                for (int g = 0; g < GW; ++g) sc[mb][g] = valid ? part[0][g] : -INFINITY;
             }
 
             if (nv > lead) {  // warp-uniform
                 // Lazy online softmax (log2 domain): the chunk max of a head is
                 // finite because this part has >= 1 valid row.
-                float mx[G];
+                float mx[GW];
                 bool raise_any = false;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < GW; ++g) {
                     float v = sc[0][g];
 #pragma unroll
                     for (int mb = 1; mb < MB; ++mb) v = fmaxf(v, sc[mb][g]);
@@ -388,7 +395,7 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
                 }
                 if (raise_any) {
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
+                    for (int g = 0; g < GW; ++g) {
                         if (mx[g] > m_run[g] + kLazyLog2) {
                             const float alpha = fast_exp2(m_run[g] - mx[g]);  // 0 on the first chunk
                             const float2 a2 = make_float2(alpha, alpha);
@@ -400,7 +407,7 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
                     }
                 }
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < GW; ++g) {
                     float ps = 0.f;
 #pragma unroll
                     for (int mb = 0; mb < MB; ++mb) {
@@ -414,7 +421,7 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
 #pragma unroll
                     for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-                        for (int g = 0; g < G; ++g) pbuf[(mb * 8 + cg) * C::GP2 + g] = make_float2(sc[mb][g], sc[mb][g]);
+                        for (int g = 0; g < GW; ++g) pbuf[(mb * 8 + cg) * C::GP2 + g] = make_float2(sc[mb][g], sc[mb][g]);
                 }
                 __syncwarp();
 
@@ -429,7 +436,7 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
                         pp[j + 1] = make_float2(x.z, x.w);
                     }
 #pragma unroll
-                    for (int g = 0; g < G; ++g)
+                    for (int g = 0; g < GW; ++g)
 #pragma unroll
                         for (int j = 0; j < E / 2; ++j) acc[g][j] = __ffma2_rn(pp[g], v2[j], acc[g][j]);
                 };
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
         // l_run counts each token once per 4 lanes (bits 0-1 replicate) and is
         // split across lane bits 2-4.
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < GW; ++g) {
             float l = l_run[g];
             l += __shfl_xor_sync(0xffffffffu, l, 4);
             l += __shfl_xor_sync(0xffffffffu, l, 8);
@@ -460,36 +467,40 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
 
     __syncthreads();  // every chunk is consumed: the stage buffers become the merge area
     const bool aborted = flags[0] != 0;
-    // Merge the NWC warp states of this split (same log-sum-exp rule as the
-    // split reduce) and write the split result: the warps store their states,
-    // warp 0 forms the weights 2^(m_w - M) / sum_w l_w 2^(m_w - M) with
-    // shuffles, and every output is a weighted sum over the warps read with
+    // Merge the warp states of this split (same log-sum-exp rule as the split
+    // reduce) and write the split result: the warps store their states
+    // ([warp][GW][D], [warp][GW]), warp 0 forms the weights 2^(m_w - M) /
+    // sum_w l_w 2^(m_w - M) over the NWH warps holding each head with
+    // shuffles, and every output is a weighted sum over those warps read with
     // 16-byte shared loads.
-    float *merge_acc = reinterpret_cast<float *>(smem);  // [NWC][G][D]
-    float *wgt = reinterpret_cast<float *>(merge_ml + NWC * G);  // [NWC][G] after (m, l)
+    float *merge_acc = reinterpret_cast<float *>(smem);  // [NWC][GW][D]
+    float *wgt = reinterpret_cast<float *>(merge_ml + NWC * GW);  // [NWC][GW] after (m, l)
     const bool poisoned = aborted || flags[1] != 0;
+    // the k-th warp holding head h (k < NWH): stream k / TS, token half k % TS
+    auto holder = [&](int h, int k) { return (k / TS) * WPC + (h / GW) * TS + (k % TS); };
     if (warp < NWC) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float *dst = merge_acc + (warp * G + g) * D + lane * E;
+        for (int g = 0; g < GW; ++g) {
+            float *dst = merge_acc + (warp * GW + g) * D + lane * E;
 #pragma unroll
             for (int j = 0; j < E / 2; j += 2)
                 *reinterpret_cast<float4 *>(dst + 2 * j) =
                     make_float4(acc[g][j].x, acc[g][j].y, acc[g][j + 1].x, acc[g][j + 1].y);
-            if (lane == 0) merge_ml[warp * G + g] = make_float2(m_run[g], l_run[g]);
+            if (lane == 0) merge_ml[warp * GW + g] = make_float2(m_run[g], l_run[g]);
         }
     }
     __syncthreads();
     if (warp == 0) {
-        // lane groups of NWP >= NWC lanes, one group per head; surplus lanes hold empty states
-        constexpr int NWP = NWC <= 8 ? 8 : (NWC <= 16 ? 16 : 32);
-        static_assert(NWC <= 32, "warp states fit one warp");
+        // lane groups of NWP >= NWH lanes, one group per head; surplus lanes hold empty states
+        constexpr int NWP = NWH <= 8 ? 8 : (NWH <= 16 ? 16 : 32);
+        static_assert(NWH <= 32, "the warp states of a head fit one warp");
         constexpr int HPP = 32 / NWP;  // heads per pass
 #pragma unroll
-        for (int g0 = 0; g0 < G; g0 += HPP) {
-            const int w = lane % NWP, g = g0 + lane / NWP;
-            const bool mine = w < NWC && g < G;
-            const float2 ml = mine ? merge_ml[w * G + g] : make_float2(-INFINITY, 0.f);
+        for (int h0 = 0; h0 < G; h0 += HPP) {
+            const int k = lane % NWP, h = h0 + lane / NWP;
+            const bool mine = k < NWH && h < G;
+            const int slot = mine ? holder(h, k) * GW + h % GW : 0;
+            const float2 ml = mine ? merge_ml[slot] : make_float2(-INFINITY, 0.f);
             float M = ml.x;
 #pragma unroll
             for (int o = 1; o < NWP; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -499,27 +510,28 @@ __global__ void __launch_bounds__((TS * NST + 1) * 32, 1)
             for (int o = 1; o < NWP; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
             const bool zero = poisoned || !(lsum > 0.f);
             if (mine) {
-                wgt[w * G + g] = zero ? 0.f : e / lsum;
-                if (w == 0 && p.num_splits > 1)
-                    p.part_ml[((size_t)b * p.num_q_heads + hq0 + g) * p.num_splits + split] =
+                wgt[slot] = zero ? 0.f : e / lsum;
+                if (k == 0 && p.num_splits > 1)
+                    p.part_ml[((size_t)b * p.num_q_heads + hq0 + h) * p.num_splits + split] =
                         make_float2(M, poisoned ? -1.f : lsum);
             }
         }
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < G * D / 4; idx += C::THREADS) {
-        const int g = (4 * idx) / D, d = 4 * idx - g * D;
+        const int h = (4 * idx) / D, d = 4 * idx - h * D;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 2
-        for (int w = 0; w < NWC; ++w) {
-            const float4 x = *reinterpret_cast<const float4 *>(merge_acc + w * G * D + 4 * idx);
-            const float wg = wgt[w * G + g];
+        for (int k = 0; k < NWH; ++k) {
+            const int slot = holder(h, k) * GW + h % GW;
+            const float4 x = *reinterpret_cast<const float4 *>(merge_acc + slot * D + d);
+            const float wg = wgt[slot];
             o.x = fmaf(x.x, wg, o.x);
             o.y = fmaf(x.y, wg, o.y);
             o.z = fmaf(x.z, wg, o.z);
             o.w = fmaf(x.w, wg, o.w);
         }
-        const size_t row = (size_t)b * p.num_q_heads + hq0 + g;
+        const size_t row = (size_t)b * p.num_q_heads + hq0 + h;
         if (p.num_splits == 1) {
             store_out(p.out, row * D + d, o.x, p.out_bf16);
             store_out(p.out, row * D + d + 1, o.y, p.out_bf16);

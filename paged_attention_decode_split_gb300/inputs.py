@@ -159,6 +159,10 @@ WORKLOADS = {
     "verify_b8_q16_l8192_bs832": dict(num_seqs=8, seq_lens=8192 + 16, num_q_heads=24, num_kv_heads=4,
                                       head_dim=256, block_size=832, scale=1.0 / 16, q_len=16,
                                       num_layers=1),
+    # wider GQA: 48 query heads on the same 4 KV heads (12 per group)
+    "decode_g12_l32768_bs784": dict(num_seqs=1, seq_lens=32768, num_q_heads=48, num_kv_heads=4,
+                                    head_dim=256, block_size=784, scale=1.0 / 16, q_len=1,
+                                    num_layers=16),
     # a chunked-prefill step: 2048 new rows of one sequence over 14336 cached tokens
     "prefill_q2048_l16384_bs832": dict(num_seqs=1, seq_lens=16384, num_q_heads=24, num_kv_heads=4,
                                        head_dim=256, block_size=832, scale=1.0 / 16, q_len=2048,

@@ -66,7 +66,7 @@ def test_decode_forced_split_counts(oracle_mod, splits):
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"splits={splits}")
 
 
-@pytest.mark.parametrize("G,hkv", [(1, 4), (2, 4), (4, 2), (6, 4)])
+@pytest.mark.parametrize("G,hkv", [(1, 4), (2, 4), (4, 2), (6, 4), (12, 4), (12, 1)])
 def test_decode_group_sizes_d256(oracle_mod, G, hkv):
     prob = hybrid(31 + G, [700, 1500], 16, num_q_heads=G * hkv, num_kv_heads=hkv)
     out, status, _ = run_attention(prob)
@@ -74,13 +74,24 @@ def test_decode_group_sizes_d256(oracle_mod, G, hkv):
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"G={G}")
 
 
-@pytest.mark.parametrize("G", [1, 2, 4, 6, 8])
+@pytest.mark.parametrize("G", [1, 2, 4, 6, 8, 12])
 def test_decode_dense_control_d128(oracle_mod, G):
     prob = make_problem(41 + G, num_seqs=3, seq_lens=[1, 100, 2049], num_q_heads=8 * G, num_kv_heads=8,
                         head_dim=128, block_size=16, scale=1 / math.sqrt(128), poison_unused=True)
     out, status, _ = run_attention(prob)
     assert status == 0
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"dense G={G}")
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3, 64])
+def test_decode_wide_group_g12(oracle_mod, splits):
+    """48 query heads on 4 KV heads: the 12 heads of a group are split over two
+    warp groups of 6, which meet again in the CTA merge."""
+    prob = hybrid(251 + splits, TAIL_LENGTHS[:7] + [5000], 784, num_q_heads=48, num_kv_heads=4,
+                  poison_unused=True)
+    out, status, plan = run_attention(prob, num_splits=splits)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_DECODE_CUDA_CORE
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"G=12 splits={splits}")
 
 
 def test_decode_empty_sequences_give_zero(oracle_mod):
@@ -250,6 +261,17 @@ def test_verify_row_blocks(oracle_mod, q_len, lens, bs, splits):
     out, status, plan = run_attention(prob, num_splits=splits)
     assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
     assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"verify rows q_len={q_len}")
+
+
+@pytest.mark.parametrize("q_len", [5, 16])
+def test_verify_wide_group_g12(oracle_mod, q_len):
+    """12 query heads per KV head: 60 or 192 rows per (sequence, KV head)."""
+    prob = hybrid(171 + q_len, [q_len, 900, 2000], 784, q_len=q_len, num_q_heads=48, num_kv_heads=4,
+                  poison_unused=True)
+    write_new_rows(prob, 19)
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"verify G=12 q_len={q_len}")
 
 
 def test_verify_row_blocks_d128(oracle_mod):

@@ -63,6 +63,16 @@ def test_decode_window_dense_d128(oracle_mod):
     assert_parity(out, oracle_out(oracle_mod, prob, window=500), what="decode window d128")
 
 
+@pytest.mark.parametrize("hd", [256, 128])
+def test_decode_window_g12(oracle_mod, hd):
+    import math
+    prob = hybrid(425 + hd, [3000, 700, 5], 784, num_q_heads=48, num_kv_heads=4, head_dim=hd,
+                  scale=1 / math.sqrt(hd))
+    out, status, _ = run_attention(prob, window=1000)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob, window=1000), what=f"decode window G=12 d{hd}")
+
+
 @pytest.mark.parametrize("q_len,lens,window", [(16, [3000, 500, 16], 1024), (16, [900], 40), (200, [1500], 300)])
 def test_verify_window(oracle_mod, q_len, lens, window):
     prob = hybrid(431 + window, lens, 832, q_len=q_len)
