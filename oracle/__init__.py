@@ -68,6 +68,8 @@ def _load():
                 ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _f64p, _f64p, _f64p]
             lib.oracle_lse_combine.restype = ctypes.c_int
             lib.oracle_lse_combine.argtypes = [_f64p, _f64p, _f64p, ctypes.c_int, ctypes.c_int, _f64p]
+            lib.oracle_hybrid_page_tokens.restype = ctypes.c_int64
+            lib.oracle_hybrid_page_tokens.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
             _lib = lib
     return _lib
 
@@ -168,3 +170,10 @@ def lse_combine(o_parts: np.ndarray, m_parts: np.ndarray, l_parts: np.ndarray) -
     if rc != 0:
         raise ValueError(f"oracle_lse_combine failed ({rc})")
     return out
+
+
+def hybrid_page_tokens(state_page_bytes: int, attn_bytes_per_token: int, alignment: int) -> int:
+    """Shared page length of a hybrid attention/recurrent-state cache: the state
+    page in attention tokens, rounded up to whole alignment groups (-1 if an
+    argument is not positive)."""
+    return int(_load().oracle_hybrid_page_tokens(state_page_bytes, attn_bytes_per_token, alignment))

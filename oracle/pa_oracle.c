@@ -355,3 +355,20 @@ int oracle_lse_combine(const double *o_parts, const double *m_parts, const doubl
         out[d] /= wsum;
     return 0;
 }
+
+/* Page length (tokens) for a hybrid model whose attention KV cache and
+ * recurrent-state cache share one page granularity, as the "Why Qwen3.5's
+ * Hybrid Cache Makes This Problem More Complex" section of the DCU page-832
+ * article states it for the path without prefix caching: the state page,
+ * measured in attention tokens, rounded up to a whole number of
+ * alignment-token groups,
+ *     page = ceil(state_page_bytes / (alignment * attn_bytes_per_token)) * alignment.
+ * Returns -1 for non-positive arguments. */
+int64_t oracle_hybrid_page_tokens(int64_t state_page_bytes, int64_t attn_bytes_per_token, int64_t alignment)
+{
+    if (state_page_bytes <= 0 || attn_bytes_per_token <= 0 || alignment <= 0)
+        return -1;
+    const int64_t group_bytes = alignment * attn_bytes_per_token;
+    const int64_t groups = (state_page_bytes + group_bytes - 1) / group_bytes;
+    return groups * alignment;
+}

@@ -365,3 +365,34 @@ def test_kv_bytes_per_token_closed_form():
     Radeon decode-collapse page quotes."""
     assert 2 * 4 * 256 * 2 == 4096 and 2 * 8 * 128 * 2 == 4096
     assert 16 * 4096 == 64 * 1024
+
+
+# -- hybrid page size -------------------------------------------------------------
+
+def test_hybrid_page_golden(oracle_mod):
+    """The article's example: a state page worth 769..784 attention tokens is a
+    784-token page at 16-token alignment and an 832-token page at 64."""
+    spec = json.load(open(os.path.join(GOLDEN, "hybrid_page.json")))
+    lo, hi = spec["state_tokens_range"]
+    for per_token in (4096, 2 * 4 * 256 * 2 * 16, 1):
+        for n in (lo, (lo + hi) // 2, hi):
+            for case in spec["cases"]:
+                got = oracle_mod.hybrid_page_tokens(n * per_token, per_token, case["alignment"])
+                assert got == case["page"], (n, per_token, case)
+    for page, pct in spec["capacity_growth_pct"].items():
+        assert abs(100.0 * (int(page) / 784 - 1) - pct) < 0.05
+
+
+def test_hybrid_page_bruteforce(oracle_mod):
+    """The smallest multiple of the alignment whose attention capacity covers
+    the state page, found by walking the multiples."""
+    for align in (1, 16, 64):
+        for per_token in (1, 3, 4096):
+            for state in (1, per_token * 5 - 1, per_token * 64, per_token * 64 + 1, per_token * 781 + 7):
+                page = align
+                while page * per_token < state:
+                    page += align
+                assert oracle_mod.hybrid_page_tokens(state, per_token, align) == page
+    assert oracle_mod.hybrid_page_tokens(0, 4096, 16) == -1
+    assert oracle_mod.hybrid_page_tokens(100, 0, 16) == -1
+    assert oracle_mod.hybrid_page_tokens(100, 4096, 0) == -1
