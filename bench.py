@@ -452,7 +452,8 @@ def _layers_beyond_l2(bytes_per_layer, minimum, l2_bytes=256 << 20):
 
 
 SECONDARY = ("decode_l512_bs16", "context_sweep", "batch32_uniform_bs784", "verify_b8_q16_l8192_bs832",
-             "prefill_q2048_l16384_bs832", "decode_window2048_l32768_bs784", "decode_g12_l32768_bs784")
+             "prefill_q2048_l16384_bs832", "decode_window2048_l32768_bs784", "decode_g12_l32768_bs784",
+             "verify_g12_b32_q5_l2048_bs784")
 
 
 def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
@@ -475,6 +476,9 @@ def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
         _window(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "decode_g12_l32768_bs784" in names:
         _wide_group(pa, dev, stream, peak, res, WORKLOADS, make_problem)
+    if "verify_g12_b32_q5_l2048_bs784" in names:
+        _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem, name="verify_g12_b32_q5_l2048_bs784",
+                layers=2)
     return res
 
 
@@ -552,14 +556,16 @@ def _batch32(pa, dev, stream, peak, res, WORKLOADS, make_problem):
                                     "plan": pa.last_plan()}
 
 
-def _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem):
-    # Speculative verify: 8 sequences x 16 new rows, 8192 prior tokens.
-    prob = make_problem(1005, **dict(WORKLOADS["verify_b8_q16_l8192_bs832"], num_layers=4), device=dev)
+def _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem, name="verify_b8_q16_l8192_bs832", layers=4):
+    # Speculative verify: 8 sequences x 16 new rows over 8192 prior tokens
+    # (256 MiB of K+V), or 32 sequences x 5 rows x 12 heads per KV head over
+    # 2048 positions (256 MiB); 4 or 2 layer copies cycled against L2.
+    prob = make_problem(1005, **dict(WORKLOADS[name], num_layers=layers), device=dev)
     calls = _attention_calls(pa, prob, dev)
     us = _time_graph(calls, stream, 100) * 1e3 / len(calls)
     kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER
     flops = _causal_flops(prob)
-    res["verify_b8_q16_l8192_bs832"] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
+    res[name] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
                                         "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak,
                                         "TFLOPs": flops / (us * 1e-6) / 1e12, "plan": pa.last_plan()}
 

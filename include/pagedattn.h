@@ -141,6 +141,22 @@ typedef struct {
  * queries the device SM count unless desc->num_sms > 0. */
 size_t pa_workspace_bytes(const pa_attn_desc *desc);
 
+/* Page length, in tokens, for a hybrid model whose attention KV cache and
+ * recurrent-state cache share one page granularity: the state page measured
+ * in attention tokens, rounded up to whole groups of alignment_tokens,
+ *     ceil(state_page_bytes / (alignment_tokens * attn_bytes_per_token)) * alignment_tokens
+ * (DCU page-832 article, section "Why Qwen3.5's Hybrid Cache Makes This
+ * Problem More Complex", the path without prefix caching).  A state page
+ * worth 769..784 attention tokens gives 784 at 16-token alignment and 832 at
+ * the 64-token access unit of the article's section 2.
+ *   state_page_bytes      bytes of one recurrent-state page
+ *   attn_bytes_per_token  one token's K+V bytes (2 * Hkv * D * 2 for bf16)
+ *   alignment_tokens      page granularity in tokens (16, 64 ...)
+ * Returns the page length, or -1 if an argument is not positive or the
+ * result does not fit in int64.  Host arithmetic only.  The attention calls
+ * accept any page length that is a multiple of 16. */
+int64_t pa_hybrid_page_tokens(int64_t state_page_bytes, int64_t attn_bytes_per_token, int32_t alignment_tokens);
+
 /* reshape_and_cache -- write new K/V rows into their page slots.
  * For every new token i with slot s = slot_mapping[i]:
  *     k_cache[s / BS, s % BS, h, :] = k_new[i, h, :]   (and the same for V)

@@ -17,6 +17,7 @@ import threading
 
 __all__ = [
     "AttnDesc", "PlanInfo", "PagedAttnError", "load_library", "make_desc", "workspace_bytes",
+    "hybrid_page_tokens",
     "reshape_and_cache", "paged_attention_decode", "paged_attention_verify", "last_plan",
     "status_string", "PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_WORKSPACE",
     "PA_ERR_CUDA", "PA_OUT_F32", "PA_OUT_BF16", "PA_DEV_BAD_SEQLEN", "PA_DEV_BAD_PAGE",
@@ -81,6 +82,8 @@ def load_library(path: str | None = None):
         lib.pa_status_string.argtypes = [ctypes.c_int]
         lib.pa_workspace_bytes.restype = ctypes.c_size_t
         lib.pa_workspace_bytes.argtypes = [ctypes.POINTER(AttnDesc)]
+        lib.pa_hybrid_page_tokens.restype = ctypes.c_int64
+        lib.pa_hybrid_page_tokens.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
         lib.pa_last_plan.restype = ctypes.c_int
         lib.pa_last_plan.argtypes = [ctypes.POINTER(PlanInfo)]
         lib.pa_reshape_and_cache.restype = ctypes.c_int
@@ -110,6 +113,14 @@ def workspace_bytes(desc: AttnDesc) -> int:
     n = load_library().pa_workspace_bytes(ctypes.byref(desc))
     if n == ctypes.c_size_t(-1).value:
         raise PagedAttnError(PA_ERR_INVALID_ARG, "pa_workspace_bytes")
+    return int(n)
+
+
+def hybrid_page_tokens(state_page_bytes: int, attn_bytes_per_token: int, alignment_tokens: int) -> int:
+    """Page length (tokens) shared by a hybrid model's attention and state caches."""
+    n = load_library().pa_hybrid_page_tokens(state_page_bytes, attn_bytes_per_token, alignment_tokens)
+    if n < 0:
+        raise PagedAttnError(PA_ERR_INVALID_ARG, "pa_hybrid_page_tokens")
     return int(n)
 
 

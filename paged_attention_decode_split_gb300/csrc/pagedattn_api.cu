@@ -289,6 +289,16 @@ size_t pa_workspace_bytes(const pa_attn_desc *desc) {
     return pl.ws_bytes;
 }
 
+int64_t pa_hybrid_page_tokens(int64_t state_page_bytes, int64_t attn_bytes_per_token, int32_t alignment_tokens) {
+    if (state_page_bytes <= 0 || attn_bytes_per_token <= 0 || alignment_tokens <= 0) return -1;
+    // bytes of one alignment group; past INT64_MAX / alignment one group already holds any state page
+    if (attn_bytes_per_token > INT64_MAX / alignment_tokens) return alignment_tokens;
+    const int64_t group_bytes = attn_bytes_per_token * alignment_tokens;
+    const int64_t groups = state_page_bytes / group_bytes + (state_page_bytes % group_bytes != 0);
+    if (groups > INT64_MAX / alignment_tokens) return -1;
+    return groups * alignment_tokens;
+}
+
 pa_status pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                                const int64_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
                                int32_t head_dim, int32_t block_size, int64_t num_pages, int32_t *device_status,

@@ -163,6 +163,11 @@ WORKLOADS = {
     "decode_g12_l32768_bs784": dict(num_seqs=1, seq_lens=32768, num_q_heads=48, num_kv_heads=4,
                                     head_dim=256, block_size=784, scale=1.0 / 16, q_len=1,
                                     num_layers=16),
+    # speculative verify with 12 query heads per KV head: 5 positions x 12 heads
+    # = 60 rows per (sequence, KV head), 32 sequences of 2048 positions
+    "verify_g12_b32_q5_l2048_bs784": dict(num_seqs=32, seq_lens=2048, num_q_heads=48, num_kv_heads=4,
+                                          head_dim=256, block_size=784, scale=1.0 / 16, q_len=5,
+                                          num_layers=1),
     # a chunked-prefill step: 2048 new rows of one sequence over 14336 cached tokens
     "prefill_q2048_l16384_bs832": dict(num_seqs=1, seq_lens=16384, num_q_heads=24, num_kv_heads=4,
                                        head_dim=256, block_size=832, scale=1.0 / 16, q_len=2048,

@@ -154,3 +154,23 @@ def test_last_plan_before_any_call(lib):
     info = pa.PlanInfo()
     # this process has made no successful attention call on this thread
     assert lib.pa_last_plan(ctypes.byref(info)) == pa.PA_ERR_INVALID_ARG
+
+
+def test_hybrid_page_tokens_matches_oracle(lib, oracle_mod):
+    """Host page-size helper against the oracle's rule on a grid of shapes."""
+    for align in (1, 16, 64, 128):
+        for per_token in (1, 3, 4096, 2 * 8 * 128 * 2):
+            for state in (1, per_token - 1, per_token, 64 * per_token + 1, 781 * per_token, 3 << 20, (1 << 40) + 5):
+                if state <= 0:
+                    continue
+                assert lib.pa_hybrid_page_tokens(state, per_token, align) == \
+                    oracle_mod.hybrid_page_tokens(state, per_token, align), (state, per_token, align)
+    assert pa.hybrid_page_tokens(780 * 4096, 4096, 16) == 784
+    assert pa.hybrid_page_tokens(780 * 4096, 4096, 64) == 832
+    for bad in ((0, 4096, 16), (100, -1, 16), (100, 4096, 0)):
+        assert lib.pa_hybrid_page_tokens(*bad) == -1
+        with pytest.raises(pa.PagedAttnError):
+            pa.hybrid_page_tokens(*bad)
+    # a group larger than any state page: one group; a page past int64: -1
+    assert lib.pa_hybrid_page_tokens(5, 1 << 62, 64) == 64
+    assert lib.pa_hybrid_page_tokens((1 << 63) - 1, 1, 1 << 30) == -1

@@ -300,6 +300,21 @@ def test_verify_b8_q16_l8192_bs832_workload(oracle_mod):
     assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what="verify workload")
 
 
+def test_verify_g12_b32_q5_l2048_bs784_sampled(oracle_mod):
+    """The wide-group verify workload in its benchmark launch: every sequence
+    checked for finiteness and agreement with the dense reference on the
+    first and last, the oracle on four sampled sequences."""
+    prob = make_problem(1005, **WORKLOADS["verify_g12_b32_q5_l2048_bs784"])
+    write_new_rows(prob, 23)
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
+    assert torch.isfinite(out).all()
+    rows = [0, 9, 22, 31]
+    sel = torch.cat([torch.arange(b * 5, (b + 1) * 5) for b in rows])
+    assert_parity(out[sel], oracle_out(oracle_mod, prob, rows=rows), rel_l2=REL_L2_VERIFY,
+                  what="verify G=12 workload")
+
+
 # -- reshape_and_cache ----------------------------------------------------------------
 
 def test_reshape_and_cache_bit_exact(oracle_mod):
