@@ -35,7 +35,11 @@
  *     W > 0 a row sees only its last W visible keys, i.e. keys
  *     (last visible key - W, last visible key]; W = 0 means no window;
  *   - a row that sees no key returns zeros;
- *   - a negative slot in reshape_and_cache is a padding slot and is skipped.
+ *   - a negative slot in reshape_and_cache is a padding slot and is skipped;
+ *   - quantised KV cache (the RTX 3090 page runs a Q4_0 cache, ggml's own
+ *     format): here fp8 e4m3 with one binary32 scale per KV head, code =
+ *     e4m3(x / scale) with the division in binary32, rounding to nearest
+ *     even and saturating to +-448; the cached value is decoded(code) * scale.
  *
  * Return codes: 0 ok, -1 bad argument, -2 an index (page, slot) out of range.
  */
@@ -52,6 +56,69 @@ static double bf16_to_double(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* fp8 e4m3 (the "FN" variant): 1 sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits, no infinities; exponent 15 with mantissa 7 is NaN, so the
+ * largest finite magnitude is 1.75 * 2^8 = 448.  Exponent 0 holds the
+ * subnormals m/8 * 2^-6.  Decoding is exact in double. */
+static double e4m3_to_double(uint8_t c)
+{
+    int e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return (c & 0x80) ? -v : v;
+}
+
+/* Nearest e4m3 value to x, ties to the even code; magnitudes at or above 448
+ * (infinities included) give +-448; NaN gives NaN with x's sign. */
+static uint8_t e4m3_from_float(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    if (isnan(x))
+        return sign | 0x7F;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    /* representable values are spaced 2^(E-3) in the binade [2^E, 2^(E+1))
+     * for E >= -6, and 2^-9 below 2^-6 */
+    int E;
+    frexp(a, &E); /* a = f * 2^E with f in [0.5, 1) */
+    E -= 1;
+    if (a == 0.0 || E < -6)
+        E = -6;
+    double step = ldexp(1.0, E - 3);
+    double k = floor(a / step);
+    double rem = a - k * step;
+    if (rem > 0.5 * step || (rem == 0.5 * step && fmod(k, 2.0) != 0.0))
+        k += 1.0;
+    double v = k * step; /* the rounded magnitude, <= 448 */
+    if (v < ldexp(1.0, -6))
+        return sign | (uint8_t)(v / ldexp(1.0, -9));
+    int e2;
+    frexp(v, &e2);
+    int eb = e2 - 1; /* v in [2^eb, 2^(eb+1)) */
+    int mant = (int)(v / ldexp(1.0, eb - 3)) - 8;
+    return sign | (uint8_t)(((eb + 7) << 3) | mant);
+}
+
+int oracle_e4m3_encode(const float *x, uint8_t *codes, int64_t n)
+{
+    if (n < 0 || (n > 0 && (!x || !codes)))
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = e4m3_from_float(x[i]);
+    return 0;
+}
+
+int oracle_e4m3_decode(const uint8_t *codes, double *out, int64_t n)
+{
+    if (n < 0 || (n > 0 && (!codes || !out)))
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_to_double(codes[i]);
+    return 0;
 }
 
 /* [DCU-832] Sec.1: logical_page = t // BLOCK_SIZE, page_offset = t % BLOCK_SIZE,
@@ -97,6 +164,37 @@ int oracle_reshape_and_cache(const uint16_t *k_new, const uint16_t *v_new,
     return 0;
 }
 
+/* reshape_and_cache into an fp8 cache: the same scatter, each element of KV
+ * head h stored as e4m3(bf16 value / scale[h]) with the division in binary32. */
+int oracle_reshape_and_cache_fp8(const uint16_t *k_new, const uint16_t *v_new,
+                                 uint8_t *k_cache, uint8_t *v_cache,
+                                 const int64_t *slot_mapping, int64_t num_tokens,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 int64_t num_pages, const float *k_scale, const float *v_scale)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_pages < 0 ||
+        !k_scale || !v_scale)
+        return -1;
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0)
+            continue;
+        if (s >= num_pages * block_size)
+            return -2;
+        int64_t dst = ((s / block_size) * block_size + s % block_size) * row;
+        for (int h = 0; h < num_kv_heads; ++h)
+            for (int d = 0; d < head_dim; ++d) {
+                int64_t e = (int64_t)h * head_dim + d;
+                float kq = (float)bf16_to_double(k_new[i * row + e]) / k_scale[h];
+                float vq = (float)bf16_to_double(v_new[i * row + e]) / v_scale[h];
+                k_cache[dst + e] = e4m3_from_float(kq);
+                v_cache[dst + e] = e4m3_from_float(vq);
+            }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Problem description shared by the attention entry points. */
 typedef struct {
@@ -109,7 +207,21 @@ typedef struct {
     int64_t num_pages;
     double scale;
     int64_t window; /* 0: none; W > 0: each row sees only its last W visible keys */
+    /* fp8 cache (k_cache/v_cache unused): e4m3 codes and one scale per KV head */
+    const uint8_t *k_cache8, *v_cache8;
+    const float *k_scale, *v_scale;
 } problem;
+
+/* Cached K (which = 0) or V (which = 1) element at element offset off. */
+static double kv_elem(const problem *p, int which, int64_t off, int kv_head)
+{
+    if (p->k_cache8) {
+        const uint8_t *c = which ? p->v_cache8 : p->k_cache8;
+        const float *sc = which ? p->v_scale : p->k_scale;
+        return e4m3_to_double(c[off]) * (double)sc[kv_head];
+    }
+    return bf16_to_double((which ? p->v_cache : p->k_cache)[off]);
+}
 
 /* Number of keys query row r of sequence b may attend to (causal rule). */
 static int64_t visible_keys(const problem *p, int b, int r)
@@ -158,7 +270,7 @@ static int attend_range(const problem *p, int64_t row, int h, int64_t t_begin, i
             return -2;
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
-            dot += bf16_to_double(qv[d]) * bf16_to_double(p->k_cache[off + d]);
+            dot += bf16_to_double(qv[d]) * kv_elem(p, 0, off + d, kv_head);
         double s = p->scale * dot;
         scratch[t - t_begin] = s;
         if (s > m)
@@ -171,7 +283,7 @@ static int attend_range(const problem *p, int64_t row, int h, int64_t t_begin, i
         double w = exp(scratch[t - t_begin] - m);
         l += w;
         for (int d = 0; d < D; ++d)
-            o[d] += w * bf16_to_double(p->v_cache[off + d]);
+            o[d] += w * kv_elem(p, 1, off + d, kv_head);
     }
     for (int d = 0; d < D; ++d)
         o[d] /= l;
@@ -182,7 +294,9 @@ static int attend_range(const problem *p, int64_t row, int h, int64_t t_begin, i
 
 static int check_problem(const problem *p)
 {
-    if (!p->q || !p->k_cache || !p->v_cache || !p->block_table || !p->seq_lens)
+    if (!p->q || !p->block_table || !p->seq_lens)
+        return -1;
+    if (p->k_cache8 ? (!p->v_cache8 || !p->k_scale || !p->v_scale) : (!p->k_cache || !p->v_cache))
         return -1;
     if (p->num_seqs < 0 || p->q_len <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
         p->head_dim <= 0 || p->block_size <= 0 || p->max_pages_per_seq < 0 || p->num_pages < 0)
@@ -245,6 +359,8 @@ int oracle_paged_attention_window(const uint16_t *q, const uint16_t *k_cache, co
                                   int64_t num_pages, double scale, int64_t window, double *out,
                                   int num_threads);
 
+static int run_attention(const problem *p, double *out, int num_threads);
+
 int oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                            const int32_t *block_table, const int32_t *seq_lens,
                            int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
@@ -265,8 +381,32 @@ int oracle_paged_attention_window(const uint16_t *q, const uint16_t *k_cache, co
                                   int num_threads)
 {
     problem p = {q, k_cache, v_cache, block_table, seq_lens, num_seqs, q_len, num_q_heads,
-                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale, window};
-    if (!out || check_problem(&p) != 0 || window < 0)
+                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale, window,
+                 NULL, NULL, NULL, NULL};
+    return run_attention(&p, out, num_threads);
+}
+
+/* The same over an fp8 cache: e4m3 codes [num_pages, block_size,
+ * num_kv_heads, head_dim] and one scale per KV head for K and for V. */
+int oracle_paged_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                               const float *k_scale, const float *v_scale,
+                               const int32_t *block_table, const int32_t *seq_lens,
+                               int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int max_pages_per_seq,
+                               int64_t num_pages, double scale, int64_t window, double *out,
+                               int num_threads)
+{
+    problem p = {q, NULL, NULL, block_table, seq_lens, num_seqs, q_len, num_q_heads,
+                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale, window,
+                 k_cache, v_cache, k_scale, v_scale};
+    return run_attention(&p, out, num_threads);
+}
+
+static int run_attention(const problem *pp, double *out, int num_threads)
+{
+    const problem p = *pp;
+    const int num_seqs = p.num_seqs, q_len = p.q_len, num_q_heads = p.num_q_heads;
+    if (!out || check_problem(&p) != 0 || p.window < 0)
         return -1;
     if (num_threads < 1)
         num_threads = 1;
@@ -311,7 +451,8 @@ int oracle_attention_partial(const uint16_t *q, const uint16_t *k_cache, const u
                              int64_t t_begin, int64_t t_end, double *o, double *m, double *l)
 {
     problem p = {q, k_cache, v_cache, block_table, seq_lens, num_seqs, q_len, num_q_heads,
-                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale, 0};
+                 num_kv_heads, head_dim, block_size, max_pages_per_seq, num_pages, scale, 0,
+                 NULL, NULL, NULL, NULL};
     if (!o || !m || !l || check_problem(&p) != 0)
         return -1;
     if (row < 0 || row >= (int64_t)num_seqs * q_len || head < 0 || head >= num_q_heads)

@@ -396,3 +396,151 @@ def test_hybrid_page_bruteforce(oracle_mod):
     assert oracle_mod.hybrid_page_tokens(0, 4096, 16) == -1
     assert oracle_mod.hybrid_page_tokens(100, 0, 16) == -1
     assert oracle_mod.hybrid_page_tokens(100, 4096, 0) == -1
+
+
+# -- fp8 e4m3 KV cache -------------------------------------------------------------
+
+E4M3_NAN_CODES = (0x7F, 0xFF)
+
+
+def _torch_e4m3_values():
+    """Every code's value through torch's float8_e4m3fn type (a library routine)."""
+    return torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def test_e4m3_decode_all_codes(oracle_mod):
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle_mod.e4m3_decode(codes)
+    ref = _torch_e4m3_values()
+    nan = np.isnan(got)
+    assert sorted(np.flatnonzero(nan).tolist()) == list(E4M3_NAN_CODES)
+    assert np.array_equal(got[~nan], ref[~nan]) and np.isnan(ref[nan]).all()
+    # points fixed by the format: 1 sign, 4 exponent (bias 7), 3 mantissa bits
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0      # largest finite
+    assert got[0x08] == 2.0 ** -6 and got[0x07] == 7 * 2.0 ** -9  # smallest normal, largest subnormal
+    assert got[0x01] == 2.0 ** -9                           # smallest subnormal
+    assert got[0x38] == 1.0 and got[0x40] == 2.0 and got[0x39] == 1.125
+    assert got[0x80] == 0.0 and math.copysign(1.0, got[0x80]) == -1.0
+
+
+def test_e4m3_encode_round_trip_and_ties(oracle_mod):
+    vals = oracle_mod.e4m3_decode(np.arange(256, dtype=np.uint8))
+    finite = [c for c in range(256) if c not in E4M3_NAN_CODES]
+    # every value encodes to its own code
+    assert np.array_equal(oracle_mod.e4m3_encode(vals[finite].astype(np.float32)), np.array(finite, np.uint8))
+    # midpoints between neighbours round to the even code; just off them, to the nearer one
+    pos = sorted(v for v in vals[:0x7F] if v >= 0)
+    for lo, hi in zip(pos[:-1], pos[1:]):
+        mid = (lo + hi) / 2
+        even = lo if int(oracle_mod.e4m3_encode(np.float32([lo]))[0]) % 2 == 0 else hi
+        got = oracle_mod.e4m3_decode(oracle_mod.e4m3_encode(np.float32([mid, -mid])))
+        assert got[0] == even and got[1] == -even, (lo, hi)
+        below, above = np.nextafter(np.float32(mid), np.float32(0)), np.nextafter(np.float32(mid), np.float32(1e9))
+        got = oracle_mod.e4m3_decode(oracle_mod.e4m3_encode(np.float32([below, above])))
+        assert got[0] == lo and got[1] == hi
+
+
+def test_e4m3_encode_matches_torch_in_range(oracle_mod):
+    """Nearest-even rounding agrees with torch's float8_e4m3fn cast wherever the
+    cast does not overflow (torch turns |x| >= 464 into NaN; the cache saturates)."""
+    g = torch.Generator().manual_seed(5)
+    x = torch.cat([torch.randn(20000, generator=g) * s for s in (1e-3, 0.05, 1.0, 30.0, 150.0)])
+    x = x[x.abs() < 464].float()
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle_mod.e4m3_encode(x.numpy()), ref)
+
+
+def test_e4m3_encode_saturates(oracle_mod):
+    x = np.float32([448.0, 448.5, 463.9, 464.0, 1e9, np.inf, -500.0, -np.inf, np.nan, -np.nan, 0.0, -0.0])
+    got = oracle_mod.e4m3_encode(x)
+    assert got.tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F, 0xFF, 0x00, 0x80]
+
+
+def _fp8_problem(gen, lens, hkv, d, bs, exact_scales):
+    """Random finite e4m3 codes paged through a block table, with per-head scales
+    (powers of two when exact_scales: decoded x scale is then a bf16 value)."""
+    P = sum(math.ceil(L / bs) for L in lens) + 2
+    kc = torch.randint(0, 256, (P, bs, hkv, d), generator=gen).to(torch.uint8)
+    vc = torch.randint(0, 256, (P, bs, hkv, d), generator=gen).to(torch.uint8)
+    for c in (kc, vc):
+        c[(c & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+        c[(c & 0x78) >= 0x58] &= 0xC7  # |value| < 16: softmax stays well spread
+    if exact_scales:
+        ks = np.float32([2.0 ** -(3 + h) for h in range(hkv)])
+        vs = np.float32([2.0 ** -(1 + 2 * h) for h in range(hkv)])
+    else:
+        ks = np.float32([0.0371 * (1 + h) for h in range(hkv)])
+        vs = np.float32([0.113 / (1 + h) for h in range(hkv)])
+    perm = torch.randperm(P, generator=gen)
+    npg = max(math.ceil(L / bs) for L in lens)
+    bt = torch.full((len(lens), npg), -1, dtype=torch.int32)
+    cur = 0
+    for b, L in enumerate(lens):
+        for lp in range(math.ceil(L / bs)):
+            bt[b, lp] = int(perm[cur])
+            cur += 1
+    return kc.numpy(), vc.numpy(), ks, vs, bt
+
+
+def test_fp8_attention_equals_bf16_attention_on_the_decoded_values_bitwise(oracle_mod):
+    """With power-of-two scales every dequantised element is a bf16 value: the
+    fp8 path must then give exactly the bf16 path's result on that cache."""
+    gen = torch.Generator().manual_seed(61)
+    lens, hkv, d, bs, hq = [37, 1, 100, 16], 2, 16, 16, 6
+    kc, vc, ks, vs, bt = _fp8_problem(gen, lens, hkv, d, bs, exact_scales=True)
+    kd = oracle_mod.e4m3_decode(kc) * ks[None, None, :, None]
+    vd = oracle_mod.e4m3_decode(vc) * vs[None, None, :, None]
+    kb = torch.from_numpy(kd).to(torch.bfloat16)
+    vb = torch.from_numpy(vd).to(torch.bfloat16)
+    assert np.array_equal(kb.double().numpy(), kd) and np.array_equal(vb.double().numpy(), vd)
+    for q_len, window in ((1, 0), (1, 20), (3, 0)):
+        q = randn_bf16((len(lens) * q_len, hq, d), gen)
+        sl = np.int32([max(L, q_len) for L in lens])
+        ref = _run(oracle_mod, q, kb, vb, bt, sl, 0.25, q_len=q_len, window=window)
+        got = oracle_mod.paged_attention_fp8(bits(q), kc, vc, ks, vs, bt.numpy(), sl, 0.25, q_len=q_len,
+                                             window=window, num_threads=3)
+        assert np.array_equal(got, ref), (q_len, window)
+
+
+def test_fp8_attention_bruteforce_dense_softmax(oracle_mod):
+    """Arbitrary per-head scales against torch fp64 softmax over the dequantised
+    contiguous K/V (codes decoded by torch's float8 type)."""
+    gen = torch.Generator().manual_seed(67)
+    lens, hkv, d, bs, hq = [50, 7, 33], 3, 8, 16, 6
+    kc, vc, ks, vs, bt = _fp8_problem(gen, lens, hkv, d, bs, exact_scales=False)
+    kt = torch.from_numpy(kc).view(torch.float8_e4m3fn).double() * torch.from_numpy(ks).double()[None, None, :, None]
+    vt = torch.from_numpy(vc).view(torch.float8_e4m3fn).double() * torch.from_numpy(vs).double()[None, None, :, None]
+    k_list, v_list = [], []
+    for b, L in enumerate(lens):
+        k_list.append(torch.cat([kt[int(bt[b, t // bs])][t % bs: t % bs + 1] for t in range(L)]))
+        v_list.append(torch.cat([vt[int(bt[b, t // bs])][t % bs: t % bs + 1] for t in range(L)]))
+    q = randn_bf16((len(lens), hq, d), gen)
+    ref = dense_attention(q, k_list, v_list, 0.3, 1, hkv).numpy()
+    got = oracle_mod.paged_attention_fp8(bits(q), kc, vc, ks, vs, bt.numpy(), np.int32(lens), 0.3)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_reshape_and_cache_fp8_quantises_and_scatters(oracle_mod):
+    """Codes equal torch's float8 cast of (bf16 value / head scale) in binary32
+    (inputs kept inside +-448), written at (slot / BS, slot % BS); other slots untouched."""
+    gen = torch.Generator().manual_seed(71)
+    P, bs, hkv, d, n = 5, 16, 3, 32, 11
+    kc = np.full((P, bs, hkv, d), 0x55, np.uint8)
+    vc = np.full((P, bs, hkv, d), 0xAA, np.uint8)
+    kn = randn_bf16((n, hkv, d), gen)
+    vn = randn_bf16((n, hkv, d), gen)
+    ks = np.float32([0.02, 0.05, 0.013])
+    vs = np.float32([0.011, 0.3, 0.07])
+    slots = np.array([0, 15, 16, 79, -1, 40, 41, 17, 63, 2, 3], dtype=np.int64)
+    oracle_mod.reshape_and_cache_fp8(bits(kn), bits(vn), kc, vc, slots, ks, vs)
+    kq = (kn.float() / torch.from_numpy(ks)[None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    vq = (vn.float() / torch.from_numpy(vs)[None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    written = np.zeros((P, bs), dtype=bool)
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        assert np.array_equal(kc[s // bs, s % bs], kq[i]) and np.array_equal(vc[s // bs, s % bs], vq[i])
+        written[s // bs, s % bs] = True
+    assert (kc[~written] == 0x55).all() and (vc[~written] == 0xAA).all()
+    with pytest.raises(ValueError):
+        oracle_mod.reshape_and_cache_fp8(bits(kn[:1]), bits(vn[:1]), kc, vc, np.array([P * bs], np.int64), ks, vs)
