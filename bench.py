@@ -453,7 +453,7 @@ def _layers_beyond_l2(bytes_per_layer, minimum, l2_bytes=256 << 20):
 
 SECONDARY = ("decode_l512_bs16", "context_sweep", "batch32_uniform_bs784", "verify_b8_q16_l8192_bs832",
              "prefill_q2048_l16384_bs832", "decode_window2048_l32768_bs784", "decode_g12_l32768_bs784",
-             "verify_g12_b32_q5_l2048_bs784")
+             "verify_g12_b32_q5_l2048_bs784", "decode_fp8_l32768_bs784")
 
 
 def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
@@ -476,10 +476,33 @@ def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
         _window(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "decode_g12_l32768_bs784" in names:
         _wide_group(pa, dev, stream, peak, res, WORKLOADS, make_problem)
+    if "decode_fp8_l32768_bs784" in names:
+        _fp8_decode(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "verify_g12_b32_q5_l2048_bs784" in names:
         _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem, name="verify_g12_b32_q5_l2048_bs784",
                 layers=2)
     return res
+
+
+def _fp8_decode(pa, dev, stream, peak, res, WORKLOADS, make_problem):
+    # The 32K hybrid layer over an fp8 e4m3 cache: 2048 B of K+V per token
+    # (half of bf16), 64 MiB per layer, 16 layers (1 GiB) cycled against L2.
+    prob = make_problem(1009, **WORKLOADS["decode_fp8_l32768_bs784"], device=dev)
+    bt, sl = prob.block_table.to(dev), prob.seq_lens.to(dev)
+    desc = pa.make_desc(num_seqs=prob.num_seqs, num_q_heads=prob.num_q_heads, num_kv_heads=prob.num_kv_heads,
+                        head_dim=prob.head_dim, block_size=prob.block_size, max_pages_per_seq=prob.max_pages_per_seq,
+                        max_seq_len=prob.max_seq_len, num_pages=prob.num_pages, scale=prob.scale)
+    import torch
+    ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=dev)
+    out = torch.empty((prob.num_seqs, prob.num_q_heads, prob.head_dim), dtype=torch.float32, device=dev)
+    calls = [(lambda l=l: pa.paged_attention_decode_fp8(prob.q[l], prob.k_cache[l], prob.v_cache[l], prob.k_scale[l],
+                                                        prob.v_scale[l], bt, sl, desc, out, ws))
+             for l in range(prob.num_layers)]
+    us = _time_graph(calls, stream, 100) * 1e3 / len(calls)
+    kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER // 2
+    res["decode_fp8_l32768_bs784"] = {"us_per_call": us, "kv_bytes_per_call": kv, "GBps": kv / (us * 1e-6) / 1e9,
+                                      "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak, "plan": pa.last_plan()}
+    del prob, calls
 
 
 def _wide_group(pa, dev, stream, peak, res, WORKLOADS, make_problem):

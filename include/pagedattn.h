@@ -210,6 +210,42 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
                                     const pa_attn_desc *desc, void *out, void *workspace,
                                     size_t workspace_bytes, int32_t *device_status, void *stream);
 
+/* ---- fp8 e4m3 KV cache ------------------------------------------------------
+ * The RTX 3090 page ("24 GB of VRAM for a 128K context") shrinks the KV cache
+ * with a quantised format (ggml's Q4_0) because decode time is KV bytes.  The
+ * counterpart here is an fp8 e4m3 cache (1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities, largest finite 448) with one binary32 scale
+ * per KV head for K and one for V, chosen by the caller (for example max |x|
+ * / 448 over a calibration set): an element x is stored as the code
+ *     e4m3(x / scale[kv_head])     (binary32 division, round to nearest even,
+ *                                   saturating to +-448; NaN stays NaN)
+ * and read back as decoded(code) * scale[kv_head].  Half the bytes of bf16. */
+
+/* reshape_and_cache into an fp8 cache: the slot rules of pa_reshape_and_cache,
+ * each element quantised as above.
+ *   k_new, v_new     device bf16 [num_tokens, num_kv_heads, head_dim]
+ *   k_cache, v_cache device uint8 e4m3 codes [num_pages, block_size, num_kv_heads, head_dim]
+ *   k_scale, v_scale device float [num_kv_heads]
+ * head_dim must be a multiple of 8 (PA_ERR_UNSUPPORTED otherwise). */
+pa_status pa_reshape_and_cache_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                   const int64_t *slot_mapping, const float *k_scale, const float *v_scale,
+                                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int64_t num_pages, int32_t *device_status,
+                                   void *stream);
+
+/* paged_attention_decode over an fp8 cache: out as pa_paged_attention_decode
+ * with K_t = decoded(k code) * k_scale[kv head], V_t likewise.  The split
+ * plan and workspace are those of the bf16 call with the same description
+ * (pa_workspace_bytes).  Window and PA_FLAG_EARLY_KV_READ behave as there.
+ *   k_cache, v_cache device uint8 e4m3 codes [P, BS, Hkv, D]
+ *   k_scale, v_scale device float [Hkv], read after the stream dependency
+ * Other arguments, results and errors as for pa_paged_attention_decode. */
+pa_status pa_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                        const float *k_scale, const float *v_scale,
+                                        const int32_t *block_table, const int32_t *seq_lens,
+                                        const pa_attn_desc *desc, void *out, void *workspace,
+                                        size_t workspace_bytes, int32_t *device_status, void *stream);
+
 /* Size of the scratch array that pa_paged_attention_decode_noalloc keeps in
  * device memory (8 MiB per GPU that loads the library, held until exit). */
 #define PA_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -17,7 +17,7 @@ import threading
 
 __all__ = [
     "AttnDesc", "PlanInfo", "PagedAttnError", "load_library", "make_desc", "workspace_bytes",
-    "hybrid_page_tokens",
+    "hybrid_page_tokens", "reshape_and_cache_fp8", "paged_attention_decode_fp8",
     "reshape_and_cache", "paged_attention_decode", "paged_attention_verify", "last_plan",
     "status_string", "PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_WORKSPACE",
     "PA_ERR_CUDA", "PA_OUT_F32", "PA_OUT_BF16", "PA_DEV_BAD_SEQLEN", "PA_DEV_BAD_PAGE",
@@ -89,6 +89,12 @@ def load_library(path: str | None = None):
         lib.pa_reshape_and_cache.restype = ctypes.c_int
         lib.pa_reshape_and_cache.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _vp, _vp]
+        lib.pa_reshape_and_cache_fp8.restype = ctypes.c_int
+        lib.pa_reshape_and_cache_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _vp, _vp]
+        lib.pa_paged_attention_decode_fp8.restype = ctypes.c_int
+        lib.pa_paged_attention_decode_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc),
+                                                      _vp, _vp, ctypes.c_size_t, _vp, _vp]
         for name in ("pa_paged_attention_decode", "pa_paged_attention_verify"):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
@@ -174,6 +180,27 @@ def paged_attention_verify(q, k_cache, v_cache, block_table, seq_lens, desc: Att
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
         _ptr(workspace), ws, _ptr(status), _stream(stream))
     _check(rc, "pa_paged_attention_verify")
+
+
+def reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale, v_scale, status=None,
+                          stream=None) -> None:
+    """Quantise new K/V rows ([N, Hkv, D] bf16) into e4m3 cache slots (uint8
+    caches [P, BS, Hkv, D]; float32 scales [Hkv])."""
+    num_pages, block_size, num_kv_heads, head_dim = k_cache.shape
+    rc = load_library().pa_reshape_and_cache_fp8(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), _ptr(k_scale), _ptr(v_scale),
+        int(slot_mapping.shape[0]), num_kv_heads, head_dim, block_size, num_pages, _ptr(status), _stream(stream))
+    _check(rc, "pa_reshape_and_cache_fp8")
+
+
+def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, desc: AttnDesc, out,
+                               workspace=None, status=None, stream=None) -> None:
+    """Decode over an e4m3 cache: K = code x k_scale[kv head], V likewise."""
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().pa_paged_attention_decode_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
+        ctypes.byref(desc), _ptr(out), _ptr(workspace), ws, _ptr(status), _stream(stream))
+    _check(rc, "pa_paged_attention_decode_fp8")
 
 
 def last_plan() -> dict:

@@ -14,7 +14,13 @@ bool decode_supported(int head_dim, int group) {
 cudaError_t launch_decode(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                           const DecodeParams &p, dim3 grid, cudaStream_t stream) {
     if (p.window > 0) return launch_decode_window(head_dim, group, tk, tv, p, grid, stream);
-    return launch_decode_cfg<false>(head_dim, group, tk, tv, p, grid, stream);
+    return launch_decode_cfg<false, false>(head_dim, group, tk, tv, p, grid, stream);
+}
+
+cudaError_t launch_decode_fp8(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
+                              const DecodeParams &p, dim3 grid, cudaStream_t stream) {
+    if (p.window > 0) return launch_decode_fp8_window(head_dim, group, tk, tv, p, grid, stream);
+    return launch_decode_fp8_full(head_dim, group, tk, tv, p, grid, stream);
 }
 
 cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, cudaStream_t stream) {

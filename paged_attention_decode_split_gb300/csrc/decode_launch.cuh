@@ -7,11 +7,11 @@
 
 namespace pa {
 
-template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN>
+template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8>
 cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, dim3 grid,
                             cudaStream_t stream, int slot) {
-    using C = DecodeCfg<D, G, TS, NST, SPS, HG>;
-    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS, HG, WIN>;
+    using C = DecodeCfg<D, G, TS, NST, SPS, HG, F8 ? 1 : 2>;
+    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS, HG, WIN, F8>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the kernel's set-up overlaps the previous
@@ -36,34 +36,62 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
 // warps, 168 registers); groups of 1 and 2 run 6 streams x 2 stages, one
 // warp per chunk; 12 heads split into 2 head groups of 6 (4 warps per chunk,
 // 2 streams x 6 stages).  D = 128: 12 streams x 2 x 8 KiB for small groups,
-// else the tokens split over 2 warps.
-template <bool WIN>
+// else the tokens split over 2 warps.  An fp8 cache halves the stage, and
+// each stream owns twice the stages: the same bytes in flight per SM.
+template <bool WIN, bool F8>
 cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                               const DecodeParams &p, dim3 grid, cudaStream_t stream) {
-    constexpr int slot0 = WIN ? 16 : 0;  // shared-memory limit bookkeeping per kernel
+    // shared-memory limit bookkeeping: one slot per kernel
+    constexpr int slot0 = (WIN ? 16 : 0) + (F8 ? 34 : 0);
+    if constexpr (F8) {
+        if (head_dim == 256) {
+            switch (group) {
+                case 1: return launch_decode_t<256, 1, 1, 6, 4, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 0);
+                case 2: return launch_decode_t<256, 2, 1, 6, 4, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 1);
+                case 4: return launch_decode_t<256, 4, 2, 4, 6, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 2);
+                case 6: return launch_decode_t<256, 6, 2, 4, 6, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 3);
+                case 12: return launch_decode_t<256, 12, 2, 2, 12, 2, WIN, F8>(tk, tv, p, grid, stream, slot0 + 9);
+            }
+        } else if (head_dim == 128) {
+            switch (group) {
+                case 1: return launch_decode_t<128, 1, 1, 12, 4, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 4);
+                case 2: return launch_decode_t<128, 2, 1, 12, 4, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 5);
+                case 4: return launch_decode_t<128, 4, 2, 6, 8, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 6);
+                case 6: return launch_decode_t<128, 6, 2, 4, 12, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 7);
+                case 8: return launch_decode_t<128, 8, 2, 4, 12, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 8);
+                case 12: return launch_decode_t<128, 12, 2, 2, 24, 2, WIN, F8>(tk, tv, p, grid, stream, slot0 + 10);
+            }
+        }
+        return cudaErrorInvalidValue;
+    }
     if (head_dim == 256) {
         switch (group) {
-            case 1: return launch_decode_t<256, 1, 1, 6, 2, 1, WIN>(tk, tv, p, grid, stream, slot0 + 0);
-            case 2: return launch_decode_t<256, 2, 1, 6, 2, 1, WIN>(tk, tv, p, grid, stream, slot0 + 1);
-            case 4: return launch_decode_t<256, 4, 2, 4, 3, 1, WIN>(tk, tv, p, grid, stream, slot0 + 2);
-            case 6: return launch_decode_t<256, 6, 2, 4, 3, 1, WIN>(tk, tv, p, grid, stream, slot0 + 3);
-            case 12: return launch_decode_t<256, 12, 2, 2, 6, 2, WIN>(tk, tv, p, grid, stream, slot0 + 9);
+            case 1: return launch_decode_t<256, 1, 1, 6, 2, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 0);
+            case 2: return launch_decode_t<256, 2, 1, 6, 2, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 1);
+            case 4: return launch_decode_t<256, 4, 2, 4, 3, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 2);
+            case 6: return launch_decode_t<256, 6, 2, 4, 3, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 3);
+            case 12: return launch_decode_t<256, 12, 2, 2, 6, 2, WIN, false>(tk, tv, p, grid, stream, slot0 + 9);
         }
     } else if (head_dim == 128) {
         switch (group) {
-            case 1: return launch_decode_t<128, 1, 1, 12, 2, 1, WIN>(tk, tv, p, grid, stream, slot0 + 4);
-            case 2: return launch_decode_t<128, 2, 1, 12, 2, 1, WIN>(tk, tv, p, grid, stream, slot0 + 5);
-            case 4: return launch_decode_t<128, 4, 2, 6, 4, 1, WIN>(tk, tv, p, grid, stream, slot0 + 6);
-            case 6: return launch_decode_t<128, 6, 2, 4, 6, 1, WIN>(tk, tv, p, grid, stream, slot0 + 7);
-            case 8: return launch_decode_t<128, 8, 2, 4, 6, 1, WIN>(tk, tv, p, grid, stream, slot0 + 8);
-            case 12: return launch_decode_t<128, 12, 2, 2, 12, 2, WIN>(tk, tv, p, grid, stream, slot0 + 10);
+            case 1: return launch_decode_t<128, 1, 1, 12, 2, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 4);
+            case 2: return launch_decode_t<128, 2, 1, 12, 2, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 5);
+            case 4: return launch_decode_t<128, 4, 2, 6, 4, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 6);
+            case 6: return launch_decode_t<128, 6, 2, 4, 6, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 7);
+            case 8: return launch_decode_t<128, 8, 2, 4, 6, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 8);
+            case 12: return launch_decode_t<128, 12, 2, 2, 12, 2, WIN, false>(tk, tv, p, grid, stream, slot0 + 10);
         }
     }
     return cudaErrorInvalidValue;
 }
 
-// the sliding-window instantiations (decode_launch_window.cu)
+// the sliding-window instantiations (decode_launch_window.cu) and the fp8
+// ones (decode_launch_fp8.cu, decode_launch_fp8_window.cu)
 cudaError_t launch_decode_window(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                                  const DecodeParams &p, dim3 grid, cudaStream_t stream);
+cudaError_t launch_decode_fp8_full(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
+                                   const DecodeParams &p, dim3 grid, cudaStream_t stream);
+cudaError_t launch_decode_fp8_window(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
+                                     const DecodeParams &p, dim3 grid, cudaStream_t stream);
 
 }  // namespace pa

@@ -6,7 +6,7 @@ namespace pa {
 
 cudaError_t launch_decode_window(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                                  const DecodeParams &p, dim3 grid, cudaStream_t stream) {
-    return launch_decode_cfg<true>(head_dim, group, tk, tv, p, grid, stream);
+    return launch_decode_cfg<true, false>(head_dim, group, tk, tv, p, grid, stream);
 }
 
 }  // namespace pa

@@ -67,20 +67,22 @@ struct DecodeParams {
     int out_bf16;
     int early_kv;         // stream the context before the new row ahead of the dependency wait
     int window;           // 0: full attention; W > 0: only the last W keys
+    const float *k_scale; // fp8 cache: [Hkv] dequantisation scales of K and V
+    const float *v_scale;
 };
 
 // D: head_dim.  G: query heads per KV head.  TS x HG warps share one chunk,
 // each taking 16 / TS of its tokens and G / HG of the heads (HG > 1 only
 // for groups too wide for one warp's registers).  NST: chunk streams
 // (consumer warps = TS * HG * NST).  SPS: stages owned by each stream (NS =
-// NST * SPS in all).
+// NST * SPS in all).  KVB: bytes per cached element (2 bf16, 1 fp8 e4m3).
 //
 // Stage ownership matters for correctness: an mbarrier wait tests the parity
 // of a phase, so a waiter must never run two phases ahead of the barrier.
 // Each stream therefore owns SPS stages and cycles through them in order; it
 // has consumed every earlier phase of a stage before it waits on the next,
 // and the producer waits on every phase of a stage's empty barrier in order.
-template <int D, int G, int TS, int NST, int SPS, int HG>
+template <int D, int G, int TS, int NST, int SPS, int HG, int KVB = 2>
 struct DecodeCfg {
     static constexpr int NS = NST * SPS;
     static constexpr int E = D / 32;
@@ -89,7 +91,7 @@ struct DecodeCfg {
     static constexpr int WPC = TS * HG;                  // warps per chunk
     static constexpr int NWC = WPC * NST;                // consumer warps
     static constexpr int NWH = TS * NST;                 // warps holding a given head
-    static constexpr int ROW_BYTES = D * 2;
+    static constexpr int ROW_BYTES = D * KVB;
     static constexpr int CHUNK_BYTES = kChunk * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;  // K chunk, then V chunk
     static constexpr int GP2 = (GW + 1) & ~1;            // (p, p) pairs per P row (16-byte rows)
@@ -125,6 +127,37 @@ __device__ __forceinline__ void load_bf16_pairs(const uint8_t *src, float2 (&f)[
     }
 }
 
+// E consecutive e4m3 codes of a row -> E/2 float pairs (exact: every e4m3
+// value is an f16 value, and every f16 value an fp32 one).
+__device__ __forceinline__ void e4m3x4_to_float(uint32_t w, float2 &a, float2 &b) {
+    uint32_t h0, h1;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(w));
+    a = __half22float2(*reinterpret_cast<const __half2 *>(&h0));
+    b = __half22float2(*reinterpret_cast<const __half2 *>(&h1));
+}
+
+template <int E>
+__device__ __forceinline__ void load_e4m3_pairs(const uint8_t *src, float2 (&f)[E / 2]) {
+    if constexpr (E == 8) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(src);
+        e4m3x4_to_float(w.x, f[0], f[1]);
+        e4m3x4_to_float(w.y, f[2], f[3]);
+    } else {
+        e4m3x4_to_float(*reinterpret_cast<const uint32_t *>(src), f[0], f[1]);
+    }
+}
+
+template <int E, bool F8>
+__device__ __forceinline__ void load_kv_pairs(const uint8_t *src, float2 (&f)[E / 2]) {
+    if constexpr (F8)
+        load_e4m3_pairs<E>(src, f);
+    else
+        load_bf16_pairs<E>(src, f);
+}
+
 __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int out_bf16) {
     if (out_bf16)
         reinterpret_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
@@ -133,12 +166,15 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
 }
 
 // WIN: the sliding-window variant (a separate instantiation, so the full-
-// attention kernel carries none of its bookkeeping).
-template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN>
+// attention kernel carries none of its bookkeeping).  F8: the cache holds fp8
+// e4m3 codes with one scale per KV head for K and for V; the K scale is folded
+// into q and the V scale into the merge weights, so the inner loops only
+// widen codes instead of bf16 values.
+template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8 = false>
 __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
     pa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecodeParams p) {
-    using C = DecodeCfg<D, G, TS, NST, SPS, HG>;
+    using C = DecodeCfg<D, G, TS, NST, SPS, HG, F8 ? 1 : 2>;
     constexpr int E = C::E, MB = C::MB, NWC = C::NWC, NS = C::NS, GW = C::GW, WPC = C::WPC, NWH = C::NWH;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -308,7 +344,8 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
         {
             const uint8_t *qrow =
                 reinterpret_cast<const uint8_t *>(p.q + ((size_t)b * p.num_q_heads + hq0 + hg * GW) * D) + lane * E * 2;
-            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float qs = F8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;
+            const float2 sc2 = make_float2(qs, qs);
 #pragma unroll
             for (int g = 0; g < GW; ++g) {
                 load_bf16_pairs<E>(qrow + g * D * 2, q2[g]);
@@ -331,7 +368,7 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
                 flags[0] = 1;
                 break;
             }
-            const uint8_t *kst = smem + s * C::STAGE_BYTES + wh * 8 * C::ROW_BYTES + lane * E * 2;
+            const uint8_t *kst = smem + s * C::STAGE_BYTES + wh * 8 * C::ROW_BYTES + lane * E * (F8 ? 1 : 2);
             const uint8_t *vst = kst + C::CHUNK_BYTES;
             // valid rows [lead, nv) of this warp's part of the chunk: nv may be
             // <= lead in the last chunk, lead > 0 only where the window starts
@@ -351,7 +388,7 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
                     for (int h = 0; h < 2; ++h) {
                         const int slot = j + 4 * h;
                         float2 k2[E / 2];
-                        load_bf16_pairs<E>(kst + (mb * 8 + (slot ^ cg)) * C::ROW_BYTES, k2);
+                        load_kv_pairs<E, F8>(kst + (mb * 8 + (slot ^ cg)) * C::ROW_BYTES, k2);
 #pragma unroll
                         for (int g = 0; g < GW; ++g) {
                             float2 a = __fmul2_rn(q2[g][0], k2[0]);
@@ -427,7 +464,7 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
 
                 auto pv_row = [&](int t) {
                     float2 v2[E / 2];
-                    load_bf16_pairs<E>(vst + t * C::ROW_BYTES, v2);
+                    load_kv_pairs<E, F8>(vst + t * C::ROW_BYTES, v2);
                     float2 pp[C::GP2];
 #pragma unroll
                     for (int j = 0; j < C::GP2; j += 2) {
@@ -510,7 +547,7 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
             for (int o = 1; o < NWP; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
             const bool zero = poisoned || !(lsum > 0.f);
             if (mine) {
-                wgt[slot] = zero ? 0.f : e / lsum;
+                wgt[slot] = zero ? 0.f : (F8 ? e / lsum * p.v_scale[kvh] : e / lsum);
                 if (k == 0 && p.num_splits > 1)
                     p.part_ml[((size_t)b * p.num_q_heads + hq0 + h) * p.num_splits + split] =
                         make_float2(M, poisoned ? -1.f : lsum);

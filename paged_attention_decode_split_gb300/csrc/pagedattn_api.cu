@@ -133,7 +133,7 @@ pa_status make_plan(const pa_attn_desc *d, bool verify, Plan *pl) {
     return PA_OK;
 }
 
-// ---- TMA descriptors of a [P, BS, Hkv, D] bf16 cache ------------------------
+// ---- TMA descriptors of a [P, BS, Hkv, D] bf16 or fp8 cache -----------------
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -153,17 +153,19 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// Box = [box_d elements of d, 1 head, 16 tokens, 1 page].
-bool encode_cache_map(CUtensorMap *map, const void *base, const pa_attn_desc *d, int box_d, bool swizzle128) {
+// Box = [box_d elements of d, 1 head, 16 tokens, 1 page]; fp8: one-byte elements.
+bool encode_cache_map(CUtensorMap *map, const void *base, const pa_attn_desc *d, int box_d, bool swizzle128,
+                      bool fp8 = false) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)d->head_dim, (cuuint64_t)d->num_kv_heads, (cuuint64_t)d->block_size,
                                 (cuuint64_t)d->num_pages};
-    const cuuint64_t row = (cuuint64_t)d->head_dim * 2;
+    const cuuint64_t row = (cuuint64_t)d->head_dim * (fp8 ? 1 : 2);
     const cuuint64_t strides[3] = {row, row * d->num_kv_heads, row * d->num_kv_heads * d->block_size};
     const cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)kChunk, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                    const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -259,6 +261,49 @@ __global__ void __launch_bounds__(128) pa_reshape_and_cache_kernel(const uint4 *
     }
 }
 
+// fp8 variant: a thread turns 8 bf16 of a row into 8 e4m3 codes, code =
+// e4m3(x / scale[kv head]) with the division in binary32, rounding to nearest
+// even and saturating to +-448 (cvt ... satfinite).
+__device__ __forceinline__ uint32_t e4m3x2_div(uint32_t two_bf16, float s) {
+    const float lo = __fdiv_rn(bf16lo(two_bf16), s), hi = __fdiv_rn(bf16hi(two_bf16), s);
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint2 e4m3x8_div(uint4 w, float s) {
+    return make_uint2(e4m3x2_div(w.x, s) | (e4m3x2_div(w.y, s) << 16), e4m3x2_div(w.z, s) | (e4m3x2_div(w.w, s) << 16));
+}
+
+__global__ void __launch_bounds__(128) pa_reshape_and_cache_fp8_kernel(
+    const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, uint2 *__restrict__ k_cache,
+    uint2 *__restrict__ v_cache, const int64_t *__restrict__ slots, const float *__restrict__ k_scale,
+    const float *__restrict__ v_scale, int row_vecs, int head_vecs, int64_t num_slots, int32_t *status) {
+    pdl_launch_dependents();
+    pdl_wait_primary();
+    const int i = blockIdx.x;
+    const int64_t s = slots[i];
+    if (s < 0) return;
+    if (s >= num_slots) {
+        if (threadIdx.x == 0) set_status(status, PA_DEV_BAD_SLOT);
+        return;
+    }
+    const uint4 *ks = k_new + (size_t)i * row_vecs;
+    const uint4 *vs = v_new + (size_t)i * row_vecs;
+    uint2 *kd = k_cache + (size_t)s * row_vecs;
+    uint2 *vd = v_cache + (size_t)s * row_vecs;
+    for (int j = threadIdx.x; j < row_vecs; j += blockDim.x) {
+        const int h = j / head_vecs;
+        kd[j] = e4m3x8_div(ks[j], k_scale[h]);
+        vd[j] = e4m3x8_div(vs[j], v_scale[h]);
+    }
+}
+
+pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                      const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
+                      const pa_attn_desc *desc, void *out, void *workspace, size_t workspace_bytes,
+                      int32_t *device_status, void *stream);
+
 }  // namespace pa
 
 using namespace pa;
@@ -329,63 +374,57 @@ pa_status pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cac
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_reshape_and_cache_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                   const int64_t *slot_mapping, const float *k_scale, const float *v_scale,
+                                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int64_t num_pages, int32_t *device_status, void *stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || num_pages < 1)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping || !k_scale || !v_scale)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+        return PA_ERR_INVALID_ARG;
+    // a thread converts 8 elements of one head: head_dim must be a multiple of 8
+    if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+    const int64_t row_vecs = static_cast<int64_t>(num_kv_heads) * head_dim / 8;
+    if (row_vecs > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_tokens));
+    cfg.blockDim = dim3(128);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, pa_reshape_and_cache_fp8_kernel, static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+        static_cast<uint2 *>(k_cache), static_cast<uint2 *>(v_cache), slot_mapping, k_scale, v_scale,
+        static_cast<int>(row_vecs), head_dim / 8, num_pages * block_size, device_status);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
                                     const int32_t *block_table, const int32_t *seq_lens, const pa_attn_desc *desc,
                                     void *out, void *workspace, size_t workspace_bytes, int32_t *device_status,
                                     void *stream) {
-    pa_status st = check_desc(desc, false);
-    if (st != PA_OK) return st;
-    if (desc->num_seqs == 0) return PA_OK;
-    st = check_common_ptrs(q, k_cache, v_cache, block_table, seq_lens, out);
-    if (st != PA_OK) return st;
-    Plan pl;
-    st = make_plan(desc, false, &pl);
-    if (st != PA_OK) return st;
-    st = check_workspace(pl, workspace, workspace_bytes);
-    if (st != PA_OK) return st;
+    return decode_call(q, k_cache, v_cache, nullptr, nullptr, block_table, seq_lens, desc, out, workspace,
+                       workspace_bytes, device_status, stream);
+}
 
-    CUtensorMap tk, tv;
-    if (!encode_cache_map(&tk, k_cache, desc, desc->head_dim, false) ||
-        !encode_cache_map(&tv, v_cache, desc, desc->head_dim, false))
-        return PA_ERR_CUDA;
-
-    const int group = desc->num_q_heads / desc->num_kv_heads;
-    DecodeParams p;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.out = out;
-    p.part_o = static_cast<float *>(workspace);
-    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
-    p.status = device_status;
-    p.num_pages = desc->num_pages;
-    p.num_q_heads = desc->num_q_heads;
-    p.max_pages_per_seq = desc->max_pages_per_seq;
-    p.max_seq_len = desc->max_seq_len;
-    p.block_size = desc->block_size;
-    p.chunks_per_split = pl.chunks_per_split;
-    p.num_splits = pl.num_splits;
-    p.scale_log2 = desc->scale * 1.4426950408889634f;
-    p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
-    p.early_kv = (desc->flags & PA_FLAG_EARLY_KV_READ) != 0;
-    p.window = desc->window;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);
-    if (launch_decode(desc->head_dim, group, tk, tv, p, grid, s) != cudaSuccess) return PA_ERR_CUDA;
-    if (pl.num_splits > 1) {
-        ReduceParams r;
-        r.part_o = p.part_o;
-        r.part_ml = p.part_ml;
-        r.out = out;
-        r.num_q_heads = desc->num_q_heads;
-        r.num_splits = pl.num_splits;
-        r.out_bf16 = p.out_bf16;
-        if (launch_reduce(desc->head_dim, r, desc->num_seqs, s) != cudaSuccess)
-            return PA_ERR_CUDA;
-    }
-    record_plan(PA_PATH_DECODE_CUDA_CORE, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
-    return PA_OK;
+pa_status pa_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                        const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                        const int32_t *seq_lens, const pa_attn_desc *desc, void *out,
+                                        void *workspace, size_t workspace_bytes, int32_t *device_status,
+                                        void *stream) {
+    if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+        return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, desc, out, workspace,
+                       workspace_bytes, device_status, stream);
 }
 
 pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const void *v_cache,
@@ -460,3 +499,72 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
 }
 
 }  // extern "C"
+
+namespace pa {
+
+// Decode over a bf16 cache (k_scale == nullptr) or an fp8 e4m3 cache.
+pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                      const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
+                      const pa_attn_desc *desc, void *out, void *workspace, size_t workspace_bytes,
+                      int32_t *device_status, void *stream) {
+    const bool fp8 = k_scale != nullptr;
+    pa_status st = check_desc(desc, false);
+    if (st != PA_OK) return st;
+    if (desc->num_seqs == 0) return PA_OK;
+    st = check_common_ptrs(q, k_cache, v_cache, block_table, seq_lens, out);
+    if (st != PA_OK) return st;
+    Plan pl;
+    st = make_plan(desc, false, &pl);
+    if (st != PA_OK) return st;
+    st = check_workspace(pl, workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+
+    CUtensorMap tk, tv;
+    if (!encode_cache_map(&tk, k_cache, desc, desc->head_dim, false, fp8) ||
+        !encode_cache_map(&tv, v_cache, desc, desc->head_dim, false, fp8))
+        return PA_ERR_CUDA;
+
+    const int group = desc->num_q_heads / desc->num_kv_heads;
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
+    p.status = device_status;
+    p.num_pages = desc->num_pages;
+    p.num_q_heads = desc->num_q_heads;
+    p.max_pages_per_seq = desc->max_pages_per_seq;
+    p.max_seq_len = desc->max_seq_len;
+    p.block_size = desc->block_size;
+    p.chunks_per_split = pl.chunks_per_split;
+    p.num_splits = pl.num_splits;
+    p.scale_log2 = desc->scale * 1.4426950408889634f;
+    p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
+    p.early_kv = (desc->flags & PA_FLAG_EARLY_KV_READ) != 0;
+    p.window = desc->window;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);
+    const cudaError_t e = fp8 ? launch_decode_fp8(desc->head_dim, group, tk, tv, p, grid, s)
+                              : launch_decode(desc->head_dim, group, tk, tv, p, grid, s);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (pl.num_splits > 1) {
+        ReduceParams r;
+        r.part_o = p.part_o;
+        r.part_ml = p.part_ml;
+        r.out = out;
+        r.num_q_heads = desc->num_q_heads;
+        r.num_splits = pl.num_splits;
+        r.out_bf16 = p.out_bf16;
+        if (launch_reduce(desc->head_dim, r, desc->num_seqs, s) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    record_plan(PA_PATH_DECODE_CUDA_CORE, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
+    return PA_OK;
+}
+
+}  // namespace pa

@@ -11,7 +11,12 @@ Recipe (every draw comes from one ``torch.Generator`` seeded per problem):
      pages lie scattered at random through one shared pool;
   3. q ~ N(0, 1) in bf16, shape [B * q_len, Hq, D];
   4. for each layer, k_cache and v_cache ~ N(0, 1) in bf16, [P, BS, Hkv, D]
-     (unused slots hold random data too, or NaN with ``poison_unused``).
+     (unused slots hold random data too, or NaN with ``poison_unused``);
+     with ``kv_fp8`` the caches hold e4m3 codes instead: N(0, 1) draws clipped
+     to +-6.5, divided by the per-KV-head scale and cast by torch's
+     float8_e4m3fn type, with scales k_scale[h] = (1 + h/4) / 64 and
+     v_scale[h] = (1 + h/8) / 48 (so |x / scale| < 448), NaN code 0x7F in
+     poisoned slots.
 Unused block-table entries are -1 so that a kernel that reads past the pages
 of a sequence trips its bounds check.
 """
@@ -23,6 +28,7 @@ from dataclasses import dataclass, field
 import torch
 
 BF16_NAN_BITS = 0x7FC0
+E4M3_NAN_CODE = 0x7F
 
 
 @dataclass
@@ -40,6 +46,9 @@ class PagedProblem:
     q: list = field(default_factory=list)        # per layer: bf16 [B*q_len, Hq, D]
     k_cache: list = field(default_factory=list)  # per layer: bf16 [P, BS, Hkv, D]
     v_cache: list = field(default_factory=list)
+    kv_fp8: bool = False
+    k_scale: list = field(default_factory=list)  # fp8 only, per layer: float32 [Hkv]
+    v_scale: list = field(default_factory=list)
 
     @property
     def max_pages_per_seq(self) -> int:
@@ -72,10 +81,22 @@ def _randn_bf16(shape, gen, device):
     return torch.randn(shape, generator=gen, dtype=torch.float32, device=device).to(torch.bfloat16)
 
 
+def fp8_scales(num_kv_heads: int, device: str = "cpu"):
+    """The synthetic per-KV-head scales of an fp8 cache (K, V)."""
+    h = torch.arange(num_kv_heads, dtype=torch.float32, device=device)
+    return (1 + h / 4) / 64, (1 + h / 8) / 48
+
+
+def _e4m3_codes(shape, gen, device, scale):
+    x = torch.randn(shape, generator=gen, dtype=torch.float32, device=device).clamp_(-6.5, 6.5)
+    x /= scale.view(1, 1, -1, 1)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
 def make_problem(seed: int, *, num_seqs: int, seq_lens, num_q_heads: int, num_kv_heads: int,
                  head_dim: int, block_size: int, q_len: int = 1, num_layers: int = 1,
                  pool_pages: int | None = None, pool_factor: float = 1.1, scale: float | None = None,
-                 device: str = "cpu", poison_unused: bool = False) -> PagedProblem:
+                 device: str = "cpu", poison_unused: bool = False, kv_fp8: bool = False) -> PagedProblem:
     """Draw one paged-attention problem.
 
     ``seq_lens`` is an int (same length for all), a list of ints, or a tuple
@@ -110,18 +131,27 @@ def make_problem(seed: int, *, num_seqs: int, seq_lens, num_q_heads: int, num_kv
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
     prob = PagedProblem(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, pool_pages,
-                        float(scale), torch.tensor(lens, dtype=torch.int32), block_table)
+                        float(scale), torch.tensor(lens, dtype=torch.int32), block_table, kv_fp8=kv_fp8)
+    cache_shape = (pool_pages, block_size, num_kv_heads, head_dim)
     for _ in range(num_layers):
         prob.q.append(_randn_bf16((num_seqs * q_len, num_q_heads, head_dim), gen, device))
-        prob.k_cache.append(_randn_bf16((pool_pages, block_size, num_kv_heads, head_dim), gen, device))
-        prob.v_cache.append(_randn_bf16((pool_pages, block_size, num_kv_heads, head_dim), gen, device))
+        if kv_fp8:
+            ks, vs = fp8_scales(num_kv_heads, device)
+            prob.k_scale.append(ks)
+            prob.v_scale.append(vs)
+            prob.k_cache.append(_e4m3_codes(cache_shape, gen, device, ks))
+            prob.v_cache.append(_e4m3_codes(cache_shape, gen, device, vs))
+        else:
+            prob.k_cache.append(_randn_bf16(cache_shape, gen, device))
+            prob.v_cache.append(_randn_bf16(cache_shape, gen, device))
     if poison_unused:
         poison_unused_slots(prob)
     return prob
 
 
 def poison_unused_slots(prob: PagedProblem) -> None:
-    """Fill every cache slot no sequence uses with bf16 NaN bits."""
+    """Fill every cache slot no sequence uses with NaN (bf16 NaN bits, or the
+    e4m3 NaN code in an fp8 cache)."""
     for kc, vc in zip(prob.k_cache, prob.v_cache):
         used = torch.zeros((prob.num_pages, prob.block_size), dtype=torch.bool)
         bt = prob.block_table.cpu()
@@ -130,7 +160,10 @@ def poison_unused_slots(prob: PagedProblem) -> None:
                 n = min(prob.block_size, L - lp * prob.block_size)
                 used[int(bt[b, lp]), :n] = True
         mask = (~used).to(kc.device)
-        nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16, device=kc.device).view(torch.bfloat16)
+        if prob.kv_fp8:
+            nan = torch.tensor(E4M3_NAN_CODE, dtype=torch.uint8, device=kc.device)
+        else:
+            nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16, device=kc.device).view(torch.bfloat16)
         kc[mask] = nan
         vc[mask] = nan
 
@@ -160,6 +193,10 @@ WORKLOADS = {
                                       head_dim=256, block_size=832, scale=1.0 / 16, q_len=16,
                                       num_layers=1),
     # wider GQA: 48 query heads on the same 4 KV heads (12 per group)
+    # the hybrid layer over an fp8 e4m3 cache (half the KV bytes)
+    "decode_fp8_l32768_bs784": dict(num_seqs=1, seq_lens=32768, num_q_heads=24, num_kv_heads=4,
+                                    head_dim=256, block_size=784, scale=1.0 / 16, q_len=1,
+                                    num_layers=16, kv_fp8=True),
     "decode_g12_l32768_bs784": dict(num_seqs=1, seq_lens=32768, num_q_heads=48, num_kv_heads=4,
                                     head_dim=256, block_size=784, scale=1.0 / 16, q_len=1,
                                     num_layers=16),

@@ -37,9 +37,14 @@ def desc_for(prob, *, num_splits=0, out_dtype=pa.PA_OUT_F32, max_seq_len=None, w
                         window=window, flags=flags)
 
 
+def scales_dev(prob, layer=0, device="cuda"):
+    return prob.k_scale[layer].to(device), prob.v_scale[layer].to(device)
+
+
 def run_attention(prob, layer=0, *, num_splits=0, out_dtype=pa.PA_OUT_F32, max_seq_len=None, tensors=None,
                   window=0, flags=0):
-    """Runs decode (q_len 1) or verify through the C ABI; returns (out on CPU, status, plan)."""
+    """Runs decode (q_len 1; over the fp8 cache for an fp8 problem) or verify
+    through the C ABI; returns (out on CPU, status, plan)."""
     q, kc, vc, bt, sl = tensors if tensors is not None else to_dev(prob, layer)
     desc = desc_for(prob, num_splits=num_splits, out_dtype=out_dtype, max_seq_len=max_seq_len, window=window,
                     flags=flags)
@@ -48,8 +53,12 @@ def run_attention(prob, layer=0, *, num_splits=0, out_dtype=pa.PA_OUT_F32, max_s
     out = torch.full((prob.num_seqs * prob.q_len, prob.num_q_heads, prob.head_dim), float("nan"), dtype=dtype,
                      device=q.device)
     status = torch.zeros(1, dtype=torch.int32, device=q.device)
-    fn = pa.paged_attention_decode if prob.q_len == 1 else pa.paged_attention_verify
-    fn(q, kc, vc, bt, sl, desc, out, ws, status)
+    if prob.kv_fp8:
+        ks, vs = scales_dev(prob, layer, q.device)
+        pa.paged_attention_decode_fp8(q, kc, vc, ks, vs, bt, sl, desc, out, ws, status)
+    else:
+        fn = pa.paged_attention_decode if prob.q_len == 1 else pa.paged_attention_verify
+        fn(q, kc, vc, bt, sl, desc, out, ws, status)
     torch.cuda.synchronize()
     return out.float().cpu(), int(status.item()), pa.last_plan()
 
@@ -61,6 +70,10 @@ def oracle_out(oracle_mod, prob, layer=0, rows=None, window=0):
         idx = torch.tensor(rows)
         qi = torch.cat([torch.arange(b * prob.q_len, (b + 1) * prob.q_len) for b in rows])
         q, bt, sl = q[qi].contiguous(), bt[idx].contiguous(), sl[idx].contiguous()
+    if prob.kv_fp8:
+        return oracle_mod.paged_attention_fp8(q, prob.k_cache[layer].cpu(), prob.v_cache[layer].cpu(),
+                                              prob.k_scale[layer].cpu(), prob.v_scale[layer].cpu(), bt.numpy(),
+                                              sl.numpy(), prob.scale, q_len=prob.q_len, window=window)
     return oracle_mod.paged_attention(q, prob.k_cache[layer].cpu(), prob.v_cache[layer].cpu(), bt.numpy(),
                                       sl.numpy(), prob.scale, q_len=prob.q_len, window=window)
 

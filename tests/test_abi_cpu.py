@@ -174,3 +174,19 @@ def test_hybrid_page_tokens_matches_oracle(lib, oracle_mod):
     # a group larger than any state page: one group; a page past int64: -1
     assert lib.pa_hybrid_page_tokens(5, 1 << 62, 64) == 64
     assert lib.pa_hybrid_page_tokens((1 << 63) - 1, 1, 1 << 30) == -1
+
+
+def test_fp8_entries_reject_bad_arguments(lib):
+    dec = lib.pa_paged_attention_decode_fp8
+    desc = hybrid_desc()
+    args = lambda ks, vs, d: (FAKE, FAKE, FAKE, ks, vs, FAKE, FAKE, ctypes.byref(d), FAKE, FAKE, 1 << 30, None, None)
+    assert dec(*args(None, FAKE, desc)) == pa.PA_ERR_INVALID_ARG       # scales are required
+    assert dec(*args(FAKE, None, desc)) == pa.PA_ERR_INVALID_ARG
+    assert dec(*args(FAKE + 2, FAKE, desc)) == pa.PA_ERR_INVALID_ARG   # misaligned float
+    assert dec(*args(FAKE, FAKE, hybrid_desc(num_q_heads=40))) == pa.PA_ERR_UNSUPPORTED  # G = 10
+    assert dec(*args(FAKE, FAKE, hybrid_desc(flags=2))) == pa.PA_ERR_INVALID_ARG
+    rc = lib.pa_reshape_and_cache_fp8
+    assert rc(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, 4, 256, 16, 10, None, None) == pa.PA_ERR_INVALID_ARG
+    assert rc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 12, 16, 10, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert rc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 256, 16, 10, None, None) == pa.PA_ERR_INVALID_ARG
+    assert rc(None, None, None, None, None, None, None, 0, 4, 256, 16, 10, None, None) == pa.PA_OK

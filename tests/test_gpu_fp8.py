@@ -1,0 +1,219 @@
+"""GPU parity of the fp8 e4m3 KV cache: the quantising reshape_and_cache must
+give the oracle's codes bit for bit, and decode over the codes must match the
+oracle's attention over the decoded values (K = code x k_scale[kv head], V
+likewise) within the bf16-path tolerance.  Edge cases: ties and saturation in
+the quantiser, NaN-poisoned unused slots, ragged tails, forced splits, every
+compiled group size, a sliding window, bf16 output, the early-K/V flag and the
+chain reshape_and_cache -> decode on one stream."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import paged_attention_decode_split_gb300 as pa
+from paged_attention_decode_split_gb300 import _build
+from paged_attention_decode_split_gb300.inputs import WORKLOADS, make_new_tokens, make_problem
+from tests.gpu_common import assert_parity, desc_for, oracle_out, run_attention, scales_dev, to_dev
+from tests.helpers import bits
+
+pytestmark = pytest.mark.gpu
+
+TAIL_LENGTHS = [1, 15, 16, 17, 63, 64, 65, 783, 784, 785, 831, 832, 833]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _build.build()
+    pa.load_library()
+
+
+def hybrid(seed, lens, bs, **kw):
+    args = dict(num_seqs=len(lens), seq_lens=list(lens), num_q_heads=24, num_kv_heads=4, head_dim=256,
+                block_size=bs, scale=1 / 16, kv_fp8=True)
+    args.update(kw)
+    return make_problem(seed, **args)
+
+
+# -- quantising reshape_and_cache -------------------------------------------------------
+
+def _reshape_fp8_both(oracle_mod, k_new, v_new, ks, vs, slots, P, bs):
+    hkv, d = k_new.shape[1], k_new.shape[2]
+    kc = torch.full((P, bs, hkv, d), 0x33, dtype=torch.uint8)
+    vc = torch.full((P, bs, hkv, d), 0x44, dtype=torch.uint8)
+    kc_d, vc_d = kc.cuda(), vc.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.reshape_and_cache_fp8(k_new.cuda(), v_new.cuda(), kc_d, vc_d, slots.cuda(), ks.cuda(), vs.cuda(), status)
+    torch.cuda.synchronize()
+    k_ref, v_ref = kc.numpy().copy(), vc.numpy().copy()
+    oracle_mod.reshape_and_cache_fp8(bits(k_new), bits(v_new), k_ref, v_ref, slots.numpy(), ks.numpy(), vs.numpy())
+    return kc_d.cpu().numpy(), vc_d.cpu().numpy(), k_ref, v_ref, int(status.item())
+
+
+@pytest.mark.parametrize("hkv,d", [(4, 256), (8, 128), (1, 8)])
+def test_reshape_and_cache_fp8_bit_exact(oracle_mod, hkv, d):
+    P, bs, n = 7, 16, 40
+    k_new, v_new = make_new_tokens(31 + d, n, hkv, d)
+    k_new = k_new * 3  # spread over more binades
+    g = torch.Generator().manual_seed(d)
+    slots = torch.randperm(P * bs, generator=g)[:n].to(torch.int64)
+    slots[5] = -1
+    ks = torch.tensor([0.013 * (1 + h) for h in range(hkv)], dtype=torch.float32)
+    vs = torch.tensor([0.05 / (1 + h) for h in range(hkv)], dtype=torch.float32)
+    kg, vg, kr, vr, st = _reshape_fp8_both(oracle_mod, k_new, v_new, ks, vs, slots, P, bs)
+    assert st == 0
+    assert np.array_equal(kg, kr) and np.array_equal(vg, vr)
+
+
+def test_reshape_and_cache_fp8_ties_saturation_and_subnormals(oracle_mod):
+    """Values at e4m3 rounding midpoints (scale 1: the division is exact), past
+    448 and +-inf, subnormal and underflowing ones: nearest-even and
+    saturation agree with the oracle bit for bit."""
+    vals = oracle_mod.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    pos = sorted(set(vals.tolist()))
+    mids = [(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])]  # need 4 mantissa bits: exact in bf16
+    special = [448.0, 450.0, 464.0, 480.0, 8192.0, float("inf"), 2.0 ** -10, 2.0 ** -11, 3 * 2.0 ** -11, 0.0]
+    row = torch.tensor(mids + special + [-x for x in mids + special], dtype=torch.float64)
+    d = 8
+    n = math.ceil(row.numel() / d)
+    row = torch.cat([row, torch.zeros(n * d - row.numel(), dtype=torch.float64)])
+    assert torch.equal(row.to(torch.bfloat16).double(), row)  # every value is exact in bf16
+    k_new = row.to(torch.bfloat16).view(n, 1, d)
+    v_new = (-row).to(torch.bfloat16).view(n, 1, d)
+    one = torch.ones(1, dtype=torch.float32)
+    slots = torch.arange(n, dtype=torch.int64)
+    kg, vg, kr, vr, st = _reshape_fp8_both(oracle_mod, k_new, v_new, one, one, slots, math.ceil(n / 16), 16)
+    assert st == 0
+    assert np.array_equal(kg, kr) and np.array_equal(vg, vr)
+
+
+def test_reshape_and_cache_fp8_bad_slot_flagged(oracle_mod):
+    """A slot past the pool sets PA_DEV_BAD_SLOT and writes nothing; the other
+    tokens land as the oracle puts them (it skips the bad token here)."""
+    k_new, v_new = make_new_tokens(5, 3, 2, 16)
+    one = torch.ones(2, dtype=torch.float32)
+    kc = torch.zeros((2, 16, 2, 16), dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.tensor([0, 999, 3], dtype=torch.int64)
+    pa.reshape_and_cache_fp8(k_new.cuda(), v_new.cuda(), kc, vc, slots.cuda(), one.cuda(), one.cuda(), status)
+    torch.cuda.synchronize()
+    assert status.item() & pa.PA_DEV_BAD_SLOT
+    k_ref = np.zeros((2, 16, 2, 16), np.uint8)
+    v_ref = np.zeros_like(k_ref)
+    oracle_mod.reshape_and_cache_fp8(bits(k_new), bits(v_new), k_ref, v_ref, np.array([0, -1, 3], np.int64),
+                                     one.numpy(), one.numpy())
+    assert np.array_equal(kc.cpu().numpy(), k_ref) and np.array_equal(vc.cpu().numpy(), v_ref)
+
+
+# -- decode over the fp8 cache ---------------------------------------------------------
+
+@pytest.mark.parametrize("bs", [16, 784, 832])
+def test_decode_fp8_ragged_tails_nan_poisoned(oracle_mod, bs):
+    prob = hybrid(501 + bs, TAIL_LENGTHS, bs, poison_unused=True)
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_DECODE_CUDA_CORE
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"fp8 tails bs={bs}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 64])
+def test_decode_fp8_forced_splits(oracle_mod, splits):
+    prob = hybrid(511, [5000, 333, 1], 784, poison_unused=True)
+    out, status, _ = run_attention(prob, num_splits=splits)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"fp8 splits={splits}")
+
+
+@pytest.mark.parametrize("G,hkv", [(1, 4), (2, 4), (4, 2), (6, 4), (12, 4)])
+def test_decode_fp8_group_sizes_d256(oracle_mod, G, hkv):
+    prob = hybrid(521 + G, [700, 1500, 9], 16, num_q_heads=G * hkv, num_kv_heads=hkv)
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"fp8 G={G}")
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 6, 8, 12])
+def test_decode_fp8_dense_d128(oracle_mod, G):
+    prob = make_problem(531 + G, num_seqs=3, seq_lens=[1, 100, 2049], num_q_heads=8 * G, num_kv_heads=8,
+                        head_dim=128, block_size=16, scale=1 / math.sqrt(128), poison_unused=True, kv_fp8=True)
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"fp8 dense G={G}")
+
+
+@pytest.mark.parametrize("window", [2048, 17])
+def test_decode_fp8_window(oracle_mod, window):
+    prob = hybrid(541 + window, [5000, 2049, 100, 0], 784, poison_unused=True)
+    out, status, _ = run_attention(prob, window=window)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob, window=window), what=f"fp8 window={window}")
+
+
+def test_decode_fp8_bf16_output(oracle_mod):
+    prob = hybrid(551, [3000, 17], 832)
+    out, status, _ = run_attention(prob, out_dtype=pa.PA_OUT_BF16)
+    ref = oracle_out(oracle_mod, prob)
+    ref_bf16 = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    err = np.abs(out.double().numpy() - ref_bf16)
+    assert status == 0 and np.isfinite(out.numpy()).all()
+    assert err.max() <= 2e-3 + 2 * 2.0 ** -8 * np.abs(ref).max()
+
+
+def test_decode_fp8_early_kv_bitwise():
+    prob = hybrid(561, [1, 15, 17, 785, 5000, 0], 784, poison_unused=True)
+    outs = []
+    for flags in (0, pa.PA_FLAG_EARLY_KV_READ):
+        out, status, _ = run_attention(prob, num_splits=5, flags=flags)
+        assert status == 0
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_decode_fp8_after_quantising_reshape_on_one_stream(oracle_mod):
+    """The serving order: the new token's K/V quantised into the fp8 cache,
+    then decode, on one stream without a host sync; the decode must see the
+    new codes (oracle run on the cache as the GPU left it, checked bit-exact
+    against the oracle's own quantisation first)."""
+    prob = hybrid(571, [32768, 900, 17], 784)
+    k_new, v_new = make_new_tokens(17, prob.num_seqs, prob.num_kv_heads, prob.head_dim)
+    q, kc, vc, bt, sl = to_dev(prob)
+    ks, vs = scales_dev(prob)
+    slots = prob.new_token_slots()
+    k_ref, v_ref = prob.k_cache[0].numpy().copy(), prob.v_cache[0].numpy().copy()
+    oracle_mod.reshape_and_cache_fp8(bits(k_new), bits(v_new), k_ref, v_ref, slots.numpy(),
+                                     prob.k_scale[0].numpy(), prob.v_scale[0].numpy())
+    desc = desc_for(prob)
+    ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device="cuda")
+    out = torch.full((prob.num_seqs, prob.num_q_heads, prob.head_dim), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kn, vn, sd = k_new.cuda(), v_new.cuda(), slots.cuda()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(2_000_000)
+        pa.reshape_and_cache_fp8(kn, vn, kc, vc, sd, ks, vs, status)
+        pa.paged_attention_decode_fp8(q, kc, vc, ks, vs, bt, sl, desc, out, ws, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert np.array_equal(kc.cpu().numpy(), k_ref) and np.array_equal(vc.cpu().numpy(), v_ref)
+    prob.k_cache[0], prob.v_cache[0] = torch.from_numpy(k_ref), torch.from_numpy(v_ref)
+    assert_parity(out.cpu(), oracle_out(oracle_mod, prob), what="fp8 decode after reshape")
+
+
+def test_decode_fp8_l32768_bs784_workload(oracle_mod):
+    """The benchmarked fp8 layer (one of its 16 layers) in the benchmark's launch."""
+    prob = make_problem(1009, **dict(WORKLOADS["decode_fp8_l32768_bs784"], num_layers=1))
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["num_splits"] > 1
+    assert_parity(out, oracle_out(oracle_mod, prob), what="fp8 32K layer")
+
+
+def test_decode_fp8_rejects_missing_scales():
+    prob = hybrid(581, [100], 16)
+    q, kc, vc, bt, sl = to_dev(prob)
+    desc = desc_for(prob)
+    out = torch.empty((1, 24, 256), device="cuda")
+    with pytest.raises(pa.PagedAttnError):
+        pa.paged_attention_decode_fp8(q, kc, vc, None, None, bt, sl, desc, out)
