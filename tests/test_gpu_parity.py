@@ -345,3 +345,42 @@ def test_reshape_and_cache_bad_slot_flagged():
     torch.cuda.synchronize()
     assert status.item() & pa.PA_DEV_BAD_SLOT
     assert torch.equal(kc[0, 3].cpu(), k_new[0]) and torch.count_nonzero(kc[1]) == 0
+
+
+# -- limits --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("splits,window", [(1, 0), (2, 0), (1, 7000)])
+def test_decode_split_wider_than_staged_page_table(oracle_mod, splits, window):
+    """A split spanning more than the 512 block-table entries a CTA stages in
+    shared memory (16-token pages, 9000 tokens in one or two splits): the
+    producer reads the table from global memory instead."""
+    prob = hybrid(271 + splits, [9000, 100], 16, poison_unused=True)
+    out, status, plan = run_attention(prob, num_splits=splits, window=window)
+    assert status == 0 and plan["num_splits"] == splits
+    assert_parity(out, oracle_out(oracle_mod, prob, window=window), what=f"unstaged splits={splits} W={window}")
+
+
+def test_verify_maximum_rows_sampled(oracle_mod):
+    """q_len x G = 8192 x 4 = 32768 rows per KV head, the largest verify block
+    set (256 row blocks x 8 KV heads): sampled (row, head) outputs against the
+    oracle's single-split attention, the rest checked finite."""
+    q_len = 8192
+    prob = make_problem(181, num_seqs=1, seq_lens=[q_len + 600], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, q_len=q_len, scale=1 / math.sqrt(128), poison_unused=True)
+    write_new_rows(prob, 29)
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
+    assert torch.isfinite(out).all()
+    g = torch.Generator().manual_seed(3)
+    rows = [0, 1, 127, 128, 4095, q_len - 1] + torch.randint(0, q_len, (10,), generator=g).tolist()
+    heads = [0, 3, 4, 31]
+    q, kc, vc = bits(prob.q[0]), bits(prob.k_cache[0]), bits(prob.v_cache[0])
+    got, ref = [], []
+    for r in rows:
+        for h in heads:
+            o, _, _ = oracle_mod.attention_partial(q, kc, vc, prob.block_table.numpy(), prob.seq_lens.numpy(),
+                                                   prob.scale, r, h, 0, 1 << 40, q_len=q_len)
+            got.append(out[r, h])
+            ref.append(o)
+    assert_parity(torch.stack(got)[:, None, :], np.stack(ref)[:, None, :], rel_l2=REL_L2_VERIFY,
+                  what="verify 32768 rows (sampled)")
