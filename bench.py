@@ -49,6 +49,7 @@ WORKLOAD = "hybrid_step_l32768_bs784_x16"
 METRIC = "paged-attn decode µs/call & achieved KV-read HBM GB/s vs context length"
 KV_BYTES_PER_TOKEN_LAYER = 4096  # 2 (K, V) x 4 KV heads x 256 dims x 2 bytes
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e datasheet rate (secondary denominator)
 
 
 def load_peaks():
@@ -400,7 +401,9 @@ def bench_gpu(args, world, rank, local):
                                   "decode calls (split kernel + reduce), timed after the step region"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": load_traffic(),
-                     "algorithmic_bytes_per_call": B * L * KV_BYTES_PER_TOKEN_LAYER},
+                     "algorithmic_bytes_per_call": B * L * KV_BYTES_PER_TOKEN_LAYER,
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "Python binding, eager calls, pinned host inputs copied in and outputs copied out every step"},
         "gpu_launches": launches_per_step * args.steps,
