@@ -465,7 +465,7 @@ def _layers_beyond_l2(bytes_per_layer, minimum, l2_bytes=256 << 20):
 
 SECONDARY = ("decode_l512_bs16", "context_sweep", "batch32_uniform_bs784", "verify_b8_q16_l8192_bs832",
              "prefill_q2048_l16384_bs832", "decode_window2048_l32768_bs784", "decode_g12_l32768_bs784",
-             "verify_g12_b32_q5_l2048_bs784", "decode_fp8_l32768_bs784")
+             "verify_g12_b32_q5_l2048_bs784", "decode_fp8_l32768_bs784", "verify_fp8_b8_q16_l8192_bs832")
 
 
 def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
@@ -490,6 +490,8 @@ def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
         _wide_group(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "decode_fp8_l32768_bs784" in names:
         _fp8_decode(pa, dev, stream, peak, res, WORKLOADS, make_problem)
+    if "verify_fp8_b8_q16_l8192_bs832" in names:
+        _verify_fp8(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "verify_g12_b32_q5_l2048_bs784" in names:
         _verify(pa, dev, stream, peak, res, WORKLOADS, make_problem, name="verify_g12_b32_q5_l2048_bs784",
                 layers=2)
@@ -514,6 +516,29 @@ def _fp8_decode(pa, dev, stream, peak, res, WORKLOADS, make_problem):
     kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER // 2
     res["decode_fp8_l32768_bs784"] = {"us_per_call": us, "kv_bytes_per_call": kv, "GBps": kv / (us * 1e-6) / 1e9,
                                       "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak, "plan": pa.last_plan()}
+    del prob, calls
+
+
+def _verify_fp8(pa, dev, stream, peak, res, WORKLOADS, make_problem):
+    # The verify workload over an fp8 e4m3 cache: 8 x 8208 tokens x 2048 B =
+    # 134 MiB of codes per call; 4 layer copies cycled against L2.
+    import torch
+    prob = make_problem(1010, **dict(WORKLOADS["verify_b8_q16_l8192_bs832"], num_layers=4, kv_fp8=True), device=dev)
+    bt, sl = prob.block_table.to(dev), prob.seq_lens.to(dev)
+    desc = pa.make_desc(num_seqs=prob.num_seqs, q_len=prob.q_len, num_q_heads=prob.num_q_heads,
+                        num_kv_heads=prob.num_kv_heads, head_dim=prob.head_dim, block_size=prob.block_size,
+                        max_pages_per_seq=prob.max_pages_per_seq, max_seq_len=prob.max_seq_len,
+                        num_pages=prob.num_pages, scale=prob.scale)
+    ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=dev)
+    out = torch.empty((prob.num_seqs * prob.q_len, prob.num_q_heads, prob.head_dim), dtype=torch.float32, device=dev)
+    calls = [(lambda l=l: pa.paged_attention_verify_fp8(prob.q[l], prob.k_cache[l], prob.v_cache[l], prob.k_scale[l],
+                                                        prob.v_scale[l], bt, sl, desc, out, ws))
+             for l in range(prob.num_layers)]
+    us = _time_graph(calls, stream, 100) * 1e3 / len(calls)
+    kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER // 2
+    res["verify_fp8_b8_q16_l8192_bs832"] = {"us_per_call": us, "kv_bytes_per_call": kv, "GBps": kv / (us * 1e-6) / 1e9,
+                                            "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak,
+                                            "TFLOPs": _causal_flops(prob) / (us * 1e-6) / 1e12, "plan": pa.last_plan()}
     del prob, calls
 
 

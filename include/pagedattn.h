@@ -246,6 +246,17 @@ pa_status pa_paged_attention_decode_fp8(const void *q, const void *k_cache, cons
                                         const pa_attn_desc *desc, void *out, void *workspace,
                                         size_t workspace_bytes, int32_t *device_status, void *stream);
 
+/* paged_attention_verify over an fp8 cache: out as pa_paged_attention_verify
+ * with K and V decoded as for pa_paged_attention_decode_fp8.  The tensor-core
+ * products run in f16 (exact for the e4m3 values; q enters as f16), with the
+ * scales applied to the scores and to the final normaliser.  Same plan,
+ * workspace, limits and errors as pa_paged_attention_verify. */
+pa_status pa_paged_attention_verify_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                        const float *k_scale, const float *v_scale,
+                                        const int32_t *block_table, const int32_t *seq_lens,
+                                        const pa_attn_desc *desc, void *out, void *workspace,
+                                        size_t workspace_bytes, int32_t *device_status, void *stream);
+
 /* Size of the scratch array that pa_paged_attention_decode_noalloc keeps in
  * device memory (8 MiB per GPU that loads the library, held until exit). */
 #define PA_NOALLOC_SCRATCH_BYTES (8u << 20)

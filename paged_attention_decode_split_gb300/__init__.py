@@ -17,7 +17,7 @@ import threading
 
 __all__ = [
     "AttnDesc", "PlanInfo", "PagedAttnError", "load_library", "make_desc", "workspace_bytes",
-    "hybrid_page_tokens", "reshape_and_cache_fp8", "paged_attention_decode_fp8",
+    "hybrid_page_tokens", "reshape_and_cache_fp8", "paged_attention_decode_fp8", "paged_attention_verify_fp8",
     "reshape_and_cache", "paged_attention_decode", "paged_attention_verify", "last_plan",
     "status_string", "PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_WORKSPACE",
     "PA_ERR_CUDA", "PA_OUT_F32", "PA_OUT_BF16", "PA_DEV_BAD_SEQLEN", "PA_DEV_BAD_PAGE",
@@ -92,9 +92,11 @@ def load_library(path: str | None = None):
         lib.pa_reshape_and_cache_fp8.restype = ctypes.c_int
         lib.pa_reshape_and_cache_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
                                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _vp, _vp]
-        lib.pa_paged_attention_decode_fp8.restype = ctypes.c_int
-        lib.pa_paged_attention_decode_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc),
-                                                      _vp, _vp, ctypes.c_size_t, _vp, _vp]
+        for name in ("pa_paged_attention_decode_fp8", "pa_paged_attention_verify_fp8"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc), _vp, _vp, ctypes.c_size_t,
+                           _vp, _vp]
         for name in ("pa_paged_attention_decode", "pa_paged_attention_verify"):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
@@ -201,6 +203,16 @@ def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tabl
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
         ctypes.byref(desc), _ptr(out), _ptr(workspace), ws, _ptr(status), _stream(stream))
     _check(rc, "pa_paged_attention_decode_fp8")
+
+
+def paged_attention_verify_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, desc: AttnDesc, out,
+                               workspace=None, status=None, stream=None) -> None:
+    """Verify (q_len > 1) over an e4m3 cache: K = code x k_scale[kv head], V likewise."""
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().pa_paged_attention_verify_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
+        ctypes.byref(desc), _ptr(out), _ptr(workspace), ws, _ptr(status), _stream(stream))
+    _check(rc, "pa_paged_attention_verify_fp8")
 
 
 def last_plan() -> dict:

@@ -25,6 +25,9 @@ cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const C
                           const CUtensorMap &tk64, const CUtensorMap &tv64, const VerifyParams &p, dim3 grid,
                           cudaStream_t stream);
 
+cudaError_t launch_verify_fp8(int head_dim, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tk64,
+                              const CUtensorMap &tv64, const VerifyParams &p, dim3 grid, cudaStream_t stream);
+
 // Sets the dynamic shared-memory limit of `fn` once per device.
 cudaError_t ensure_smem_limit(const void *fn, int bytes, int slot);
 

@@ -172,20 +172,23 @@ bool encode_cache_map(CUtensorMap *map, const void *base, const pa_attn_desc *d,
     return r == CUDA_SUCCESS;
 }
 
-// 5-D view for the tensor-core path: {64 dims, tokens, 64-dim blocks, head,
-// page}; one box of {64, 64 tokens, D/64 blocks, 1, 1} lands in shared memory
-// as [D/64 blocks][64 tokens][128 B] with the 128-byte swizzle -- the K-major
-// (and MN-major) operand layout the MMA reads -- in a single copy.
-bool encode_cache_map_blocks(CUtensorMap *map, const void *base, const pa_attn_desc *d) {
+// 5-D view for the tensor-core path: {128-byte column block, tokens, blocks,
+// head, page}; one box of {block, 64 tokens, all blocks, 1, 1} lands in
+// shared memory as [blocks][64 tokens][128 B] with the 128-byte swizzle -- the
+// K-major (and MN-major) operand layout the MMA reads -- in a single copy.
+// bf16: 64-dim blocks; fp8: 128-code blocks.
+bool encode_cache_map_blocks(CUtensorMap *map, const void *base, const pa_attn_desc *d, bool fp8 = false) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
-    const cuuint64_t row = (cuuint64_t)d->head_dim * 2;
-    const cuuint64_t dims[5] = {64, (cuuint64_t)d->block_size, (cuuint64_t)(d->head_dim / 64),
+    const int esz = fp8 ? 1 : 2, blk = 128 / esz;
+    const cuuint64_t row = (cuuint64_t)d->head_dim * esz;
+    const cuuint64_t dims[5] = {(cuuint64_t)blk, (cuuint64_t)d->block_size, (cuuint64_t)(d->head_dim / blk),
                                 (cuuint64_t)d->num_kv_heads, (cuuint64_t)d->num_pages};
     const cuuint64_t strides[4] = {row * d->num_kv_heads, 128, row, row * d->num_kv_heads * d->block_size};
-    const cuuint32_t box[5] = {64, 64, (cuuint32_t)(d->head_dim / 64), 1, 1};
+    const cuuint32_t box[5] = {(cuuint32_t)blk, 64, (cuuint32_t)(d->head_dim / blk), 1, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                    const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -300,6 +303,10 @@ __global__ void __launch_bounds__(128) pa_reshape_and_cache_fp8_kernel(
 }
 
 pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                      const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
+                      const pa_attn_desc *desc, void *out, void *workspace, size_t workspace_bytes,
+                      int32_t *device_status, void *stream);
+pa_status verify_call(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
                       const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
                       const pa_attn_desc *desc, void *out, void *workspace, size_t workspace_bytes,
                       int32_t *device_status, void *stream);
@@ -431,71 +438,20 @@ pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const vo
                                     const int32_t *block_table, const int32_t *seq_lens, const pa_attn_desc *desc,
                                     void *out, void *workspace, size_t workspace_bytes, int32_t *device_status,
                                     void *stream) {
-    pa_status st = check_desc(desc, true);
-    if (st != PA_OK) return st;
-    if (desc->num_seqs == 0) return PA_OK;
-    st = check_common_ptrs(q, k_cache, v_cache, block_table, seq_lens, out);
-    if (st != PA_OK) return st;
-    Plan pl;
-    st = make_plan(desc, true, &pl);
-    if (st != PA_OK) return st;
-    st = check_workspace(pl, workspace, workspace_bytes);
-    if (st != PA_OK) return st;
+    return verify_call(q, k_cache, v_cache, nullptr, nullptr, block_table, seq_lens, desc, out, workspace,
+                       workspace_bytes, device_status, stream);
+}
 
-    CUtensorMap tk, tv;
-    if (!encode_cache_map(&tk, k_cache, desc, 64, true) || !encode_cache_map(&tv, v_cache, desc, 64, true))
-        return PA_ERR_CUDA;
-    CUtensorMap tk64, tv64;  // whole-tile copies; only used where a 64-token tile fits in a page
-    if (desc->block_size >= 64) {
-        if (!encode_cache_map_blocks(&tk64, k_cache, desc) || !encode_cache_map_blocks(&tv64, v_cache, desc))
-            return PA_ERR_CUDA;
-    } else {
-        tk64 = tk;  // never used: no 64-token tile fits in a smaller page
-        tv64 = tv;
-    }
-
-    const int group = desc->num_q_heads / desc->num_kv_heads;
-    VerifyParams p;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.out = out;
-    p.part_o = static_cast<float *>(workspace);
-    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
-    p.status = device_status;
-    p.num_pages = desc->num_pages;
-    p.num_q_heads = desc->num_q_heads;
-    p.q_len = desc->q_len;
-    p.group = group;
-    p.max_pages_per_seq = desc->max_pages_per_seq;
-    p.max_seq_len = desc->max_seq_len;
-    p.block_size = desc->block_size;
-    p.chunks_per_split = pl.chunks_per_split;
-    p.num_splits = pl.num_splits;
-    p.scale_log2 = desc->scale * 1.4426950408889634f;
-    p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
-    p.early_kv = (desc->flags & PA_FLAG_EARLY_KV_READ) != 0;
-    p.window = desc->window;
-    p.num_kv_heads = desc->num_kv_heads;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int row_blocks = (desc->q_len * group + 127) / 128;
-    const dim3 grid(pl.num_splits, desc->num_kv_heads * row_blocks, desc->num_seqs);
-    if (launch_verify(desc->head_dim, desc->q_len * group, tk, tv, tk64, tv64, p, grid, s) != cudaSuccess)
-        return PA_ERR_CUDA;
-    if (pl.num_splits > 1) {
-        ReduceParams r;
-        r.part_o = p.part_o;
-        r.part_ml = p.part_ml;
-        r.out = out;
-        r.num_q_heads = desc->num_q_heads;
-        r.num_splits = pl.num_splits;
-        r.out_bf16 = p.out_bf16;
-        if (launch_reduce(desc->head_dim, r, desc->num_seqs * desc->q_len, s) != cudaSuccess)
-            return PA_ERR_CUDA;
-    }
-    record_plan(PA_PATH_VERIFY_TCGEN05, pl, desc, pl.num_splits * desc->num_kv_heads * row_blocks * desc->num_seqs);
-    return PA_OK;
+pa_status pa_paged_attention_verify_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                        const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                        const int32_t *seq_lens, const pa_attn_desc *desc, void *out,
+                                        void *workspace, size_t workspace_bytes, int32_t *device_status,
+                                        void *stream) {
+    if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+        return PA_ERR_INVALID_ARG;
+    return verify_call(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, desc, out, workspace,
+                       workspace_bytes, device_status, stream);
 }
 
 }  // extern "C"
@@ -564,6 +520,95 @@ pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, c
             return PA_ERR_CUDA;
     }
     record_plan(PA_PATH_DECODE_CUDA_CORE, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
+    return PA_OK;
+}
+
+// Verify over a bf16 cache (k_scale == nullptr) or an fp8 e4m3 cache.
+pa_status verify_call(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                      const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
+                      const pa_attn_desc *desc, void *out, void *workspace, size_t workspace_bytes,
+                      int32_t *device_status, void *stream) {
+    const bool fp8 = k_scale != nullptr;
+    pa_status st = check_desc(desc, true);
+    if (st != PA_OK) return st;
+    if (desc->num_seqs == 0) return PA_OK;
+    st = check_common_ptrs(q, k_cache, v_cache, block_table, seq_lens, out);
+    if (st != PA_OK) return st;
+    Plan pl;
+    st = make_plan(desc, true, &pl);
+    if (st != PA_OK) return st;
+    st = check_workspace(pl, workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+
+    CUtensorMap tk, tv;
+    CUtensorMap tk64, tv64;  // whole-tile copies; only used where a 64-token tile fits in a page
+    if (fp8) {
+        // e4m3 in 128-code column blocks, 128-byte swizzle: a 16-token chunk
+        // per block, or a whole 64-token tile in one 5-D box
+        if (!encode_cache_map(&tk, k_cache, desc, 128, true, true) ||
+            !encode_cache_map(&tv, v_cache, desc, 128, true, true))
+            return PA_ERR_CUDA;
+        if (desc->block_size < 64) {
+            tk64 = tk;  // never used: no 64-token tile fits in a smaller page
+            tv64 = tv;
+        } else if (!encode_cache_map_blocks(&tk64, k_cache, desc, true) ||
+                   !encode_cache_map_blocks(&tv64, v_cache, desc, true)) {
+            return PA_ERR_CUDA;
+        }
+    } else if (!encode_cache_map(&tk, k_cache, desc, 64, true) || !encode_cache_map(&tv, v_cache, desc, 64, true)) {
+        return PA_ERR_CUDA;
+    } else if (desc->block_size >= 64) {
+        if (!encode_cache_map_blocks(&tk64, k_cache, desc) || !encode_cache_map_blocks(&tv64, v_cache, desc))
+            return PA_ERR_CUDA;
+    } else {
+        tk64 = tk;  // never used: no 64-token tile fits in a smaller page
+        tv64 = tv;
+    }
+
+    const int group = desc->num_q_heads / desc->num_kv_heads;
+    VerifyParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
+    p.status = device_status;
+    p.num_pages = desc->num_pages;
+    p.num_q_heads = desc->num_q_heads;
+    p.q_len = desc->q_len;
+    p.group = group;
+    p.max_pages_per_seq = desc->max_pages_per_seq;
+    p.max_seq_len = desc->max_seq_len;
+    p.block_size = desc->block_size;
+    p.chunks_per_split = pl.chunks_per_split;
+    p.num_splits = pl.num_splits;
+    p.scale_log2 = desc->scale * 1.4426950408889634f;
+    p.out_bf16 = desc->out_dtype == PA_OUT_BF16;
+    p.early_kv = (desc->flags & PA_FLAG_EARLY_KV_READ) != 0;
+    p.window = desc->window;
+    p.num_kv_heads = desc->num_kv_heads;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int row_blocks = (desc->q_len * group + 127) / 128;
+    const dim3 grid(pl.num_splits, desc->num_kv_heads * row_blocks, desc->num_seqs);
+    const cudaError_t e = fp8 ? launch_verify_fp8(desc->head_dim, tk, tv, tk64, tv64, p, grid, s)
+                              : launch_verify(desc->head_dim, desc->q_len * group, tk, tv, tk64, tv64, p, grid, s);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (pl.num_splits > 1) {
+        ReduceParams r;
+        r.part_o = p.part_o;
+        r.part_ml = p.part_ml;
+        r.out = out;
+        r.num_q_heads = desc->num_q_heads;
+        r.num_splits = pl.num_splits;
+        r.out_bf16 = p.out_bf16;
+        if (launch_reduce(desc->head_dim, r, desc->num_seqs * desc->q_len, s) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    record_plan(PA_PATH_VERIFY_TCGEN05, pl, desc, pl.num_splits * desc->num_kv_heads * row_blocks * desc->num_seqs);
     return PA_OK;
 }
 

@@ -37,6 +37,16 @@
 //       boxes per chunk
 //   V_i same layout as K_i, read as the MN-major (N = d) B operand
 // Warp roles: 0-3 softmax, 4 MMA issue (and tensor-memory allocation), 5 TMA.
+//
+// fp8 e4m3 cache (NSG > 0): the copies land e4m3 tiles as [D/128 blocks][64
+// tokens][128 B] with the 128-byte swizzle in a staging ring of NSG slots per
+// tensor (so 8 lanes reading one 16-byte column of 8 consecutive tokens hit 8
+// different bank groups), and four more warps
+// widen them (warps 6-7: K, 8-9: V) into the same swizzled K/V rings as f16
+// -- exact, since every e4m3 value is an f16 value -- zeroing rows past the
+// tile's last key.  Q and P then enter the products as f16 (kind::f16 with
+// f16 A and B), the K scale joins the softmax scale and the V scale the final
+// normaliser.
 #pragma once
 
 #include "decode_split.cuh"
@@ -65,6 +75,8 @@ struct VerifyParams {
     int early_kv;  // stream the context before the new rows ahead of the dependency wait
     int num_kv_heads;  // grid y = num_kv_heads x 128-row blocks
     int window;        // 0: full attention; W > 0: each row sees only its last W keys
+    const float *k_scale;  // fp8 cache: [Hkv] dequantisation scales of K and V
+    const float *v_scale;
 };
 
 // Byte offset of 16-byte column chunk c of row t in a [D/64][rows][128 B]
@@ -83,6 +95,35 @@ __device__ __forceinline__ void split_bf16(float a, float b, uint32_t &head, uin
     head = pack_bf16(a, b);
     const float ha = __uint_as_float(head << 16), hb = __uint_as_float(head & 0xffff0000u);
     resid = pack_bf16(a - ha, b - hb);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// The same split with both parts in f16.
+__device__ __forceinline__ void split_f16(float a, float b, uint32_t &head, uint32_t &resid) {
+    head = pack_f16(a, b);
+    const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&head));
+    resid = pack_f16(a - h.x, b - h.y);
+}
+
+// Two bf16 (packed) -> two f16 (packed); exact for the magnitudes q takes.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Eight e4m3 codes (one 32-bit word each of four) -> eight f16 in 16 bytes.
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint32_t w0, uint32_t w1) {
+    uint4 r;
+    asm("{\n\t.reg .b16 a, b, c, d;\n\t"
+        "mov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "r"(w0), "r"(w1));
+    return r;
 }
 
 namespace tc {
@@ -139,11 +180,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     d |= (uint64_t)(layout & 7u) << 61;
     return d;
 }
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
-// B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16
+// (ab_f16 = false) or both f16, A K-major, B K-major (b_mn = 0) or MN-major
+// (b_mn = 1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn, bool ab_f16 = false) {
+    return (1u << 4) | (ab_f16 ? 0u : (1u << 7) | (1u << 10)) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // 16 consecutive fp32 columns of this thread's tensor-memory lane.
@@ -187,18 +229,23 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
 
 }  // namespace tc
 
-template <int D, int NK, int NV>
+template <int D, int NK, int NV, int NSG = 0>
 struct VerifyTcCfg {
+    static constexpr bool F8 = NSG > 0;                // fp8 cache: e4m3 staging ring of NSG slots per tensor
     static constexpr int M = 128;                      // MMA rows (query rows, zero padded)
     static constexpr int TT = 64;                      // tokens per tile (4 TMA chunks)
     static constexpr int CPT = TT / kChunk;            // chunks per tile
     static constexpr int DB = D / 64;                  // 128-byte column blocks
-    static constexpr int TILE_BYTES = TT * D * 2;      // K or V of one tile
-    static constexpr int CHUNK_BYTES = kChunk * D * 2;
+    static constexpr int TILE_BYTES = TT * D * 2;      // K or V of one tile (bf16 or f16)
+    static constexpr int KVB = F8 ? 1 : 2;             // bytes per cached element
+    static constexpr int CHUNK_BYTES = kChunk * D * KVB;  // one TMA chunk as copied
+    static constexpr int STG_BYTES = TT * D;           // one e4m3 tile, [D/128][64 tokens][128 B] swizzled
     static constexpr int OFF_V = NK * TILE_BYTES;       // K ring, then V ring
-    static constexpr int OFF_BAR = OFF_V + NV * TILE_BYTES;
-    // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done[2], mma_fin
-    static constexpr int OFF_TMEM = OFF_BAR + (2 * NK + 2 * NV + 7) * 8;
+    static constexpr int OFF_STG = OFF_V + NV * TILE_BYTES;  // K staging, then V staging
+    static constexpr int OFF_BAR = OFF_STG + 2 * NSG * STG_BYTES;
+    // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done[2], mma_fin,
+    // then (fp8) kst_full[NSG], kst_empty[NSG], vst_full[NSG], vst_empty[NSG]
+    static constexpr int OFF_TMEM = OFF_BAR + (2 * NK + 2 * NV + 7 + 4 * NSG) * 8;
     static constexpr int OFF_FLAGS = OFF_TMEM + 16;
     static constexpr int SMEM_BYTES = OFF_FLAGS + 16 + 1024;
     // tensor-memory columns: O (fp32, D), two S/P buffers (64 each), Q (bf16 pairs, D / 2)
@@ -206,18 +253,23 @@ struct VerifyTcCfg {
     static constexpr int O_COL = 0;
     static constexpr int S_COL = D;
     static constexpr int Q_COL = D + 2 * TT;
-    static constexpr int THREADS = 6 * 32;
+    static constexpr int CW = 2;                       // fp8: widening warps per tensor
+    static constexpr int THREADS = (F8 ? 6 + 2 * CW : 6) * 32;
     static_assert(D == 256 || D == 128, "head_dim 256 or 128");
     static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor-memory columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-template <int D, int NK, int NV>
-__global__ void __launch_bounds__(6 * 32, 1)
+// NSG > 0: fp8 cache (tm_k / tm_v: e4m3 boxes of 128 codes x 16 tokens,
+// tm_k64 / tm_v64: 5-D boxes of a whole 64-token tile, both with the 128-byte
+// swizzle).
+template <int D, int NK, int NV, int NSG>
+__global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
     pa_verify_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
                         const VerifyParams p) {
-    using C = VerifyTcCfg<D, NK, NV>;
+    using C = VerifyTcCfg<D, NK, NV, NSG>;
+    constexpr bool F8 = C::F8;
     constexpr int TT = C::TT, CPT = C::CPT;
     constexpr float kLazy = 8.f;  // raise the reference max only when it grows by more than 2^8
     extern __shared__ uint8_t smem_dyn[];
@@ -232,6 +284,10 @@ __global__ void __launch_bounds__(6 * 32, 1)
     uint64_t *p_full = s_full + 2;   // [2]: P_i written by the softmax warps
     uint64_t *o_done = p_full + 2;   // [2]: O += P_i V_i finished
     uint64_t *mma_fin = o_done + 2;
+    uint64_t *kst_full = mma_fin + 1;  // fp8: e4m3 tile landed in a staging slot
+    uint64_t *kst_empty = kst_full + NSG;  // fp8: staging slot widened, free again
+    uint64_t *vst_full = kst_empty + NSG;
+    uint64_t *vst_empty = vst_full + NSG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::OFF_FLAGS);  // [0] abort, [1] bad page
 
@@ -243,12 +299,14 @@ __global__ void __launch_bounds__(6 * 32, 1)
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
+        // a K/V ring slot is filled by the copy engine (one expect-tx arrival),
+        // or with an fp8 cache by the CW widening warps of its tensor
         for (int s = 0; s < NK; ++s) {
-            mbar_init(&k_full[s], 1);
+            mbar_init(&k_full[s], F8 ? C::CW : 1);
             mbar_init(&k_empty[s], 1);
         }
         for (int s = 0; s < NV; ++s) {
-            mbar_init(&v_full[s], 1);
+            mbar_init(&v_full[s], F8 ? C::CW : 1);
             mbar_init(&v_empty[s], 1);
         }
         for (int j = 0; j < 2; ++j) {
@@ -257,6 +315,12 @@ __global__ void __launch_bounds__(6 * 32, 1)
             mbar_init(&o_done[j], 1);
         }
         mbar_init(mma_fin, 1);
+        for (int s = 0; s < NSG; ++s) {
+            mbar_init(&kst_full[s], 1);
+            mbar_init(&kst_empty[s], C::CW);
+            mbar_init(&vst_full[s], 1);
+            mbar_init(&vst_empty[s], C::CW);
+        }
         flags[0] = 0;
         flags[1] = 0;
         fence_mbar_init();
@@ -312,9 +376,10 @@ __global__ void __launch_bounds__(6 * 32, 1)
     int lp_cache[2] = {-1, -1}, page_cache[2] = {0, 0};  // per tensor: last page looked up
     int issued_k = 0, issued_v = 0;
     auto issue_tile = [&](int i, int tensor, uint64_t policy) {
-        const int s = tensor == 0 ? i % NK : i % NV;
-        uint64_t *bar = tensor == 0 ? &k_full[s] : &v_full[s];
-        uint8_t *dst0 = smem + (tensor == 0 ? s * C::TILE_BYTES : C::OFF_V + s * C::TILE_BYTES);
+        const int s = F8 ? i % (NSG > 0 ? NSG : 1) : (tensor == 0 ? i % NK : i % NV);
+        uint64_t *bar = F8 ? (tensor == 0 ? &kst_full[s] : &vst_full[s]) : (tensor == 0 ? &k_full[s] : &v_full[s]);
+        uint8_t *dst0 = F8 ? smem + C::OFF_STG + (tensor * NSG + s) * C::STG_BYTES
+                           : smem + (tensor == 0 ? s * C::TILE_BYTES : C::OFF_V + s * C::TILE_BYTES);
         const CUtensorMap *m4 = tensor == 0 ? &tm_k : &tm_v;
         const CUtensorMap *m5 = tensor == 0 ? &tm_k64 : &tm_v64;
         const int nc = min(CPT, n_my - i * CPT);  // chunks in this tile
@@ -332,6 +397,17 @@ __global__ void __launch_bounds__(6 * 32, 1)
             }
             const int page = page_cache[tensor];
             const int off = t0 - lp * p.block_size;
+            if constexpr (F8) {
+                // e4m3 in 128-code column blocks: the whole tile in one copy when it lies in one page
+                if (c == 0 && nc == CPT && off + TT <= p.block_size) {
+                    tma_load_5d(dst0, m5, bar, 0, off, 0, kvh, page, policy);
+                    break;
+                }
+#pragma unroll
+                for (int db = 0; db < D / 128; ++db)
+                    tma_load_4d(dst0 + db * TT * 128 + c * kChunk * 128, m4, bar, db * 128, kvh, off, page, policy);
+                continue;
+            }
             if (c == 0 && nc == CPT && off + TT <= p.block_size) {
                 // the whole tile lies in one page: one copy lands it as
                 // [D/64 blocks][64 tokens][128 B]
@@ -352,8 +428,9 @@ __global__ void __launch_bounds__(6 * 32, 1)
         if (warp == 5 && lane == 0) {
             // first use of each slot: tiles that end before the new rows
             const uint64_t policy = l2_policy_evict_first();
-            while (issued_k < min(NK, n_tiles) && before_new_rows(issued_k)) issue_tile(issued_k++, 0, policy);
-            while (issued_v < min(NV, n_tiles) && before_new_rows(issued_v)) issue_tile(issued_v++, 1, policy);
+            constexpr int FK = F8 ? NSG : NK, FV = F8 ? NSG : NV;  // slots the copies land in
+            while (issued_k < min(FK, n_tiles) && before_new_rows(issued_k)) issue_tile(issued_k++, 0, policy);
+            while (issued_v < min(FV, n_tiles) && before_new_rows(issued_v)) issue_tile(issued_v++, 1, policy);
         }
         pdl_wait_primary();
     }
@@ -381,8 +458,11 @@ __global__ void __launch_bounds__(6 * 32, 1)
             uint32_t r[2][32];
 #pragma unroll
             for (int v = 0; v < 16; ++v) {
-                const uint4 w = (int)threadIdx.x < R ? *reinterpret_cast<const uint4 *>(qrow + 2 * c0 + 8 * v)
-                                                     : make_uint4(0u, 0u, 0u, 0u);
+                uint4 w = (int)threadIdx.x < R ? *reinterpret_cast<const uint4 *>(qrow + 2 * c0 + 8 * v)
+                                               : make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (F8)  // the products run in f16: Q too
+                    w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                                   bf16x2_to_f16x2(w.w));
                 r[v >> 3][4 * (v & 7)] = w.x;
                 r[v >> 3][4 * (v & 7) + 1] = w.y;
                 r[v >> 3][4 * (v & 7) + 2] = w.z;
@@ -406,15 +486,19 @@ __global__ void __launch_bounds__(6 * 32, 1)
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
             uint32_t idle = 0;
+            // the slots the copies land in: the K/V rings, or the fp8 staging rings
+            constexpr int FK = F8 ? NSG : NK, FV = F8 ? NSG : NV;
+            uint64_t *ke = F8 ? kst_empty : k_empty;
+            uint64_t *ve = F8 ? vst_empty : v_empty;
             while (issued_k < n_tiles || issued_v < n_tiles) {
                 bool progress = false;
                 if (issued_k < n_tiles &&
-                    (issued_k < NK || mbar_test_wait(&k_empty[issued_k % NK], ((issued_k / NK) - 1) & 1))) {
+                    (issued_k < FK || mbar_test_wait(&ke[issued_k % FK], ((issued_k / FK) - 1) & 1))) {
                     issue_tile(issued_k++, 0, policy);
                     progress = true;
                 }
                 if (issued_v < n_tiles &&
-                    (issued_v < NV || mbar_test_wait(&v_empty[issued_v % NV], ((issued_v / NV) - 1) & 1))) {
+                    (issued_v < FV || mbar_test_wait(&ve[issued_v % FV], ((issued_v / FV) - 1) & 1))) {
                     issue_tile(issued_v++, 1, policy);
                     progress = true;
                 }
@@ -427,11 +511,13 @@ __global__ void __launch_bounds__(6 * 32, 1)
             }
             if (flags[0]) {
                 // let the copies in flight land before the CTA ends
-                for (int i = max(0, issued_k - NK); i < issued_k; ++i)
-                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&k_full[i % NK], (i / NK) & 1); ++n) {
+                uint64_t *kf = F8 ? kst_full : k_full;
+                uint64_t *vf = F8 ? vst_full : v_full;
+                for (int i = max(0, issued_k - FK); i < issued_k; ++i)
+                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&kf[i % FK], (i / FK) & 1); ++n) {
                     }
-                for (int i = max(0, issued_v - NV); i < issued_v; ++i)
-                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&v_full[i % NV], (i / NV) & 1); ++n) {
+                for (int i = max(0, issued_v - FV); i < issued_v; ++i)
+                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&vf[i % FV], (i / FV) & 1); ++n) {
                     }
                 set_status(p.status, PA_DEV_TIMEOUT);
             }
@@ -439,8 +525,8 @@ __global__ void __launch_bounds__(6 * 32, 1)
     } else if (warp == 4) {
         // ---------------- MMA issue: one lane ----------------
         if (lane == 0) {
-            constexpr uint32_t kIdQK = tc::idesc_bf16(128, TT, 0);
-            constexpr uint32_t kIdPV = tc::idesc_bf16(128, D, 1);
+            constexpr uint32_t kIdQK = tc::idesc_bf16(128, TT, 0, F8);
+            constexpr uint32_t kIdPV = tc::idesc_bf16(128, D, 1, F8);
             // Event loop: each product is issued as soon as its own inputs are
             // ready -- O += P_i V_i when the softmax warps have written P_i,
             // S_i = Q K_i^T when tile i has landed and P_{i-2}, which shares
@@ -508,6 +594,64 @@ __global__ void __launch_bounds__(6 * 32, 1)
             for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(mma_fin, 0); ++n) {
             }
         }
+    } else if (warp >= 6) {
+        if constexpr (F8) {
+            // ---------------- fp8: widen staged e4m3 tiles into the K (warps 6, 7) / V (8, 9) ring ----------------
+            const int tensor = (warp - 6) / C::CW, part = (warp - 6) % C::CW;
+            constexpr int NR0 = NK, NR1 = NV;
+            const int NR = tensor == 0 ? NR0 : NR1;
+            uint64_t *ring_full = tensor == 0 ? k_full : v_full;
+            uint64_t *ring_empty = tensor == 0 ? k_empty : v_empty;
+            uint64_t *stg_full = tensor == 0 ? kst_full : vst_full;
+            uint64_t *stg_empty = tensor == 0 ? kst_empty : vst_empty;
+            uint8_t *ring = smem + (tensor == 0 ? 0 : C::OFF_V);
+            const uint8_t *stg = smem + C::OFF_STG + tensor * NSG * C::STG_BYTES;
+            const int t_end = min(L, (c_begin + n_my) * kChunk);
+            // A lane widens 16 codes -- 16-byte column j of 128-code block b of
+            // token t -- into two 16-byte f16 chunks of the swizzled ring row.
+            // The 8 lanes of a shared-memory phase take 8 consecutive tokens of
+            // one column (t & 7 = lane & 7), so both the staged reads and the
+            // ring writes spread over the 8 bank groups; a lane then walks its
+            // column down the tile in steps of 8 tokens (1 KiB in both layouts).
+            constexpr int QG = D / 64;  // groups of 4 columns: warp `part` takes every CW-th
+            const int t_lo = lane & 7, q_lo = lane >> 3;
+            for (int i = 0; i < n_tiles; ++i) {
+                // the staged tile has landed, and the ring slot's previous tile has been consumed
+                bool ok = __all_sync(0xffffffffu, mbar_wait(&stg_full[i % NSG], (i / NSG) & 1, &flags[0]));
+                if (ok && i >= NR)
+                    ok = __all_sync(0xffffffffu, mbar_wait(&ring_empty[i % NR], ((i / NR) - 1) & 1, &flags[0]));
+                if (!ok) {
+                    flags[0] = 1;
+                    break;
+                }
+                const int nvl = min(TT, t_end - (c_begin + i * CPT) * kChunk) - t_lo;  // rows t < nv hold keys
+                const uint8_t *stg_tile = stg + (i % NSG) * C::STG_BYTES;
+                uint8_t *ring_tile = ring + (i % NR) * C::TILE_BYTES;
+                for (int qg = part; qg < QG; qg += C::CW) {
+                    const int q = 4 * qg + q_lo, b = q >> 3, j = q & 7, c = (q & 3) * 2;
+                    const uint8_t *src = stg_tile + b * (TT * 128) + t_lo * 128 + ((j ^ t_lo) << 4);
+                    uint8_t *dst = ring_tile + (q >> 2) * (TT * 128) + t_lo * 128;
+                    const int o_lo = (c ^ t_lo) << 4, o_hi = ((c + 1) ^ t_lo) << 4;
+#pragma unroll
+                    for (int u = 0; u < TT / 8; ++u) {
+                        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                        if (8 * u < nvl) {
+                            const uint4 w = *reinterpret_cast<const uint4 *>(src + u * 1024);
+                            lo = e4m3x8_to_f16x8(w.x, w.y);
+                            hi = e4m3x8_to_f16x8(w.z, w.w);
+                        }
+                        *reinterpret_cast<uint4 *>(dst + u * 1024 + o_lo) = lo;
+                        *reinterpret_cast<uint4 *>(dst + u * 1024 + o_hi) = hi;
+                    }
+                }
+                tc::fence_async_smem();  // the tensor core reads the widened tile
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&ring_full[i % NR]);
+                    mbar_arrive(&stg_empty[i % NSG]);
+                }
+            }
+        }
     } else {
         // ---------------- softmax: thread = query row = tensor-memory lane ----------------
         const int rho = row0 + threadIdx.x;  // this thread's row (tensor-memory lane threadIdx.x)
@@ -517,6 +661,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
         const int t_end = min(L, (c_begin + n_my) * kChunk);
         const int lim = live ? min(L - p.q_len + rho / G, t_end - 1) : -1;
         const int lo = p.window > 0 ? L - p.q_len + rho / G - p.window + 1 : 0;  // first key of the row's window
+        const float sl = F8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;  // fp8: K's scale joins q's
         float m_ref = -INFINITY, l_sum = 0.f;
         bool ok = true;
         // O += P_k V_k of tile k is waited for in order per barrier (tile k + 2,
@@ -550,7 +695,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
             float mx = -INFINITY;
 #pragma unroll
             for (int c = 0; c < TT; ++c) {
-                sv[c] = (t0 + c <= lim && t0 + c >= lo) ? sv[c] * p.scale_log2 : -INFINITY;
+                sv[c] = (t0 + c <= lim && t0 + c >= lo) ? sv[c] * sl : -INFINITY;
                 mx = fmaxf(mx, sv[c]);
             }
             // lazy rescale: only when the max grows by more than 2^kLazy, and
@@ -579,7 +724,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
             // end hold stale data (even NaN), and 0 * NaN would reach O through
             // the tensor core, so zero them before the P.V product reads them.
             const int nv = min(TT, t_end - t0);
-            if (nv < TT) {
+            if (!F8 && nv < TT) {  // (fp8: the widening warp writes those rows as zeros)
                 if (!__all_sync(0xffffffffu, mbar_wait(&v_full[i % NV], (i / NV) & 1, &flags[0]))) {
                     ok = false;
                     break;
@@ -601,7 +746,10 @@ __global__ void __launch_bounds__(6 * 32, 1)
                 const float p0 = (m_ref == -INFINITY) ? 0.f : fast_exp2(sv[2 * c] - m_ref);
                 const float p1 = (m_ref == -INFINITY) ? 0.f : fast_exp2(sv[2 * c + 1] - m_ref);
                 ps += p0 + p1;
-                split_bf16(p0, p1, hw[c], lw[c]);
+                if constexpr (F8)
+                    split_f16(p0, p1, hw[c], lw[c]);
+                else
+                    split_bf16(p0, p1, hw[c], lw[c]);
             }
             l_sum += ps;
             tc::st32(lane_base + C::S_COL + j * TT, hw);
@@ -616,7 +764,7 @@ __global__ void __launch_bounds__(6 * 32, 1)
         if (!ok) flags[0] = 1;
         tc::fence_after();
         const bool poisoned = !ok || flags[1] != 0;
-        const float inv = (poisoned || !(l_sum > 0.f)) ? 0.f : 1.f / l_sum;
+        const float inv = (poisoned || !(l_sum > 0.f)) ? 0.f : (F8 ? p.v_scale[kvh] : 1.f) / l_sum;
         const size_t orow = live ? ((size_t)b * p.q_len + rho / G) * p.num_q_heads + kvh * G + rho % G : 0;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 16) {

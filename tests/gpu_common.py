@@ -55,7 +55,8 @@ def run_attention(prob, layer=0, *, num_splits=0, out_dtype=pa.PA_OUT_F32, max_s
     status = torch.zeros(1, dtype=torch.int32, device=q.device)
     if prob.kv_fp8:
         ks, vs = scales_dev(prob, layer, q.device)
-        pa.paged_attention_decode_fp8(q, kc, vc, ks, vs, bt, sl, desc, out, ws, status)
+        fn = pa.paged_attention_decode_fp8 if prob.q_len == 1 else pa.paged_attention_verify_fp8
+        fn(q, kc, vc, ks, vs, bt, sl, desc, out, ws, status)
     else:
         fn = pa.paged_attention_decode if prob.q_len == 1 else pa.paged_attention_verify
         fn(q, kc, vc, bt, sl, desc, out, ws, status)

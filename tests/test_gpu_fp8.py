@@ -14,7 +14,7 @@ import torch
 import paged_attention_decode_split_gb300 as pa
 from paged_attention_decode_split_gb300 import _build
 from paged_attention_decode_split_gb300.inputs import WORKLOADS, make_new_tokens, make_problem
-from tests.gpu_common import assert_parity, desc_for, oracle_out, run_attention, scales_dev, to_dev
+from tests.gpu_common import REL_L2_VERIFY, assert_parity, desc_for, oracle_out, run_attention, scales_dev, to_dev
 from tests.helpers import bits
 
 pytestmark = pytest.mark.gpu
@@ -217,3 +217,61 @@ def test_decode_fp8_rejects_missing_scales():
     out = torch.empty((1, 24, 256), device="cuda")
     with pytest.raises(pa.PagedAttnError):
         pa.paged_attention_decode_fp8(q, kc, vc, None, None, bt, sl, desc, out)
+
+
+# -- verify over the fp8 cache (tcgen05, f16 products) --------------------------------
+
+@pytest.mark.parametrize("q_len,lens,bs", [(2, [2, 33, 900], 16), (5, [5, 64, 785], 784),
+                                           (16, [16, 17, 831, 1700], 832), (16, [3000], 16)])
+def test_verify_fp8_small(oracle_mod, q_len, lens, bs):
+    prob = hybrid(601 + q_len, lens, bs, q_len=q_len, poison_unused=True)
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"fp8 verify q_len={q_len}")
+
+
+@pytest.mark.parametrize("splits", [2, 5, 13])
+def test_verify_fp8_forced_splits(oracle_mod, splits):
+    prob = hybrid(611 + splits, [1700, 900, 37], 784, q_len=16, poison_unused=True)
+    out, status, plan = run_attention(prob, num_splits=splits)
+    assert status == 0 and plan["num_splits"] > 1
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"fp8 verify splits={splits}")
+
+
+@pytest.mark.parametrize("q_len,lens,window", [(48, [1000, 48], 0), (200, [1500], 300), (16, [3000, 500], 1024)])
+def test_verify_fp8_row_blocks_and_window(oracle_mod, q_len, lens, window):
+    prob = hybrid(621 + q_len, lens, 784, q_len=q_len, poison_unused=True)
+    out, status, _ = run_attention(prob, window=window)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob, window=window), rel_l2=REL_L2_VERIFY,
+                  what=f"fp8 verify q_len={q_len} W={window}")
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_verify_fp8_dense_d128(oracle_mod, splits):
+    prob = make_problem(631, num_seqs=2, seq_lens=[300, 77], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, q_len=8, scale=1 / math.sqrt(128), poison_unused=True, kv_fp8=True)
+    out, status, _ = run_attention(prob, num_splits=splits)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what="fp8 verify d128")
+
+
+def test_verify_fp8_early_kv_bitwise():
+    prob = hybrid(641, [16, 17, 831, 1700], 832, q_len=16, poison_unused=True)
+    outs = []
+    for flags in (0, pa.PA_FLAG_EARLY_KV_READ):
+        out, status, _ = run_attention(prob, flags=flags)
+        assert status == 0
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_verify_fp8_b8_q16_l8192_bs832_workload(oracle_mod):
+    prob = make_problem(1010, **dict(WORKLOADS["verify_b8_q16_l8192_bs832"], kv_fp8=True))
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    rows = [0, 3, 7]
+    sel = torch.cat([torch.arange(b * 16, (b + 1) * 16) for b in rows])
+    assert torch.isfinite(out).all()
+    assert_parity(out[sel], oracle_out(oracle_mod, prob, rows=rows), rel_l2=REL_L2_VERIFY,
+                  what="fp8 verify workload (sampled)")
