@@ -132,25 +132,36 @@ class ClockSampler:
 
 
 def dist_setup(n_gpus):
+    """One process per GPU under torchrun (NCCL); replicas exchange only the
+    barrier and the max of their timings.  Without a GPU (host-side tests of
+    this logic) the group runs on gloo."""
     import torch
     import torch.distributed as dist
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
 
 
-def barrier(world):
+def _device_sync():
     import torch
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+
+
+def barrier(world):
     import torch.distributed as dist
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
+    _device_sync()
 
 
 def max_over_ranks(world, value: float) -> float:
@@ -158,9 +169,16 @@ def max_over_ranks(world, value: float) -> float:
     import torch.distributed as dist
     if world == 1:
         return value
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the bytes every replica processed in one step over
+    the slowest replica's step time (weak scaling: fixed work per GPU)."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------------
@@ -326,7 +344,7 @@ def bench_gpu(args, world, rank, local):
     call_us = [dec_events[k].elapsed_time(dec_events[k + 1]) * 1e3 / n_layers for k in range(dec_reps)]
 
     bytes_step = n_layers * B * L * KV_BYTES_PER_TOKEN_LAYER
-    value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, bytes_step, ms_per_step)
     peak, peak_kind = load_peaks()
     avg_call_us = dec_events[0].elapsed_time(dec_events[-1]) * 1e3 / (dec_reps * n_layers)
     achieved = (B * L * KV_BYTES_PER_TOKEN_LAYER) / (avg_call_us * 1e-6) / 1e9

@@ -1,0 +1,57 @@
+"""Host-side checks of the multi-GPU path, which is replicas only (each GPU
+runs its own sequences; no exchange on the data path): two gloo ranks on the
+CPU go through bench.py's process-group set-up, barrier, max-over-ranks timing
+and whole-job aggregation, and the reference arm does its work on rank 0 only."""
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world), RANK=str(rank),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import argparse
+    import torch.distributed as dist
+    import bench
+    w, r, local = bench.dist_setup(world)
+    backend = dist.get_backend()
+    bench.barrier(w)
+    slowest = bench.max_over_ranks(w, 10.0 + rank)  # rank 1 is the slow one
+    gbs = bench.whole_job_gbs(w, 1 << 30, slowest)
+    # the reference arm: rank 0 works and prints, the others return at once
+    ran = False
+    if r != 0:
+        args = argparse.Namespace(steps=1, warmup=0, reference_budget=1.0)
+        bench.bench_reference(args, w, r)
+        ran = True
+    bench.barrier(w)
+    dist.destroy_process_group()
+    with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+        json.dump({"world": w, "rank": r, "backend": backend, "slowest": slowest, "gbs": gbs,
+                   "reference_returned": ran}, f)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-side test: with a GPU the group would use NCCL")
+def test_two_gloo_replicas(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, start_method="spawn")
+    recs = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)]
+    for r, rec in enumerate(recs):
+        assert rec["world"] == world and rec["rank"] == r and rec["backend"] == "gloo"
+        assert rec["slowest"] == 11.0  # the max over ranks, seen by every rank
+        assert rec["gbs"] == pytest.approx(2 * (1 << 30) / 11e-3 / 1e9)
+    assert recs[1]["reference_returned"] is True
