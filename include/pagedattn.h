@@ -132,8 +132,7 @@ typedef struct {
 } pa_plan_info;
 
 #define PA_PATH_DECODE_CUDA_CORE 1  /* split-KV decode, CUDA cores, TMA-staged chunks */
-#define PA_PATH_VERIFY_MMA 2        /* multi-row verify, tensor-core mma.sync */
-#define PA_PATH_VERIFY_TCGEN05 3    /* multi-row verify, tcgen05 + TMEM */
+#define PA_PATH_VERIFY_TCGEN05 3    /* multi-row verify, tcgen05 + TMEM (2 is not used) */
 
 /* Bytes of device workspace an attention call with this description needs
  * (split partials: out vectors, max and sum per split).  0 when the plan does

@@ -21,15 +21,16 @@ __all__ = [
     "reshape_and_cache", "paged_attention_decode", "paged_attention_verify", "last_plan",
     "status_string", "PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_WORKSPACE",
     "PA_ERR_CUDA", "PA_OUT_F32", "PA_OUT_BF16", "PA_DEV_BAD_SEQLEN", "PA_DEV_BAD_PAGE",
-    "PA_DEV_BAD_SLOT", "PA_DEV_TIMEOUT", "PA_PATH_DECODE_CUDA_CORE", "PA_PATH_VERIFY_MMA",
-    "PA_PATH_VERIFY_TCGEN05",
+    "PA_DEV_BAD_SLOT", "PA_DEV_TIMEOUT", "PA_PATH_DECODE_CUDA_CORE",
+    "PA_PATH_VERIFY_TCGEN05", "PA_FLAG_EARLY_KV_READ", "PA_NOALLOC_SCRATCH_BYTES", "paged_attention_decode_noalloc",
 ]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, 1, 2, 3, 4
 PA_OUT_F32, PA_OUT_BF16 = 0, 1
 PA_DEV_BAD_SEQLEN, PA_DEV_BAD_PAGE, PA_DEV_BAD_SLOT, PA_DEV_TIMEOUT = 1, 2, 4, 8
-PA_PATH_DECODE_CUDA_CORE, PA_PATH_VERIFY_MMA, PA_PATH_VERIFY_TCGEN05 = 1, 2, 3
+PA_PATH_DECODE_CUDA_CORE, PA_PATH_VERIFY_TCGEN05 = 1, 3
 PA_FLAG_EARLY_KV_READ = 1
+PA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libpagedattn.so")
@@ -97,6 +98,9 @@ def load_library(path: str | None = None):
             fn.restype = ctypes.c_int
             fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc), _vp, _vp, ctypes.c_size_t,
                            _vp, _vp]
+        lib.pa_paged_attention_decode_noalloc.restype = ctypes.c_int
+        lib.pa_paged_attention_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc), _vp,
+                                                          _vp, _vp]
         for name in ("pa_paged_attention_decode", "pa_paged_attention_verify"):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
@@ -172,6 +176,16 @@ def paged_attention_decode(q, k_cache, v_cache, block_table, seq_lens, desc: Att
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
         _ptr(workspace), ws, _ptr(status), _stream(stream))
     _check(rc, "pa_paged_attention_decode")
+
+
+def paged_attention_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, status=None,
+                                   stream=None) -> None:
+    """Decode without a workspace argument (split partials in the library's
+    device scratch array; calls that overlap on the GPU must be ordered)."""
+    rc = load_library().pa_paged_attention_decode_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
+        _ptr(status), _stream(stream))
+    _check(rc, "pa_paged_attention_decode_noalloc")
 
 
 def paged_attention_verify(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, workspace=None,

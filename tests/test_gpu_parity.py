@@ -227,7 +227,7 @@ def test_verify_small(oracle_mod, q_len, lens, bs):
     prob = hybrid(111 + q_len, lens, bs, q_len=q_len, poison_unused=True)
     write_new_rows(prob, 5)
     out, status, plan = run_attention(prob)
-    assert status == 0 and plan["path_id"] in (pa.PA_PATH_VERIFY_MMA, pa.PA_PATH_VERIFY_TCGEN05)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
     assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"verify q_len={q_len}")
 
 

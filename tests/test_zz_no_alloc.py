@@ -89,3 +89,15 @@ def test_noalloc_rejects_plans_beyond_its_scratch(lib):
     fake = 0x10000  # never dereferenced: the size check comes first
     rc = lib.pa_paged_attention_decode_noalloc(fake, fake, fake, fake, fake, ctypes.byref(desc), fake, None, None)
     assert rc == pa.PA_ERR_WORKSPACE
+
+
+def test_noalloc_through_the_binding(lib):
+    prob = hybrid(97, [3000, 17], 784)
+    rc, ref, status = run_noalloc(lib, prob)
+    assert rc == pa.PA_OK and status == 0
+    q, kc, vc, bt, sl = to_dev(prob)
+    out = torch.full((prob.num_seqs, prob.num_q_heads, prob.head_dim), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.paged_attention_decode_noalloc(q, kc, vc, bt, sl, desc_for(prob), out, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0 and torch.equal(out.cpu(), ref)
