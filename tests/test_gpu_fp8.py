@@ -275,3 +275,10 @@ def test_verify_fp8_b8_q16_l8192_bs832_workload(oracle_mod):
     assert torch.isfinite(out).all()
     assert_parity(out[sel], oracle_out(oracle_mod, prob, rows=rows), rel_l2=REL_L2_VERIFY,
                   what="fp8 verify workload (sampled)")
+
+
+def test_verify_fp8_wide_group_g12(oracle_mod):
+    prob = hybrid(651, [5, 900, 2000], 784, q_len=5, num_q_heads=48, num_kv_heads=4, poison_unused=True)
+    out, status, _ = run_attention(prob)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what="fp8 verify G=12")
