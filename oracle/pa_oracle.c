@@ -24,7 +24,7 @@
  *              (flozi.net), Lektion 3: verify rows share K/V tiles, a causal
  *              mask is applied per row, partial softmax statistics are merged.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - query head h reads KV head h / (num_q_heads / num_kv_heads)  (contiguous GQA);
  *   - seq_lens[b] counts every cached token of sequence b, including the q_len
  *     rows just written; row r (0-based) of a q_len-row block sees keys
