@@ -93,8 +93,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // x = head + residual with both parts in bf16 (packed pairs for elements a, b).
 __device__ __forceinline__ void split_bf16(float a, float b, uint32_t &head, uint32_t &resid) {
     head = pack_bf16(a, b);
-    const float ha = __uint_as_float(head << 16), hb = __uint_as_float(head & 0xffff0000u);
-    resid = pack_bf16(a - ha, b - hb);
+    const float2 h = make_float2(__uint_as_float(head << 16), __uint_as_float(head & 0xffff0000u));
+    const float2 r = __ffma2_rn(h, make_float2(-1.f, -1.f), make_float2(a, b));  // (a, b) - head, exact
+    resid = pack_bf16(r.x, r.y);
 }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -106,7 +107,8 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 __device__ __forceinline__ void split_f16(float a, float b, uint32_t &head, uint32_t &resid) {
     head = pack_f16(a, b);
     const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&head));
-    resid = pack_f16(a - h.x, b - h.y);
+    const float2 r = __ffma2_rn(h, make_float2(-1.f, -1.f), make_float2(a, b));
+    resid = pack_f16(r.x, r.y);
 }
 
 // Two bf16 (packed) -> two f16 (packed); exact for the magnitudes q takes.
@@ -201,6 +203,16 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
+// 16 consecutive fp32 columns, without waiting (tcgen05.wait::ld before use).
+__device__ __forceinline__ void ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // 32 consecutive 32-bit columns of this thread's tensor-memory lane.
 __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
@@ -679,12 +691,13 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
             }
             tc::fence_after();
             float sv[TT];
+            {
+                uint32_t r[TT / 16][16];  // the tile's scores: all loads in flight, one wait
 #pragma unroll
-            for (int c0 = 0; c0 < TT; c0 += 16) {
-                float t16[16];
-                tc::ld16(lane_base + C::S_COL + j * TT + c0, t16);
+                for (int c0 = 0; c0 < TT / 16; ++c0) tc::ld16_nowait(lane_base + C::S_COL + j * TT + 16 * c0, r[c0]);
+                tc::wait_ld();
 #pragma unroll
-                for (int c = 0; c < 16; ++c) sv[c0 + c] = t16[c];
+                for (int c = 0; c < TT; ++c) sv[c] = __uint_as_float(r[c / 16][c % 16]);
             }
             if (i >= 2 && !wait_pv(i - 2)) {
                 ok = false;
@@ -693,10 +706,23 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
 
             const int t0 = (c_begin + i * CPT) * kChunk;
             float mx = -INFINITY;
+            // the exponent is 2^(sv * mul - m): raw scores with mul = scale when
+            // every key of the tile is visible to this row (no mask, and the
+            // max of the scaled scores is the scaled max for scale > 0), else
+            // scaled and masked scores with mul = 1
+            float mul = 1.f;
+            if (sl > 0.f && t0 + TT - 1 <= lim && t0 >= lo) {
+                float mr = sv[0];
 #pragma unroll
-            for (int c = 0; c < TT; ++c) {
-                sv[c] = (t0 + c <= lim && t0 + c >= lo) ? sv[c] * sl : -INFINITY;
-                mx = fmaxf(mx, sv[c]);
+                for (int c = 1; c < TT; ++c) mr = fmaxf(mr, sv[c]);
+                mx = mr * sl;
+                mul = sl;
+            } else {
+#pragma unroll
+                for (int c = 0; c < TT; ++c) {
+                    sv[c] = (t0 + c <= lim && t0 + c >= lo) ? sv[c] * sl : -INFINITY;
+                    mx = fmaxf(mx, sv[c]);
+                }
             }
             // lazy rescale: only when the max grows by more than 2^kLazy, and
             // then only after the previous tile's P.V product has finished
@@ -739,19 +765,21 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
             }
             // P = 2^(s - m) as a bf16 head and a bf16 residual, written over S_i
             // (tokens packed two per column: head in the first 32 columns)
-            float ps = 0.f;
+            // with no visible key yet (m = -inf) every p is 0: 2^(x - inf)
+            const float m_use = m_ref == -INFINITY ? INFINITY : m_ref;
+            float2 ps2 = make_float2(0.f, 0.f);
             uint32_t hw[TT / 2], lw[TT / 2];
 #pragma unroll
             for (int c = 0; c < TT / 2; ++c) {
-                const float p0 = (m_ref == -INFINITY) ? 0.f : fast_exp2(sv[2 * c] - m_ref);
-                const float p1 = (m_ref == -INFINITY) ? 0.f : fast_exp2(sv[2 * c + 1] - m_ref);
-                ps += p0 + p1;
+                const float p0 = fast_exp2(fmaf(sv[2 * c], mul, -m_use));
+                const float p1 = fast_exp2(fmaf(sv[2 * c + 1], mul, -m_use));
+                ps2 = __fadd2_rn(ps2, make_float2(p0, p1));
                 if constexpr (F8)
                     split_f16(p0, p1, hw[c], lw[c]);
                 else
                     split_bf16(p0, p1, hw[c], lw[c]);
             }
-            l_sum += ps;
+            l_sum += ps2.x + ps2.y;
             tc::st32(lane_base + C::S_COL + j * TT, hw);
             tc::st32(lane_base + C::S_COL + j * TT + TT / 2, lw);
             tc::wait_st();
