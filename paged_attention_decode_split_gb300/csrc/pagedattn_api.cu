@@ -111,9 +111,14 @@ pa_status make_plan(const pa_attn_desc *d, bool verify, Plan *pl) {
         // never spills a few CTAs into a second wave
         splits = static_cast<int>(std::max<int64_t>(1, sms / units));
         splits = std::min(splits, std::max(1, n_chunks / kMinChunksPerSplit));
-        // long contexts are cut further to bound the longest CTA -- unless the
-        // units alone already fill the SMs (a verify with many row blocks)
-        if (units < sms) splits = std::max(splits, (n_chunks + kMaxChunksPerSplit - 1) / kMaxChunksPerSplit);
+        // decode: long contexts are cut further to bound the longest CTA (a
+        // batch of mixed lengths then balances over several waves).  Verify
+        // CTAs carry a large fixed cost (Q into tensor memory, the pipeline
+        // fill), so verify stays at whole waves: for 8 sequences x 16 rows of
+        // the 32/8/128 shape, 2 splits (128 CTAs) take 74 us where the 3 the
+        // rule asks for (192 CTAs) take 100 us.
+        if (units < sms && !verify)
+            splits = std::max(splits, (n_chunks + kMaxChunksPerSplit - 1) / kMaxChunksPerSplit);
     }
     splits = std::max(1, std::min(splits, std::max(1, n_chunks)));
     int cps = std::max(1, (n_chunks + splits - 1) / splits);

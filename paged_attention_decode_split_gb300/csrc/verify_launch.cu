@@ -6,12 +6,12 @@ namespace pa {
 
 namespace {
 
-template <int D, int NK, int NV, int NSG>
+template <int D, int NK, int NV, int NSG, int NSB>
 cudaError_t launch_verify_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tk64,
                              const CUtensorMap &tv64, const VerifyParams &p, dim3 grid, cudaStream_t stream,
                              int slot) {
-    using C = VerifyTcCfg<D, NK, NV, NSG>;
-    auto kern = pa_verify_tc_kernel<D, NK, NV, NSG>;
+    using C = VerifyTcCfg<D, NK, NV, NSG, NSB>;
+    auto kern = pa_verify_tc_kernel<D, NK, NV, NSG, NSB>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
     // programmatic dependent launch: the set-up overlaps the work before it
@@ -40,8 +40,8 @@ cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const C
                           const CUtensorMap &tk64, const CUtensorMap &tv64, const VerifyParams &p, dim3 grid,
                           cudaStream_t stream) {
     (void)rows;  // each CTA runs one M = 128 block of rows
-    if (head_dim == 256) return launch_verify_tc<256, 4, 3, 0>(tk, tv, tk64, tv64, p, grid, stream, 32);
-    if (head_dim == 128) return launch_verify_tc<128, 6, 6, 0>(tk, tv, tk64, tv64, p, grid, stream, 33);
+    if (head_dim == 256) return launch_verify_tc<256, 4, 3, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 32);
+    if (head_dim == 128) return launch_verify_tc<128, 6, 6, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 33);
     return cudaErrorInvalidValue;
 }
 
@@ -49,8 +49,8 @@ cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const C
 // (D = 256: 2 K + 3 V slots of 32 KiB and 2 + 2 staging slots of 16 KiB).
 cudaError_t launch_verify_fp8(int head_dim, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tk64,
                               const CUtensorMap &tv64, const VerifyParams &p, dim3 grid, cudaStream_t stream) {
-    if (head_dim == 256) return launch_verify_tc<256, 2, 3, 2>(tk, tv, tk64, tv64, p, grid, stream, 45);
-    if (head_dim == 128) return launch_verify_tc<128, 4, 4, 4>(tk, tv, tk64, tv64, p, grid, stream, 46);
+    if (head_dim == 256) return launch_verify_tc<256, 2, 3, 2, 2>(tk, tv, tk64, tv64, p, grid, stream, 45);
+    if (head_dim == 128) return launch_verify_tc<128, 4, 4, 4, 2>(tk, tv, tk64, tv64, p, grid, stream, 46);
     return cudaErrorInvalidValue;
 }
 

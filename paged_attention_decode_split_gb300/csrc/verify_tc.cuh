@@ -28,10 +28,11 @@
 // the same reference max.  Because O is touched only then, the softmax of tile
 // i+1 overlaps the P.V product of tile i.
 //
-// Tensor memory (512 columns x 128 lanes): O fp32 in columns [0, D), S/P
-// buffers in [D, D + 128), Q as bf16 pairs in [D + 128, D + 128 + D/2).
-// Shared memory holds only K and V tiles, in two rings (4 K and 3 V slots of
-// 32 KiB for D = 256); a K slot is refilled once S_i is done:
+// Tensor memory (512 columns x 128 lanes): O fp32 in columns [0, D), NSB = 2
+// S/P buffers of 64 columns from D on, and Q as bf16 pairs after them.
+// Shared memory holds the K and V tiles in two rings (4 K and 3 V slots of
+// 32 KiB for D = 256) and the split's block-table entries; a K slot is
+// refilled once S_i is done:
 //   K_i [D/64 blocks][64 tokens][128 B], 128-byte swizzle, K-major: one 5-D TMA
 //       box of 64 tokens when the tile lies in one page, else 64-dim x 16-token
 //       boxes per chunk
@@ -127,6 +128,11 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint32_t w0, uint32_t w1) {
         : "r"(w0), "r"(w1));
     return r;
 }
+
+// Block-table entries a verify CTA stages in shared memory: with 16-token
+// pages a 64-token tile spans 4 pages, and a page lookup per chunk from global
+// memory would put a dependent load in front of every copy.
+constexpr int kVerifyPageTab = 256;
 
 namespace tc {
 
@@ -241,7 +247,9 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
 
 }  // namespace tc
 
-template <int D, int NK, int NV, int NSG = 0>
+// NSB: S/P tensor-memory buffers (the Q K^T products run up to NSB tiles ahead
+// of P V).
+template <int D, int NK, int NV, int NSG = 0, int NSB = 2>
 struct VerifyTcCfg {
     static constexpr bool F8 = NSG > 0;                // fp8 cache: e4m3 staging ring of NSG slots per tensor
     static constexpr int M = 128;                      // MMA rows (query rows, zero padded)
@@ -255,16 +263,17 @@ struct VerifyTcCfg {
     static constexpr int OFF_V = NK * TILE_BYTES;       // K ring, then V ring
     static constexpr int OFF_STG = OFF_V + NV * TILE_BYTES;  // K staging, then V staging
     static constexpr int OFF_BAR = OFF_STG + 2 * NSG * STG_BYTES;
-    // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done[2], mma_fin,
+    // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[NSB], p_full[NSB], o_done[NSB], mma_fin,
     // then (fp8) kst_full[NSG], kst_empty[NSG], vst_full[NSG], vst_empty[NSG]
-    static constexpr int OFF_TMEM = OFF_BAR + (2 * NK + 2 * NV + 7 + 4 * NSG) * 8;
+    static constexpr int OFF_TMEM = OFF_BAR + (2 * NK + 2 * NV + 3 * NSB + 1 + 4 * NSG) * 8;
     static constexpr int OFF_FLAGS = OFF_TMEM + 16;
-    static constexpr int SMEM_BYTES = OFF_FLAGS + 16 + 1024;
-    // tensor-memory columns: O (fp32, D), two S/P buffers (64 each), Q (bf16 pairs, D / 2)
+    static constexpr int OFF_PT = OFF_FLAGS + 16;                    // the split's block-table entries
+    static constexpr int SMEM_BYTES = OFF_PT + kVerifyPageTab * 4 + 1024;
+    // tensor-memory columns: O (fp32, D), NSB S/P buffers (64 each), Q (bf16 pairs, D / 2)
     static constexpr int TMEM_COLS = 512;
     static constexpr int O_COL = 0;
     static constexpr int S_COL = D;
-    static constexpr int Q_COL = D + 2 * TT;
+    static constexpr int Q_COL = D + NSB * TT;
     static constexpr int CW = 2;                       // fp8: widening warps per tensor
     static constexpr int THREADS = (F8 ? 6 + 2 * CW : 6) * 32;
     static_assert(D == 256 || D == 128, "head_dim 256 or 128");
@@ -275,12 +284,12 @@ struct VerifyTcCfg {
 // NSG > 0: fp8 cache (tm_k / tm_v: e4m3 boxes of 128 codes x 16 tokens,
 // tm_k64 / tm_v64: 5-D boxes of a whole 64-token tile, both with the 128-byte
 // swizzle).
-template <int D, int NK, int NV, int NSG>
-__global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
+template <int D, int NK, int NV, int NSG, int NSB>
+__global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
     pa_verify_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
                         const VerifyParams p) {
-    using C = VerifyTcCfg<D, NK, NV, NSG>;
+    using C = VerifyTcCfg<D, NK, NV, NSG, NSB>;
     constexpr bool F8 = C::F8;
     constexpr int TT = C::TT, CPT = C::CPT;
     constexpr float kLazy = 8.f;  // raise the reference max only when it grows by more than 2^8
@@ -292,16 +301,17 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
     uint64_t *k_empty = k_full + NK;
     uint64_t *v_full = k_empty + NK;
     uint64_t *v_empty = v_full + NV;
-    uint64_t *s_full = v_empty + NV; // [2]: S_i written (tile parity)
-    uint64_t *p_full = s_full + 2;   // [2]: P_i written by the softmax warps
-    uint64_t *o_done = p_full + 2;   // [2]: O += P_i V_i finished
-    uint64_t *mma_fin = o_done + 2;
+    uint64_t *s_full = v_empty + NV;   // [NSB]: S_i written (buffer i % NSB)
+    uint64_t *p_full = s_full + NSB;   // [NSB]: P_i written by the softmax warps
+    uint64_t *o_done = p_full + NSB;   // [NSB]: O += P_i V_i finished
+    uint64_t *mma_fin = o_done + NSB;
     uint64_t *kst_full = mma_fin + 1;  // fp8: e4m3 tile landed in a staging slot
     uint64_t *kst_empty = kst_full + NSG;  // fp8: staging slot widened, free again
     uint64_t *vst_full = kst_empty + NSG;
     uint64_t *vst_empty = vst_full + NSG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::OFF_FLAGS);  // [0] abort, [1] bad page
+    int32_t *page_tab = reinterpret_cast<int32_t *>(smem + C::OFF_PT);
 
     const int split = blockIdx.x, b = blockIdx.z;
     const int kvh = blockIdx.y % p.num_kv_heads;
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
             mbar_init(&v_full[s], F8 ? C::CW : 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < NSB; ++j) {
             mbar_init(&s_full[j], 1);
             mbar_init(&p_full[j], 128);
             mbar_init(&o_done[j], 1);
@@ -383,8 +393,17 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
     }
     const int n_tiles = (n_my + CPT - 1) / CPT;
 
-    // TMA copies of one tile (4 chunks) of K or of V; state of the producer lane.
+    // The split's block-table entries, staged in shared memory by all threads
+    // (visible to the producer after the next __syncthreads); splits spanning
+    // more pages read the table from global memory.
     const int32_t *bt = p.block_table + (size_t)b * p.max_pages_per_seq;
+    const int lp_first = (c_begin * kChunk) / p.block_size;
+    const int n_pt = ((c_begin + n_my) * kChunk - 1) / p.block_size - lp_first + 1;
+    const bool staged = n_pt <= kVerifyPageTab;
+    if (staged)
+        for (int j = threadIdx.x; j < n_pt; j += C::THREADS) page_tab[j] = bt[lp_first + j];
+
+    // TMA copies of one tile (4 chunks) of K or of V; state of the producer lane.
     int lp_cache[2] = {-1, -1}, page_cache[2] = {0, 0};  // per tensor: last page looked up
     int issued_k = 0, issued_v = 0;
     auto issue_tile = [&](int i, int tensor, uint64_t policy) {
@@ -401,7 +420,7 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
             const int lp = t0 / p.block_size;
             if (lp != lp_cache[tensor]) {
                 lp_cache[tensor] = lp;
-                page_cache[tensor] = bt[lp];
+                page_cache[tensor] = staged ? page_tab[lp - lp_first] : bt[lp];
                 if (page_cache[tensor] < 0 || (int64_t)page_cache[tensor] >= p.num_pages) {
                     flags[1] = 1;
                     set_status(p.status, PA_DEV_BAD_PAGE);
@@ -550,9 +569,9 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
             bool ok = true;
             while (next_pv < n_tiles) {
                 bool progress = false;
-                if (next_pv < next_qk && mbar_test_wait(&p_full[next_pv & 1], (next_pv >> 1) & 1) &&
+                if (next_pv < next_qk && mbar_test_wait(&p_full[next_pv % NSB], (next_pv / NSB) & 1) &&
                     mbar_test_wait(&v_full[next_pv % NV], (next_pv / NV) & 1)) {
-                    const int i = next_pv, j = i & 1;
+                    const int i = next_pv, j = i % NSB;
                     tc::fence_after();
                     const uint32_t v_addr = smem_addr(smem + C::OFF_V + (i % NV) * C::TILE_BYTES);
 #pragma unroll
@@ -571,8 +590,8 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
                     ++next_pv;
                     progress = true;
                 }
-                if (next_qk < n_tiles && next_qk - next_pv < 2) {
-                    const int i = next_qk, s = i % NK, j = i & 1;
+                if (next_qk < n_tiles && next_qk - next_pv < NSB) {
+                    const int i = next_qk, s = i % NK, j = i % NSB;
                     if (mbar_test_wait(&k_full[s], (i / NK) & 1)) {
                         tc::fence_after();
                         const uint32_t k_addr = smem_addr(smem + s * C::TILE_BYTES);
@@ -676,16 +695,16 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
         const float sl = F8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;  // fp8: K's scale joins q's
         float m_ref = -INFINITY, l_sum = 0.f;
         bool ok = true;
-        // O += P_k V_k of tile k is waited for in order per barrier (tile k + 2,
-        // where it is long finished), so no wait ever tests a phase parity
+        // O += P_k V_k of tile k is waited for in order per barrier (tile k +
+        // NSB, where it is long finished), so no wait ever tests a phase parity
         // two phases behind the barrier.
         auto wait_pv = [&](int k) {
-            return __all_sync(0xffffffffu, mbar_wait(&o_done[k & 1], (k >> 1) & 1, &flags[0]));
+            return __all_sync(0xffffffffu, mbar_wait(&o_done[k % NSB], (k / NSB) & 1, &flags[0]));
         };
         for (int i = 0; i < n_tiles; ++i) {
-            const int j = i & 1;
+            const int j = i % NSB;
             // waits ahead of a warp-collective tensor-memory access end the same way for the whole warp
-            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j], (i >> 1) & 1, &flags[0]))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j], (i / NSB) & 1, &flags[0]))) {
                 ok = false;
                 break;
             }
@@ -699,7 +718,7 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG>::THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < TT; ++c) sv[c] = __uint_as_float(r[c / 16][c % 16]);
             }
-            if (i >= 2 && !wait_pv(i - 2)) {
+            if (i >= NSB && !wait_pv(i - NSB)) {
                 ok = false;
                 break;
             }

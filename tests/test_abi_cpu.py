@@ -190,3 +190,17 @@ def test_fp8_entries_reject_bad_arguments(lib):
     assert rc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 12, 16, 10, None, None) == pa.PA_ERR_UNSUPPORTED
     assert rc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 256, 16, 10, None, None) == pa.PA_ERR_INVALID_ARG
     assert rc(None, None, None, None, None, None, None, 0, 4, 256, 16, 10, None, None) == pa.PA_OK
+
+
+def test_verify_plan_stays_at_whole_waves(lib):
+    """Verify grids stay within whole waves of 152 CTAs even for long contexts
+    (the decode-only rule that cuts splits to at most 256 chunks is not applied):
+    8 x 8 units of the 32/8/128 shape at 8208 tokens take 2 splits (128 CTAs)."""
+    dense = hybrid_desc(num_seqs=8, q_len=16, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=784,
+                        max_pages_per_seq=11, max_seq_len=8208, num_pages=100)
+    rows = 8 * 16 * 32
+    assert pa.workspace_bytes(dense) == ((rows * 2 * 128 * 4 + 255) // 256 * 256) + rows * 2 * 8
+    # decode of the same context keeps the rule: 8 x 8 units, 513 chunks -> 3 splits
+    dec = hybrid_desc(num_seqs=8, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=784,
+                      max_pages_per_seq=11, max_seq_len=8208, num_pages=100)
+    assert pa.workspace_bytes(dec) == ((8 * 32 * 3 * 128 * 4 + 255) // 256 * 256) + 8 * 32 * 3 * 8
