@@ -120,6 +120,13 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 
 // 2^x with the hardware approximation instruction (ex2.approx, relative error
 // about 2^-22); exp2(-inf) = +0.
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -733,15 +733,15 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
             if (sl > 0.f && t0 + TT - 1 <= lim && t0 >= lo) {
                 float mr = sv[0];
 #pragma unroll
-                for (int c = 1; c < TT; ++c) mr = fmaxf(mr, sv[c]);
+                for (int c = 1; c + 1 < TT; c += 2) mr = fmax3(mr, sv[c], sv[c + 1]);
+                mr = fmaxf(mr, sv[TT - 1]);
                 mx = mr * sl;
                 mul = sl;
             } else {
 #pragma unroll
-                for (int c = 0; c < TT; ++c) {
-                    sv[c] = (t0 + c <= lim && t0 + c >= lo) ? sv[c] * sl : -INFINITY;
-                    mx = fmaxf(mx, sv[c]);
-                }
+                for (int c = 0; c < TT; ++c) sv[c] = (t0 + c <= lim && t0 + c >= lo) ? sv[c] * sl : -INFINITY;
+#pragma unroll
+                for (int c = 0; c < TT; c += 2) mx = fmax3(mx, sv[c], sv[c + 1]);
             }
             // lazy rescale: only when the max grows by more than 2^kLazy, and
             // then only after the previous tile's P.V product has finished
