@@ -403,10 +403,15 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
     if (staged)
         for (int j = threadIdx.x; j < n_pt; j += C::THREADS) page_tab[j] = bt[lp_first + j];
 
-    // TMA copies of one tile (4 chunks) of K or of V; state of the producer lane.
-    int lp_cache[2] = {-1, -1}, page_cache[2] = {0, 0};  // per tensor: last page looked up
+    // TMA copies of one tile (4 chunks) of K or of V, issued by the whole
+    // producer warp: lane 0 arms the barrier; a tile inside one page is one
+    // 5-D box (lane 0), otherwise lane c * NB + b copies column block b of
+    // chunk c, so a tile over 16-token pages (16 boxes per tensor for D = 256)
+    // costs no more issue time than one box.
     int issued_k = 0, issued_v = 0;
     auto issue_tile = [&](int i, int tensor, uint64_t policy) {
+        constexpr int NB = F8 ? D / 128 : C::DB;  // boxes per 16-token chunk (128-byte columns)
+        constexpr int BW = F8 ? 128 : 64;         // elements per box row
         const int s = F8 ? i % (NSG > 0 ? NSG : 1) : (tensor == 0 ? i % NK : i % NV);
         uint64_t *bar = F8 ? (tensor == 0 ? &kst_full[s] : &vst_full[s]) : (tensor == 0 ? &k_full[s] : &v_full[s]);
         uint8_t *dst0 = F8 ? smem + C::OFF_STG + (tensor * NSG + s) * C::STG_BYTES
@@ -414,49 +419,36 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
         const CUtensorMap *m4 = tensor == 0 ? &tm_k : &tm_v;
         const CUtensorMap *m5 = tensor == 0 ? &tm_k64 : &tm_v64;
         const int nc = min(CPT, n_my - i * CPT);  // chunks in this tile
-        mbar_arrive_expect_tx(bar, nc * C::CHUNK_BYTES);
-        for (int c = 0; c < nc; ++c) {
-            const int t0 = (c_begin + i * CPT + c) * kChunk;
-            const int lp = t0 / p.block_size;
-            if (lp != lp_cache[tensor]) {
-                lp_cache[tensor] = lp;
-                page_cache[tensor] = staged ? page_tab[lp - lp_first] : bt[lp];
-                if (page_cache[tensor] < 0 || (int64_t)page_cache[tensor] >= p.num_pages) {
-                    flags[1] = 1;
-                    set_status(p.status, PA_DEV_BAD_PAGE);
-                }
+        if (lane == 0) mbar_arrive_expect_tx(bar, nc * C::CHUNK_BYTES);
+        __syncwarp();
+        auto page_of = [&](int lp) {
+            const int page = staged ? page_tab[lp - lp_first] : bt[lp];
+            if (page < 0 || (int64_t)page >= p.num_pages) {
+                flags[1] = 1;  // the copy reads zeros (box outside the tensor)
+                set_status(p.status, PA_DEV_BAD_PAGE);
             }
-            const int page = page_cache[tensor];
-            const int off = t0 - lp * p.block_size;
-            if constexpr (F8) {
-                // e4m3 in 128-code column blocks: the whole tile in one copy when it lies in one page
-                if (c == 0 && nc == CPT && off + TT <= p.block_size) {
-                    tma_load_5d(dst0, m5, bar, 0, off, 0, kvh, page, policy);
-                    break;
-                }
-#pragma unroll
-                for (int db = 0; db < D / 128; ++db)
-                    tma_load_4d(dst0 + db * TT * 128 + c * kChunk * 128, m4, bar, db * 128, kvh, off, page, policy);
-                continue;
-            }
-            if (c == 0 && nc == CPT && off + TT <= p.block_size) {
-                // the whole tile lies in one page: one copy lands it as
-                // [D/64 blocks][64 tokens][128 B]
-                tma_load_5d(dst0, m5, bar, 0, off, 0, kvh, page, policy);
-                break;
-            }
-#pragma unroll
-            for (int db = 0; db < C::DB; ++db)
-                tma_load_4d(dst0 + db * TT * 128 + c * kChunk * 128, m4, bar, db * 64, kvh, off, page, policy);
+            return page;
+        };
+        const int t00 = (c_begin + i * CPT) * kChunk;
+        const int lp0 = t00 / p.block_size, off0 = t00 - lp0 * p.block_size;
+        if (nc == CPT && off0 + TT <= p.block_size) {
+            // the whole tile lies in one page: one copy lands it as [blocks][64 tokens][128 B]
+            if (lane == 0) tma_load_5d(dst0, m5, bar, 0, off0, 0, kvh, page_of(lp0), policy);
+        } else if (lane < nc * NB) {
+            const int c = lane / NB, db = lane % NB;
+            const int t0 = t00 + c * kChunk, lp = t0 / p.block_size;
+            tma_load_4d(dst0 + db * TT * 128 + c * kChunk * 128, m4, bar, db * BW, kvh, t0 - lp * p.block_size,
+                        page_of(lp), policy);
         }
+        __syncwarp();
     };
     // tiles that end before the new rows (early_kv reads only those before the wait)
     auto before_new_rows = [&](int i) {
         return (c_begin + i * CPT + min(CPT, n_my - i * CPT)) * kChunk <= L - p.q_len;
     };
     if (p.early_kv) {
-        __syncthreads();  // barrier initialisation is visible to the producer lane
-        if (warp == 5 && lane == 0) {
+        __syncthreads();  // barrier initialisation and the page table are visible to the producer warp
+        if (warp == 5) {
             // first use of each slot: tiles that end before the new rows
             const uint64_t policy = l2_policy_evict_first();
             constexpr int FK = F8 ? NSG : NK, FV = F8 ? NSG : NV;  // slots the copies land in
@@ -512,46 +504,49 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
 
     if (warp == 5) {
         // ---------------- producer: TMA copies of K and V, 4 chunks per tile ----------------
-        // Two rings refilled independently: the lane probes the next slot of
-        // each without blocking, and within a ring issues tiles in order.
-        if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_first();
-            uint32_t idle = 0;
-            // the slots the copies land in: the K/V rings, or the fp8 staging rings
-            constexpr int FK = F8 ? NSG : NK, FV = F8 ? NSG : NV;
-            uint64_t *ke = F8 ? kst_empty : k_empty;
-            uint64_t *ve = F8 ? vst_empty : v_empty;
-            while (issued_k < n_tiles || issued_v < n_tiles) {
-                bool progress = false;
-                if (issued_k < n_tiles &&
-                    (issued_k < FK || mbar_test_wait(&ke[issued_k % FK], ((issued_k / FK) - 1) & 1))) {
-                    issue_tile(issued_k++, 0, policy);
-                    progress = true;
-                }
-                if (issued_v < n_tiles &&
-                    (issued_v < FV || mbar_test_wait(&ve[issued_v % FV], ((issued_v / FV) - 1) & 1))) {
-                    issue_tile(issued_v++, 1, policy);
-                    progress = true;
-                }
-                if (progress) {
-                    idle = 0;
-                } else if (++idle > kWaitPollLimit || flags[0]) {
-                    flags[0] = 1;
+        // Two rings refilled independently: lane 0 probes the next slot of
+        // each without blocking and the warp issues the tile; within a ring
+        // tiles go in order.  Every decision is lane 0's, so the warp stays
+        // converged.
+        const uint64_t policy = l2_policy_evict_first();
+        uint32_t idle = 0;
+        // the slots the copies land in: the K/V rings, or the fp8 staging rings
+        constexpr int FK = F8 ? NSG : NK, FV = F8 ? NSG : NV;
+        uint64_t *ke = F8 ? kst_empty : k_empty;
+        uint64_t *ve = F8 ? vst_empty : v_empty;
+        while (issued_k < n_tiles || issued_v < n_tiles) {
+            bool go_k = false, go_v = false;
+            if (lane == 0) {
+                go_k = issued_k < n_tiles &&
+                       (issued_k < FK || mbar_test_wait(&ke[issued_k % FK], ((issued_k / FK) - 1) & 1));
+                go_v = issued_v < n_tiles &&
+                       (issued_v < FV || mbar_test_wait(&ve[issued_v % FV], ((issued_v / FV) - 1) & 1));
+            }
+            go_k = __shfl_sync(0xffffffffu, go_k, 0);
+            go_v = __shfl_sync(0xffffffffu, go_v, 0);
+            if (go_k) issue_tile(issued_k++, 0, policy);
+            if (go_v) issue_tile(issued_v++, 1, policy);
+            if (go_k || go_v) {
+                idle = 0;
+            } else {
+                const bool stop = __shfl_sync(0xffffffffu, ++idle > kWaitPollLimit || flags[0] != 0, 0);
+                if (stop) {
+                    if (lane == 0) flags[0] = 1;
                     break;
                 }
             }
-            if (flags[0]) {
-                // let the copies in flight land before the CTA ends
-                uint64_t *kf = F8 ? kst_full : k_full;
-                uint64_t *vf = F8 ? vst_full : v_full;
-                for (int i = max(0, issued_k - FK); i < issued_k; ++i)
-                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&kf[i % FK], (i / FK) & 1); ++n) {
-                    }
-                for (int i = max(0, issued_v - FV); i < issued_v; ++i)
-                    for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&vf[i % FV], (i / FV) & 1); ++n) {
-                    }
-                set_status(p.status, PA_DEV_TIMEOUT);
-            }
+        }
+        if (lane == 0 && flags[0]) {
+            // let the copies in flight land before the CTA ends
+            uint64_t *kf = F8 ? kst_full : k_full;
+            uint64_t *vf = F8 ? vst_full : v_full;
+            for (int i = max(0, issued_k - FK); i < issued_k; ++i)
+                for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&kf[i % FK], (i / FK) & 1); ++n) {
+                }
+            for (int i = max(0, issued_v - FV); i < issued_v; ++i)
+                for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(&vf[i % FV], (i / FV) & 1); ++n) {
+                }
+            set_status(p.status, PA_DEV_TIMEOUT);
         }
     } else if (warp == 4) {
         // ---------------- MMA issue: one lane ----------------
