@@ -51,7 +51,7 @@ cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, co
                 case 2: return launch_decode_t<256, 2, 1, 6, 4, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 1);
                 case 4: return launch_decode_t<256, 4, 2, 4, 6, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 2);
                 case 6: return launch_decode_t<256, 6, 2, 4, 6, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 3);
-                case 12: return launch_decode_t<256, 12, 2, 2, 12, 2, WIN, F8>(tk, tv, p, grid, stream, slot0 + 9);
+                case 12: return launch_decode_t<256, 12, 1, 4, 6, 3, WIN, F8>(tk, tv, p, grid, stream, slot0 + 9);
             }
         } else if (head_dim == 128) {
             switch (group) {
