@@ -400,17 +400,51 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
                                 hi[g] = a.x + a.y;
                         }
                     }
+                    // with an even number of heads, pairs of heads are added as packed
+                    // fp32 pairs (one instruction per two heads)
+                    if constexpr (GW % 2 == 0) {
 #pragma unroll
-                    for (int g = 0; g < GW; ++g) part[j][g] += __shfl_xor_sync(0xffffffffu, hi[g], 16);
+                        for (int g = 0; g < GW; g += 2) {
+                            const float2 x = __fadd2_rn(make_float2(part[j][g], part[j][g + 1]),
+                                                        make_float2(__shfl_xor_sync(0xffffffffu, hi[g], 16),
+                                                                    __shfl_xor_sync(0xffffffffu, hi[g + 1], 16)));
+                            part[j][g] = x.x;
+                            part[j][g + 1] = x.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < GW; ++g) part[j][g] += __shfl_xor_sync(0xffffffffu, hi[g], 16);
+                    }
                 }
                 // Rest of the transposing butterfly: 4 slots x GW -> 1 slot x GW.
+                if constexpr (GW % 2 == 0) {
+                    auto add2 = [&](float &a, float &b, float x, float y) {
+                        const float2 r = __fadd2_rn(make_float2(a, b), make_float2(x, y));
+                        a = r.x;
+                        b = r.y;
+                    };
 #pragma unroll
-                for (int g = 0; g < GW; ++g) {
+                    for (int g = 0; g < GW; g += 2) {
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) part[j][g] += __shfl_xor_sync(0xffffffffu, part[j + 2][g], 8);
-                    part[0][g] += __shfl_xor_sync(0xffffffffu, part[1][g], 4);
-                    part[0][g] += __shfl_xor_sync(0xffffffffu, part[0][g], 2);
-                    part[0][g] += __shfl_xor_sync(0xffffffffu, part[0][g], 1);
+                        for (int j = 0; j < 2; ++j)
+                            add2(part[j][g], part[j][g + 1], __shfl_xor_sync(0xffffffffu, part[j + 2][g], 8),
+                                 __shfl_xor_sync(0xffffffffu, part[j + 2][g + 1], 8));
+                        add2(part[0][g], part[0][g + 1], __shfl_xor_sync(0xffffffffu, part[1][g], 4),
+                             __shfl_xor_sync(0xffffffffu, part[1][g + 1], 4));
+                        add2(part[0][g], part[0][g + 1], __shfl_xor_sync(0xffffffffu, part[0][g], 2),
+                             __shfl_xor_sync(0xffffffffu, part[0][g + 1], 2));
+                        add2(part[0][g], part[0][g + 1], __shfl_xor_sync(0xffffffffu, part[0][g], 1),
+                             __shfl_xor_sync(0xffffffffu, part[0][g + 1], 1));
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < GW; ++g) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) part[j][g] += __shfl_xor_sync(0xffffffffu, part[j + 2][g], 8);
+                        part[0][g] += __shfl_xor_sync(0xffffffffu, part[1][g], 4);
+                        part[0][g] += __shfl_xor_sync(0xffffffffu, part[0][g], 2);
+                        part[0][g] += __shfl_xor_sync(0xffffffffu, part[0][g], 1);
+                    }
                 }
                 const bool valid = (mb * 8 + cg) < nv && (mb * 8 + cg) >= lead;
 #pragma unroll
