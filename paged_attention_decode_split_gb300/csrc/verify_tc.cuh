@@ -37,7 +37,8 @@
 //       box of 64 tokens when the tile lies in one page, else 64-dim x 16-token
 //       boxes per chunk
 //   V_i same layout as K_i, read as the MN-major (N = d) B operand
-// Warp roles: 0-3 softmax, 4 MMA issue (and tensor-memory allocation), 5 TMA.
+// Warp roles: 0-3 softmax, 4 MMA issue (and tensor-memory allocation), 5 TMA
+// (lane 0 decides, the whole warp issues a tile's boxes).
 //
 // fp8 e4m3 cache (NSG > 0): the copies land e4m3 tiles as [D/128 blocks][64
 // tokens][128 B] with the 128-byte swizzle in a staging ring of NSG slots per
