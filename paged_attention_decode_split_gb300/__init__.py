@@ -70,6 +70,8 @@ _vp = ctypes.c_void_p
 def load_library(path: str | None = None):
     """Load libpagedattn.so (built by ``_build.build()``); raises if absent."""
     global _lib
+    if _lib is not None and path is None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -145,10 +147,20 @@ def _ptr(t) -> int | None:
     return t.data_ptr()
 
 
+def _current_stream_handle() -> int:
+    """The current CUDA stream of the current device as a raw handle.  The raw
+    query avoids building a torch.cuda.Stream object on every call (about 5 us
+    of host time); the public path is the fallback."""
+    import torch
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
 def _stream(stream) -> int | None:
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream_handle()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream

@@ -158,9 +158,47 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
+// Encoded tensor maps are kept per host thread: a serving loop passes the same
+// cache tensors every step, and an encode costs microseconds of host time.  A
+// map depends only on the key (address and geometry), so a hit is exact.
+struct MapKey {
+    const void *base;
+    int64_t num_pages;
+    int32_t block_size, num_kv_heads, head_dim, box_d, kind;  // kind: 0 chunk box, 1 whole-tile 5-D box
+    bool swizzle128, fp8;
+    bool operator==(const MapKey &o) const {
+        return base == o.base && num_pages == o.num_pages && block_size == o.block_size &&
+               num_kv_heads == o.num_kv_heads && head_dim == o.head_dim && box_d == o.box_d && kind == o.kind &&
+               swizzle128 == o.swizzle128 && fp8 == o.fp8;
+    }
+};
+struct MapEntry {
+    CUtensorMap map;
+    MapKey key;
+    bool valid;
+};
+constexpr int kMapCache = 64;
+thread_local MapEntry g_maps[kMapCache];
+thread_local int g_map_next = 0;
+
+template <typename Encode>
+bool cached_map(CUtensorMap *map, const MapKey &key, Encode encode) {
+    for (const MapEntry &e : g_maps)
+        if (e.valid && e.key == key) {
+            *map = e.map;
+            return true;
+        }
+    if (!encode(map)) return false;
+    g_maps[g_map_next].map = *map;
+    g_maps[g_map_next].key = key;
+    g_maps[g_map_next].valid = true;
+    g_map_next = (g_map_next + 1) % kMapCache;
+    return true;
+}
+
 // Box = [box_d elements of d, 1 head, 16 tokens, 1 page]; fp8: one-byte elements.
-bool encode_cache_map(CUtensorMap *map, const void *base, const pa_attn_desc *d, int box_d, bool swizzle128,
-                      bool fp8 = false) {
+bool encode_cache_map_uncached(CUtensorMap *map, const void *base, const pa_attn_desc *d, int box_d,
+                               bool swizzle128, bool fp8) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)d->head_dim, (cuuint64_t)d->num_kv_heads, (cuuint64_t)d->block_size,
@@ -182,7 +220,7 @@ bool encode_cache_map(CUtensorMap *map, const void *base, const pa_attn_desc *d,
 // shared memory as [blocks][64 tokens][128 B] with the 128-byte swizzle -- the
 // K-major (and MN-major) operand layout the MMA reads -- in a single copy.
 // bf16: 64-dim blocks; fp8: 128-code blocks.
-bool encode_cache_map_blocks(CUtensorMap *map, const void *base, const pa_attn_desc *d, bool fp8 = false) {
+bool encode_cache_map_blocks_uncached(CUtensorMap *map, const void *base, const pa_attn_desc *d, bool fp8) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
     const int esz = fp8 ? 1 : 2, blk = 128 / esz;
@@ -197,6 +235,19 @@ bool encode_cache_map_blocks(CUtensorMap *map, const void *base, const pa_attn_d
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool encode_cache_map(CUtensorMap *map, const void *base, const pa_attn_desc *d, int box_d, bool swizzle128,
+                      bool fp8 = false) {
+    const MapKey key{base, d->num_pages, d->block_size, d->num_kv_heads, d->head_dim, box_d, 0, swizzle128, fp8};
+    return cached_map(map, key, [&](CUtensorMap *m) {
+        return encode_cache_map_uncached(m, base, d, box_d, swizzle128, fp8);
+    });
+}
+
+bool encode_cache_map_blocks(CUtensorMap *map, const void *base, const pa_attn_desc *d, bool fp8 = false) {
+    const MapKey key{base, d->num_pages, d->block_size, d->num_kv_heads, d->head_dim, 0, 1, true, fp8};
+    return cached_map(map, key, [&](CUtensorMap *m) { return encode_cache_map_blocks_uncached(m, base, d, fp8); });
 }
 
 void record_plan(int path, const Plan &pl, const pa_attn_desc *d, int ctas) {
