@@ -384,3 +384,44 @@ def test_verify_maximum_rows_sampled(oracle_mod):
             ref.append(o)
     assert_parity(torch.stack(got)[:, None, :], np.stack(ref)[:, None, :], rel_l2=REL_L2_VERIFY,
                   what="verify 32768 rows (sampled)")
+
+
+# -- the other benchmarked workloads at full size, in their benchmark launch ---------
+
+def test_decode_window2048_l32768_bs784_workload(oracle_mod):
+    """The 32K hybrid layer with a 2048-key window (the benchmark's window line)."""
+    prob = make_problem(1007, **dict(WORKLOADS["hybrid_step_l32768_bs784_x16"], num_layers=1))
+    out, status, plan = run_attention(prob, window=2048)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob, window=2048), what="window 2048 at 32K")
+
+
+def test_decode_g12_l32768_bs784_workload(oracle_mod):
+    prob = make_problem(1008, **dict(WORKLOADS["decode_g12_l32768_bs784"], num_layers=1))
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["num_splits"] > 1
+    assert_parity(out, oracle_out(oracle_mod, prob), what="G=12 at 32K")
+
+
+def test_prefill_q2048_l16384_bs832_workload_sampled(oracle_mod):
+    """The chunked-prefill step (2048 new rows over 14336 cached tokens) in its
+    benchmark launch: every output finite; sampled (row, head) outputs against
+    the oracle's attention of that row, including the first and last rows of
+    row blocks and of the step."""
+    prob = make_problem(1006, **WORKLOADS["prefill_q2048_l16384_bs832"])
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
+    assert torch.isfinite(out).all()
+    q, kc, vc = bits(prob.q[0]), bits(prob.k_cache[0]), bits(prob.v_cache[0])
+    g = torch.Generator().manual_seed(11)
+    rows = [0, 20, 21, 1023, 2047] + torch.randint(0, 2048, (6,), generator=g).tolist()
+    heads = [0, 5, 6, 23]
+    got, ref = [], []
+    for r in rows:
+        for h in heads:
+            o, _, _ = oracle_mod.attention_partial(q, kc, vc, prob.block_table.numpy(), prob.seq_lens.numpy(),
+                                                   prob.scale, r, h, 0, 1 << 40, q_len=prob.q_len)
+            got.append(out[r, h])
+            ref.append(o)
+    assert_parity(torch.stack(got)[:, None, :], np.stack(ref)[:, None, :], rel_l2=REL_L2_VERIFY,
+                  what="prefill 2048 rows (sampled)")
