@@ -64,9 +64,9 @@ typedef enum { PA_OUT_F32 = 0, PA_OUT_BF16 = 1 } pa_out_dtype;
  *   num_seqs          B, number of sequences (>= 0; 0 is a no-op)
  *   q_len             query rows per sequence: 1 for decode, > 1 for verify
  *   num_q_heads       Hq;  num_kv_heads Hkv; Hq % Hkv == 0, G = Hq / Hkv.
- *                     Decode is compiled for G in {1, 2, 4, 6, 12} at D = 256
- *                     and {1, 2, 4, 6, 8, 12} at D = 128 (PA_ERR_UNSUPPORTED
- *                     otherwise); verify takes any G with G * q_len <= 32768
+ *                     Decode is compiled for G in {1, 2, 3, 4, 5, 6, 8, 12, 16}
+ *                     at D = 256 and D = 128 (PA_ERR_UNSUPPORTED otherwise);
+ *                     verify takes any G with G * q_len <= 32768
  *   head_dim          D (128 or 256)
  *   block_size        BS, tokens per physical page (a multiple of 16: 16, 784, 832 ...)
  *   max_pages_per_seq columns of block_table

@@ -6,8 +6,10 @@
 namespace pa {
 
 bool decode_supported(int head_dim, int group) {
-    if (head_dim == 256) return group == 1 || group == 2 || group == 4 || group == 6 || group == 12;
-    if (head_dim == 128) return group == 1 || group == 2 || group == 4 || group == 6 || group == 8 || group == 12;
+    if (head_dim != 256 && head_dim != 128) return false;
+    switch (group) {
+        case 1: case 2: case 3: case 4: case 5: case 6: case 8: case 12: case 16: return true;
+    }
     return false;
 }
 

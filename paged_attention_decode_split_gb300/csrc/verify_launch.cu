@@ -40,8 +40,8 @@ cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const C
                           const CUtensorMap &tk64, const CUtensorMap &tv64, const VerifyParams &p, dim3 grid,
                           cudaStream_t stream) {
     (void)rows;  // each CTA runs one M = 128 block of rows
-    if (head_dim == 256) return launch_verify_tc<256, 4, 3, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 32);
-    if (head_dim == 128) return launch_verify_tc<128, 6, 6, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 33);
+    if (head_dim == 256) return launch_verify_tc<256, 4, 3, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 100);
+    if (head_dim == 128) return launch_verify_tc<128, 6, 6, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 101);
     return cudaErrorInvalidValue;
 }
 
@@ -49,8 +49,8 @@ cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const C
 // (D = 256: 2 K + 3 V slots of 32 KiB and 2 + 2 staging slots of 16 KiB).
 cudaError_t launch_verify_fp8(int head_dim, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tk64,
                               const CUtensorMap &tv64, const VerifyParams &p, dim3 grid, cudaStream_t stream) {
-    if (head_dim == 256) return launch_verify_tc<256, 2, 3, 2, 2>(tk, tv, tk64, tv64, p, grid, stream, 45);
-    if (head_dim == 128) return launch_verify_tc<128, 4, 4, 4, 2>(tk, tv, tk64, tv64, p, grid, stream, 46);
+    if (head_dim == 256) return launch_verify_tc<256, 2, 3, 2, 2>(tk, tv, tk64, tv64, p, grid, stream, 102);
+    if (head_dim == 128) return launch_verify_tc<128, 4, 4, 4, 2>(tk, tv, tk64, tv64, p, grid, stream, 103);
     return cudaErrorInvalidValue;
 }
 

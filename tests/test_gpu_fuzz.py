@@ -16,7 +16,7 @@ from tests.gpu_common import REL_L2_VERIFY, assert_parity, oracle_out, run_atten
 
 pytestmark = pytest.mark.gpu
 
-DECODE_GROUPS = {256: [1, 2, 4, 6, 12], 128: [1, 2, 4, 6, 8, 12]}
+DECODE_GROUPS = {256: [1, 2, 3, 4, 5, 6, 8, 12, 16], 128: [1, 2, 3, 4, 5, 6, 8, 12, 16]}
 N_CASES = 120
 
 
@@ -32,7 +32,7 @@ def draw_case(i):
     r = random.Random(7000 + i)
     d = r.choice([128, 256])
     g = r.choice(DECODE_GROUPS[d])
-    hkv = r.choice([1, 2, 4]) if g * 4 <= 48 else r.choice([1, 2])
+    hkv = r.choice([1, 2, 4]) if g * 4 <= 64 else r.choice([1, 2])
     bs = r.choice([16, 32, 48, 64, 784, 832])
     q_len = 1 if r.random() < 0.55 else r.choice([2, 3, 5, 8, 16, 23])
     b = r.randint(1, 4)

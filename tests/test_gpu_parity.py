@@ -66,7 +66,8 @@ def test_decode_forced_split_counts(oracle_mod, splits):
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"splits={splits}")
 
 
-@pytest.mark.parametrize("G,hkv", [(1, 4), (2, 4), (4, 2), (6, 4), (12, 4), (12, 1)])
+@pytest.mark.parametrize("G,hkv", [(1, 4), (2, 4), (3, 4), (4, 2), (5, 4), (6, 4), (8, 4), (12, 4), (12, 1), (16, 4),
+                                   (16, 1)])
 def test_decode_group_sizes_d256(oracle_mod, G, hkv):
     prob = hybrid(31 + G, [700, 1500], 16, num_q_heads=G * hkv, num_kv_heads=hkv)
     out, status, _ = run_attention(prob)
@@ -74,7 +75,7 @@ def test_decode_group_sizes_d256(oracle_mod, G, hkv):
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"G={G}")
 
 
-@pytest.mark.parametrize("G", [1, 2, 4, 6, 8, 12])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 8, 12, 16])
 def test_decode_dense_control_d128(oracle_mod, G):
     prob = make_problem(41 + G, num_seqs=3, seq_lens=[1, 100, 2049], num_q_heads=8 * G, num_kv_heads=8,
                         head_dim=128, block_size=16, scale=1 / math.sqrt(128), poison_unused=True)
