@@ -7,11 +7,11 @@
 
 namespace pa {
 
-template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8>
+template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8, bool LP>
 cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, dim3 grid,
                             cudaStream_t stream, int slot) {
     using C = DecodeCfg<D, G, TS, NST, SPS, HG, F8 ? 1 : 2>;
-    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS, HG, WIN, F8>;
+    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS, HG, WIN, F8, LP>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the kernel's set-up overlaps the previous
@@ -31,16 +31,24 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
 }
 
 // Per (head_dim, group): token halves (TS), chunk streams (NST), stages per
-// stream (SPS), head groups (HG).  D = 256: groups of 4 and 6 heads run 4
-// streams x 3 stages x 16 KiB with each chunk's tokens split over 2 warps (9
-// warps, 168 registers); groups of 1 and 2 run 6 streams x 2 stages, one
-// warp per chunk; 12 heads split into 3 head groups of 4, each warp taking a
-// whole chunk (4 streams x 3 stages, 13 warps: measured 54.6 us against 60 us
-// for 2 groups of 6 with split tokens at 32K).  D = 128: 12 streams x 2 x 8
-// KiB for small groups, else the tokens split over 2 warps.  Groups of 3 and 5
-// heads run like 4 and 6; 8 and 16 heads split into head groups of 4 (D = 256)
-// or 8 (D = 128, 16 heads).  An fp8 cache halves the stage, and
-// each stream owns twice the stages: the same bytes in flight per SM.
+// stream (SPS), head groups (HG), a producer lane per stream (LP).
+//  * D = 256: groups of 3 to 6 heads run 4 streams x 3 stages x 16 KiB with
+//    each chunk's tokens split over 2 warps (9 warps, 168 registers); groups
+//    of 1 and 2 run 6 streams x 2 stages, one warp per chunk; 8, 12 and 16
+//    heads split into head groups of 4, each warp taking a whole chunk (12
+//    heads: 13 warps, measured 54.6 us against 60 us for 2 groups of 6 with
+//    split tokens at 32K).  One producer lane serves all streams.
+//  * D = 128 (8 KiB stages): every stream has its own producer lane.  Up to 4
+//    heads: 12 streams x 2 stages (1 and 2 heads) or 6 x 4 with split tokens;
+//    5 and 6 heads: 6 x 4 with split tokens; 8, 12 and 16 heads: head groups
+//    of 4 (8 x 3, 6 x 4 and 4 x 6 streams x stages).  Measured at 32K over
+//    8 KV heads against one producer lane and the earlier layouts: 4 heads 41.9 -> 28.3 us, 8 heads 48.6 -> 46.3 us, 12 heads
+//    68.9 -> 65.3 us.
+//  * An fp8 cache halves the stage and each stream owns twice the stages:
+//    the same bytes in flight per SM.  At D = 256, groups of up to 4 heads
+//    take a producer lane per stream (1 head: 21.3 -> 17.5 us at 32K); wider
+//    groups, whose widening arithmetic bounds them, measured 0-1 % faster
+//    with one lane.
 template <bool WIN, bool F8>
 cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                               const DecodeParams &p, dim3 grid, cudaStream_t stream) {
@@ -49,54 +57,54 @@ cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, co
     if constexpr (F8) {
         if (head_dim == 256) {
             switch (group) {
-                case 1: return launch_decode_t<256, 1, 1, 6, 4, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 0);
-                case 2: return launch_decode_t<256, 2, 1, 6, 4, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 1);
-                case 4: return launch_decode_t<256, 4, 2, 4, 6, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 2);
-                case 6: return launch_decode_t<256, 6, 2, 4, 6, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 3);
-                case 12: return launch_decode_t<256, 12, 1, 4, 6, 3, WIN, F8>(tk, tv, p, grid, stream, slot0 + 9);
-                case 3: return launch_decode_t<256, 3, 2, 4, 6, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 11);
-                case 5: return launch_decode_t<256, 5, 2, 4, 6, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 12);
-                case 8: return launch_decode_t<256, 8, 1, 4, 6, 2, WIN, F8>(tk, tv, p, grid, stream, slot0 + 13);
-                case 16: return launch_decode_t<256, 16, 1, 3, 8, 4, WIN, F8>(tk, tv, p, grid, stream, slot0 + 14);
+                case 1: return launch_decode_t<256, 1, 1, 6, 4, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 0);
+                case 2: return launch_decode_t<256, 2, 1, 6, 4, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 1);
+                case 4: return launch_decode_t<256, 4, 2, 4, 6, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 2);
+                case 6: return launch_decode_t<256, 6, 2, 4, 6, 1, WIN, F8, false>(tk, tv, p, grid, stream, slot0 + 3);
+                case 12: return launch_decode_t<256, 12, 1, 4, 6, 3, WIN, F8, false>(tk, tv, p, grid, stream, slot0 + 9);
+                case 3: return launch_decode_t<256, 3, 2, 4, 6, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 11);
+                case 5: return launch_decode_t<256, 5, 2, 4, 6, 1, WIN, F8, false>(tk, tv, p, grid, stream, slot0 + 12);
+                case 8: return launch_decode_t<256, 8, 1, 4, 6, 2, WIN, F8, false>(tk, tv, p, grid, stream, slot0 + 13);
+                case 16: return launch_decode_t<256, 16, 1, 3, 8, 4, WIN, F8, false>(tk, tv, p, grid, stream, slot0 + 14);
             }
         } else if (head_dim == 128) {
             switch (group) {
-                case 1: return launch_decode_t<128, 1, 1, 12, 4, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 4);
-                case 2: return launch_decode_t<128, 2, 1, 12, 4, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 5);
-                case 4: return launch_decode_t<128, 4, 2, 6, 8, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 6);
-                case 6: return launch_decode_t<128, 6, 2, 4, 12, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 7);
-                case 8: return launch_decode_t<128, 8, 2, 4, 12, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 8);
-                case 12: return launch_decode_t<128, 12, 2, 2, 24, 2, WIN, F8>(tk, tv, p, grid, stream, slot0 + 10);
-                case 3: return launch_decode_t<128, 3, 2, 6, 8, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 15);
-                case 5: return launch_decode_t<128, 5, 2, 4, 12, 1, WIN, F8>(tk, tv, p, grid, stream, slot0 + 16);
-                case 16: return launch_decode_t<128, 16, 1, 4, 12, 2, WIN, F8>(tk, tv, p, grid, stream, slot0 + 17);
+                case 1: return launch_decode_t<128, 1, 1, 12, 4, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 4);
+                case 2: return launch_decode_t<128, 2, 1, 12, 4, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 5);
+                case 4: return launch_decode_t<128, 4, 2, 6, 8, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 6);
+                case 6: return launch_decode_t<128, 6, 2, 6, 8, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 7);
+                case 8: return launch_decode_t<128, 8, 1, 8, 6, 2, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 8);
+                case 12: return launch_decode_t<128, 12, 1, 6, 8, 3, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 10);
+                case 3: return launch_decode_t<128, 3, 2, 6, 8, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 15);
+                case 5: return launch_decode_t<128, 5, 2, 6, 8, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 16);
+                case 16: return launch_decode_t<128, 16, 1, 4, 12, 4, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 17);
             }
         }
         return cudaErrorInvalidValue;
     }
     if (head_dim == 256) {
         switch (group) {
-            case 1: return launch_decode_t<256, 1, 1, 6, 2, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 0);
-            case 2: return launch_decode_t<256, 2, 1, 6, 2, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 1);
-            case 4: return launch_decode_t<256, 4, 2, 4, 3, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 2);
-            case 6: return launch_decode_t<256, 6, 2, 4, 3, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 3);
-            case 12: return launch_decode_t<256, 12, 1, 4, 3, 3, WIN, false>(tk, tv, p, grid, stream, slot0 + 9);
-            case 3: return launch_decode_t<256, 3, 2, 4, 3, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 11);
-            case 5: return launch_decode_t<256, 5, 2, 4, 3, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 12);
-            case 8: return launch_decode_t<256, 8, 1, 4, 3, 2, WIN, false>(tk, tv, p, grid, stream, slot0 + 13);
-            case 16: return launch_decode_t<256, 16, 1, 3, 4, 4, WIN, false>(tk, tv, p, grid, stream, slot0 + 14);
+            case 1: return launch_decode_t<256, 1, 1, 6, 2, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 0);
+            case 2: return launch_decode_t<256, 2, 1, 6, 2, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 1);
+            case 4: return launch_decode_t<256, 4, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 2);
+            case 6: return launch_decode_t<256, 6, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 3);
+            case 12: return launch_decode_t<256, 12, 1, 4, 3, 3, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 9);
+            case 3: return launch_decode_t<256, 3, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 11);
+            case 5: return launch_decode_t<256, 5, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 12);
+            case 8: return launch_decode_t<256, 8, 1, 4, 3, 2, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 13);
+            case 16: return launch_decode_t<256, 16, 1, 3, 4, 4, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 14);
         }
     } else if (head_dim == 128) {
         switch (group) {
-            case 1: return launch_decode_t<128, 1, 1, 12, 2, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 4);
-            case 2: return launch_decode_t<128, 2, 1, 12, 2, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 5);
-            case 4: return launch_decode_t<128, 4, 2, 6, 4, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 6);
-            case 6: return launch_decode_t<128, 6, 2, 4, 6, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 7);
-            case 8: return launch_decode_t<128, 8, 2, 4, 6, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 8);
-            case 12: return launch_decode_t<128, 12, 2, 2, 12, 2, WIN, false>(tk, tv, p, grid, stream, slot0 + 10);
-            case 3: return launch_decode_t<128, 3, 2, 6, 4, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 15);
-            case 5: return launch_decode_t<128, 5, 2, 4, 6, 1, WIN, false>(tk, tv, p, grid, stream, slot0 + 16);
-            case 16: return launch_decode_t<128, 16, 1, 4, 6, 2, WIN, false>(tk, tv, p, grid, stream, slot0 + 17);
+            case 1: return launch_decode_t<128, 1, 1, 12, 2, 1, WIN, false, true>(tk, tv, p, grid, stream, slot0 + 4);
+            case 2: return launch_decode_t<128, 2, 1, 12, 2, 1, WIN, false, true>(tk, tv, p, grid, stream, slot0 + 5);
+            case 4: return launch_decode_t<128, 4, 2, 6, 4, 1, WIN, false, true>(tk, tv, p, grid, stream, slot0 + 6);
+            case 6: return launch_decode_t<128, 6, 2, 6, 4, 1, WIN, false, true>(tk, tv, p, grid, stream, slot0 + 7);
+            case 8: return launch_decode_t<128, 8, 1, 8, 3, 2, WIN, false, true>(tk, tv, p, grid, stream, slot0 + 8);
+            case 12: return launch_decode_t<128, 12, 1, 6, 4, 3, WIN, false, true>(tk, tv, p, grid, stream, slot0 + 10);
+            case 3: return launch_decode_t<128, 3, 2, 6, 4, 1, WIN, false, true>(tk, tv, p, grid, stream, slot0 + 15);
+            case 5: return launch_decode_t<128, 5, 2, 6, 4, 1, WIN, false, true>(tk, tv, p, grid, stream, slot0 + 16);
+            case 16: return launch_decode_t<128, 16, 1, 4, 6, 4, WIN, false, true>(tk, tv, p, grid, stream, slot0 + 17);
         }
     }
     return cudaErrorInvalidValue;

@@ -18,9 +18,9 @@
 //    a page, and the split's block-table entries are staged in shared memory
 //    once (the page-contiguous walk of Sec.7 reads the table once per page).  Only the last chunk of a sequence
 //    can be partial; its rows past the end are masked (scores) and skipped (PV).
-//  * One producer lane issues the copies into NS stages; NST chunk streams
-//    take chunks round-robin, each owning SPS stages that are refilled as
-//    soon as the stream frees one.  A chunk is shared by TS warps that split
+//  * NST chunk streams take chunks round-robin, each owning SPS of the NS
+//    stages; one lane of the producer warp (or one lane per stream) issues
+//    the copies and refills a stage as soon as its stream frees it.  A chunk is shared by TS warps that split
 //    its 16 tokens (8 each when TS = 2); every warp keeps its own online
 //    softmax state over the tokens it sees, and the CTA merges the states.
 //  * Every warp handles all G query heads of the group, so each K/V element
@@ -169,8 +169,9 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
 // attention kernel carries none of its bookkeeping).  F8: the cache holds fp8
 // e4m3 codes with one scale per KV head for K and for V; the K scale is folded
 // into q and the V scale into the merge weights, so the inner loops only
-// widen codes instead of bf16 values.
-template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8 = false>
+// widen codes instead of bf16 values.  LP: one producer lane per chunk stream
+// (else one lane serves all streams).
+template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8 = false, bool LP = false>
 __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
     pa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecodeParams p) {
@@ -260,17 +261,26 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
     float m_run[GW], l_run[GW];
     float2 acc[GW][E / 2];
     if (warp == NWC) {
-        // ---------------- producer: one lane issues every copy ----------------
-        // Streams are refilled independently: the lane probes each stream's
-        // next stage without blocking and issues as soon as that stage is
-        // free, so a slow stream never holds back the others.  Within a
-        // stream, chunks and stage phases are issued strictly in order.
-        if (lane == 0) {
+        // ---------------- producer: PL lanes issue the copies ----------------
+        // Lane c0 < PL serves streams c0, c0 + PL, ... (PL = NST: a lane per
+        // stream; PL = 1: one lane for all).  A lane polls its streams' next
+        // stages without blocking and issues as soon as one is free, so a
+        // slow stream never holds back the others; within a stream, chunks
+        // and stage phases are issued strictly in order.  One issuing lane
+        // caps a CTA at roughly one stage per 0.3 us, which 8 KiB stages feel
+        // (D = 128, fp8 caches); with 16 KiB stages and wide groups the one
+        // lane, which staggers the streams, measured faster.
+        constexpr int PL = LP ? NST : 1, SPL = NST / PL;
+        static_assert(PL <= 32, "one producer warp");
+        if (lane < PL) {
+            const unsigned mask = PL == 32 ? 0xffffffffu : (1u << PL) - 1u;
+            auto any = [&](bool v) {  // over the producer lanes
+                if constexpr (PL == 1)
+                    return v;
+                else
+                    return __any_sync(mask, v);
+            };
             const uint64_t policy = l2_policy_evict_first();
-            int next[NST];
-#pragma unroll
-            for (int c = 0; c < NST; ++c) next[c] = 0;
-            int remaining = n_my;
             auto issue = [&](int c, int k) {  // chunk c + k * NST into stream c's stage k % SPS
                 const int i = c + k * NST, s = c * SPS + k % SPS;
                 const int t0 = (c_begin + i) * kChunk;
@@ -286,50 +296,65 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
                 tma_load_4d(st, &tm_k, &full[s], 0, kvh, off, page, policy);
                 tma_load_4d(st + C::CHUNK_BYTES, &tm_v, &full[s], 0, kvh, off, page, policy);
             };
+            int next[SPL];
+            int remaining = PL == 1 ? n_my : 0;
+#pragma unroll
+            for (int j = 0; j < SPL; ++j) {
+                next[j] = 0;
+                if constexpr (PL > 1) remaining += max(0, (n_my - lane - j * PL + NST - 1) / NST);  // chunks c, c + NST, ...
+            }
             if (p.early_kv) {
                 // First use of every stage: the chunks i < n_pre (those that
                 // end before the new row, token L - 1) go out before the
-                // dependency wait; chunk i is stream i % NST's (i / NST)-th.
+                // dependency wait; chunk i is stream i % NST's (i / NST)-th,
+                // and n_pre <= NS, so none of them waits for a free stage.
                 const int n_pre = max(0, min(min(NS, n_my), (L - 1) / kChunk - c_begin));
 #pragma unroll 1
-                for (int i = 0; i < n_pre; ++i) issue(i % NST, i / NST);
+                for (int i = lane; i < n_pre; i += PL) issue(i % NST, i / NST);
 #pragma unroll
-                for (int c = 0; c < NST; ++c) next[c] = c < n_pre ? (n_pre - c + NST - 1) / NST : 0;
-                remaining -= n_pre;
+                for (int j = 0; j < SPL; ++j) {
+                    const int c = lane + j * PL;
+                    next[j] = max(0, (n_pre - c + NST - 1) / NST);
+                    remaining -= next[j];
+                }
                 pdl_wait_primary();
             }
             uint32_t idle = 0;
-            while (remaining > 0) {
+            bool gave_up = false;
+            while (any(remaining > 0)) {
                 bool progress = false;
 #pragma unroll
-                for (int c = 0; c < NST; ++c) {
-                    const int k = next[c], i = c + k * NST;
+                for (int j = 0; j < SPL; ++j) {
+                    const int c = lane + j * PL, k = next[j], i = c + k * NST;
                     if (i >= n_my) continue;
                     const int s = c * SPS + k % SPS, ph = k / SPS;
                     if (ph > 0 && !mbar_test_wait(&empty[s], (ph - 1) & 1)) continue;
                     issue(c, k);
-                    next[c] = k + 1;
+                    next[j] = k + 1;
                     --remaining;
                     progress = true;
                 }
-                if (progress) {
+                if (any(progress)) {
                     idle = 0;
-                } else if (++idle > kWaitPollLimit || flags[0]) {
-                    flags[0] = 1;
+                } else if (++idle > kWaitPollLimit || any(flags[0] != 0)) {
+                    gave_up = true;
                     break;
                 }
             }
-            if (flags[0]) {
+            if (gave_up || flags[0]) {
                 // Giving up: let the copies already in flight land before the
                 // CTA ends (each stream's last SPS chunks, one per stage).
+                if (lane == 0) flags[0] = 1;
 #pragma unroll
-                for (int c = 0; c < NST; ++c)
-                    for (int k = max(0, next[c] - SPS); k < next[c]; ++k) {
+                for (int j = 0; j < SPL; ++j) {
+                    const int c = lane + j * PL;
+                    for (int k = max(0, next[j] - SPS); k < next[j]; ++k) {
                         uint64_t *bar = &full[c * SPS + k % SPS];
                         for (uint32_t n = 0; n < kWaitPollLimit && !mbar_try_wait(bar, (k / SPS) & 1); ++n) {
                         }
                     }
-                set_status(p.status, PA_DEV_TIMEOUT);
+                }
+                if (lane == 0) set_status(p.status, PA_DEV_TIMEOUT);
             }
         }
     } else {

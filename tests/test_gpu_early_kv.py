@@ -47,10 +47,17 @@ def call(prob, tensors, flags, num_splits=0):
     return out, status
 
 
+# The dense shape (8 KV heads of 128 dims) runs the kernels whose chunk
+# streams each have their own producer lane; the hybrid shape one lane for all.
+DENSE = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, scale=128 ** -0.5)
+SHAPES = {"hybrid": {}, "dense": DENSE}
+
+
+@pytest.mark.parametrize("shape", ["hybrid", "dense"])
 @pytest.mark.parametrize("splits", [0, 1, 5])
 @pytest.mark.parametrize("bs", [16, 784])
-def test_decode_early_equals_default_bitwise(bs, splits):
-    prob = hybrid(301 + bs, [1, 15, 16, 17, 785, 5000, 0], bs, poison_unused=True)
+def test_decode_early_equals_default_bitwise(bs, splits, shape):
+    prob = hybrid(301 + bs, [1, 15, 16, 17, 785, 5000, 0], bs, poison_unused=True, **SHAPES[shape])
     t = to_dev(prob)
     ref, st0 = call(prob, t, 0, splits)
     got, st1 = call(prob, t, EARLY, splits)
@@ -86,9 +93,11 @@ def chained(prob, seed, flags):
     return out.cpu(), status.item(), prob
 
 
-@pytest.mark.parametrize("lens,bs", [([32768], 784), ([17, 4000, 1], 16), ([832, 833], 832)])
-def test_decode_early_chain_reads_new_row(oracle_mod, lens, bs):
-    prob = hybrid(321, lens, bs)
+@pytest.mark.parametrize("lens,bs,shape", [([32768], 784, "hybrid"), ([17, 4000, 1], 16, "hybrid"),
+                                           ([832, 833], 832, "hybrid"), ([17, 4000, 1], 16, "dense"),
+                                           ([32768], 16, "dense")])
+def test_decode_early_chain_reads_new_row(oracle_mod, lens, bs, shape):
+    prob = hybrid(321, lens, bs, **SHAPES[shape])
     out, status, prob = chained(prob, 7, EARLY)
     assert status == 0
     assert_parity(out, oracle_out(oracle_mod, prob), what="early decode after reshape_and_cache")

@@ -161,8 +161,9 @@ def test_decode_fp8_bf16_output(oracle_mod):
     assert err.max() <= 2e-3 + 2 * 2.0 ** -8 * np.abs(ref).max()
 
 
-def test_decode_fp8_early_kv_bitwise():
-    prob = hybrid(561, [1, 15, 17, 785, 5000, 0], 784, poison_unused=True)
+@pytest.mark.parametrize("hq", [24, 16])  # 6 heads per KV head: one producer lane; 4: a lane per stream
+def test_decode_fp8_early_kv_bitwise(hq):
+    prob = hybrid(561, [1, 15, 17, 785, 5000, 0], 784, poison_unused=True, num_q_heads=hq)
     outs = []
     for flags in (0, pa.PA_FLAG_EARLY_KV_READ):
         out, status, _ = run_attention(prob, num_splits=5, flags=flags)
