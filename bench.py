@@ -490,7 +490,8 @@ def _layers_beyond_l2(bytes_per_layer, minimum, l2_bytes=256 << 20):
 
 SECONDARY = ("decode_l512_bs16", "context_sweep", "batch32_uniform_bs784", "verify_b8_q16_l8192_bs832",
              "prefill_q2048_l16384_bs832", "decode_window2048_l32768_bs784", "decode_g12_l32768_bs784",
-             "verify_g12_b32_q5_l2048_bs784", "decode_fp8_l32768_bs784", "verify_fp8_b8_q16_l8192_bs832")
+             "verify_g12_b32_q5_l2048_bs784", "decode_fp8_l32768_bs784", "verify_fp8_b8_q16_l8192_bs832",
+             "decode_dense_l32768_bs16")
 
 
 def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
@@ -513,6 +514,8 @@ def secondary_workloads(args, dev, stream, peak, names=SECONDARY):
         _window(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "decode_g12_l32768_bs784" in names:
         _wide_group(pa, dev, stream, peak, res, WORKLOADS, make_problem)
+    if "decode_dense_l32768_bs16" in names:
+        _dense(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "decode_fp8_l32768_bs784" in names:
         _fp8_decode(pa, dev, stream, peak, res, WORKLOADS, make_problem)
     if "verify_fp8_b8_q16_l8192_bs832" in names:
@@ -576,6 +579,18 @@ def _wide_group(pa, dev, stream, peak, res, WORKLOADS, make_problem):
     kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER
     res["decode_g12_l32768_bs784"] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
                                       "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak, "plan": pa.last_plan()}
+    del prob, calls
+
+
+def _dense(pa, dev, stream, peak, res, WORKLOADS, make_problem):
+    # The dense control at 32K: 32 query heads on 8 KV heads of 128 dims,
+    # 16-token pages; 128 MiB of K+V per layer, 16 layers (2 GiB).
+    prob = make_problem(1011, **WORKLOADS["decode_dense_l32768_bs16"], device=dev)
+    calls = _attention_calls(pa, prob, dev)
+    us = _time_graph(calls, stream, 50) * 1e3 / len(calls)
+    kv = prob.context_tokens() * KV_BYTES_PER_TOKEN_LAYER
+    res["decode_dense_l32768_bs16"] = {"us_per_call": us, "GBps": kv / (us * 1e-6) / 1e9,
+                                       "frac_of_peak": kv / (us * 1e-6) / 1e9 / peak, "plan": pa.last_plan()}
     del prob, calls
 
 

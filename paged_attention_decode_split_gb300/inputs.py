@@ -200,6 +200,11 @@ WORKLOADS = {
     "decode_g12_l32768_bs784": dict(num_seqs=1, seq_lens=32768, num_q_heads=48, num_kv_heads=4,
                                     head_dim=256, block_size=784, scale=1.0 / 16, q_len=1,
                                     num_layers=16),
+    # the dense control at full depth: 32 query heads on 8 KV heads, head_dim
+    # 128, 16-token pages (the same 4096 B of K+V per token as the hybrid)
+    "decode_dense_l32768_bs16": dict(num_seqs=1, seq_lens=32768, num_q_heads=32, num_kv_heads=8,
+                                     head_dim=128, block_size=16, scale=1.0 / math.sqrt(128), q_len=1,
+                                     num_layers=16),
     # speculative verify with 12 query heads per KV head: 5 positions x 12 heads
     # = 60 rows per (sequence, KV head), 32 sequences of 2048 positions
     "verify_g12_b32_q5_l2048_bs784": dict(num_seqs=32, seq_lens=2048, num_q_heads=48, num_kv_heads=4,

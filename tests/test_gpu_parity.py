@@ -404,6 +404,15 @@ def test_decode_g12_l32768_bs784_workload(oracle_mod):
     assert_parity(out, oracle_out(oracle_mod, prob), what="G=12 at 32K")
 
 
+def test_decode_dense_l32768_bs16_workload(oracle_mod):
+    """The dense control at 32K (8 KV heads of 128 dims over 2048 pages of 16
+    tokens), in its benchmark launch: a producer lane per chunk stream."""
+    prob = make_problem(1011, **dict(WORKLOADS["decode_dense_l32768_bs16"], num_layers=1))
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["num_splits"] > 1
+    assert_parity(out, oracle_out(oracle_mod, prob), what="dense 32/8/128 at 32K")
+
+
 def test_prefill_q2048_l16384_bs832_workload_sampled(oracle_mod):
     """The chunked-prefill step (2048 new rows over 14336 cached tokens) in its
     benchmark launch: every output finite; sampled (row, head) outputs against
