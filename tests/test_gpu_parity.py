@@ -55,7 +55,7 @@ def test_decode_ragged_tails_nan_poisoned(oracle_mod, bs):
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"tails bs={bs}")
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64, 100, 313])  # > 64: the reduce loads its splits in several rounds
 def test_decode_forced_split_counts(oracle_mod, splits):
     prob = hybrid(21, [5000, 333, 1], 784, poison_unused=True)
     out, status, plan = run_attention(prob, num_splits=splits)
@@ -64,6 +64,16 @@ def test_decode_forced_split_counts(oracle_mod, splits):
     per_split = math.ceil(n_chunks / min(splits, n_chunks))
     assert plan["num_splits"] == math.ceil(n_chunks / per_split)  # no empty trailing split
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"splits={splits}")
+
+
+@pytest.mark.parametrize("splits", [100, 250])
+def test_decode_dense_many_splits(oracle_mod, splits):
+    """The dense shape (head_dim 128) merged from more than 64 splits."""
+    prob = make_problem(23, num_seqs=2, seq_lens=[4000, 90], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, scale=1 / math.sqrt(128), poison_unused=True)
+    out, status, plan = run_attention(prob, num_splits=splits)
+    assert status == 0 and plan["num_splits"] > 64
+    assert_parity(out, oracle_out(oracle_mod, prob), what=f"dense splits={splits}")
 
 
 @pytest.mark.parametrize("G,hkv", [(1, 4), (2, 4), (3, 4), (4, 2), (5, 4), (6, 4), (8, 4), (12, 4), (12, 1), (16, 4),
@@ -103,9 +113,11 @@ def test_decode_empty_sequences_give_zero(oracle_mod):
     assert_parity(out, oracle_out(oracle_mod, prob), what="empty")
 
 
-def test_decode_bf16_output(oracle_mod):
+@pytest.mark.parametrize("splits", [0, 4, 1])  # the large-split merge, the few-split merge, no merge
+def test_decode_bf16_output(oracle_mod, splits):
     prob = hybrid(61, [3000, 17], 832)
-    out, status, _ = run_attention(prob, out_dtype=pa.PA_OUT_BF16)
+    out, status, plan = run_attention(prob, out_dtype=pa.PA_OUT_BF16, num_splits=splits)
+    assert splits == 0 or plan["num_splits"] == splits
     ref = oracle_out(oracle_mod, prob)
     ref_bf16 = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
     err = np.abs(out.double().numpy() - ref_bf16)
@@ -158,6 +170,34 @@ def test_decode_bad_page_sets_status_and_zeroes(oracle_mod, splits):
     assert status & pa.PA_DEV_BAD_PAGE
     assert torch.all(out[1] == 0)
     assert_parity(out[:1], oracle_out(oracle_mod, prob, rows=[0]), what="good row next to a bad page")
+
+
+def test_workspace_reused_across_descriptions(oracle_mod):
+    """One workspace, sized for the largest call, serves calls of other batch
+    sizes, split counts and shapes in turn without being cleared: every split
+    writes its record, so nothing of an earlier call is read."""
+    probs = [hybrid(181, [4000, 2500, 300], 784), hybrid(182, [5000], 784),
+             make_problem(183, num_seqs=2, seq_lens=[3000, 40], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                          block_size=16, scale=1 / math.sqrt(128)),
+             hybrid(184, [700, 20], 832, q_len=8)]
+    splits = [0, 37, 0, 3]
+    from tests.gpu_common import desc_for
+    need = max(pa.workspace_bytes(desc_for(p, num_splits=k)) for p, k in zip(probs, splits))
+    ws = torch.full((need,), 0xff, dtype=torch.uint8, device="cuda")  # NaN in every fp32 slot
+    for prob, k in zip(probs, splits):
+        if prob.q_len > 1:
+            write_new_rows(prob, 17)
+        q, kc, vc, bt, sl = to_dev(prob)
+        desc = desc_for(prob, num_splits=k)
+        out = torch.empty((prob.num_seqs * prob.q_len, prob.num_q_heads, prob.head_dim), dtype=torch.float32,
+                          device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fn = pa.paged_attention_decode if prob.q_len == 1 else pa.paged_attention_verify
+        fn(q, kc, vc, bt, sl, desc, out, ws, status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        assert_parity(out.cpu(), oracle_out(oracle_mod, prob),
+                      rel_l2=REL_L2_VERIFY if prob.q_len > 1 else REL_L2_DECODE, what=f"reused workspace q_len={prob.q_len}")
 
 
 def test_decode_cuda_graph_replay_matches_eager():
@@ -232,7 +272,7 @@ def test_verify_small(oracle_mod, q_len, lens, bs):
     assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what=f"verify q_len={q_len}")
 
 
-@pytest.mark.parametrize("splits", [2, 5, 13])
+@pytest.mark.parametrize("splits", [2, 5, 13, 40])
 def test_verify_forced_splits_tiles_cross_split_ends(oracle_mod, splits):
     """Split sizes that are not whole 64-token tiles: a tile reaches into the
     next split's tokens, which must be masked out (and the ends zero-filled)."""
