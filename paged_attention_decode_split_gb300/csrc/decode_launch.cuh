@@ -3,17 +3,35 @@
 // units (compiled in parallel).
 #pragma once
 
+#include <atomic>
+
 #include "pa_internal.h"
 
 namespace pa {
 
-template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8, bool LP>
+template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8, bool LP, bool RB = false>
 cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, dim3 grid,
                             cudaStream_t stream, int slot) {
-    using C = DecodeCfg<D, G, TS, NST, SPS, HG, F8 ? 1 : 2>;
-    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS, HG, WIN, F8, LP>;
+    using C = DecodeCfg<D, G, TS, NST, SPS, HG, F8 ? 1 : 2, RB ? 4 : 1>;
+    auto kern = pa_decode_split_kernel<D, G, TS, NST, SPS, HG, WIN, F8, LP, RB>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
+    if constexpr (RB) {
+        // The warpgroups' register budgets add up to REG_LAUNCH per thread;
+        // a kernel launched with fewer registers would wait forever in
+        // setmaxnreg.inc, so it is not launched.
+        static std::atomic<int> launch_regs{0};  // per instantiation; the same on every sm_103a device
+        int regs = launch_regs.load(std::memory_order_relaxed);
+        if (regs == 0) {
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kern));
+            if (e != cudaSuccess) return e;
+            regs = fa.numRegs;
+            launch_regs.store(regs, std::memory_order_relaxed);
+        }
+        if (regs * C::THREADS < 128 * C::REG_PRODUCER + C::NWC * 32 * C::REG_CONSUMER)
+            return cudaErrorInvalidConfiguration;
+    }
     // Programmatic dependent launch: the kernel's set-up overlaps the previous
     // kernel in the stream (e.g. reshape_and_cache); it waits for that kernel
     // before touching global memory.
@@ -33,7 +51,10 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
 // Per (head_dim, group): token halves (TS), chunk streams (NST), stages per
 // stream (SPS), head groups (HG), a producer lane per stream (LP).
 //  * D = 256: groups of 3 to 6 heads run 4 streams x 3 stages x 16 KiB with
-//    each chunk's tokens split over 2 warps (9 warps, 168 registers); groups
+//    each chunk's tokens split over 2 warps (9 warps, 168 registers; for 6
+//    heads the producer sits in a warpgroup of its own that hands its
+//    registers to the 8 consumers, 232 each: no spills, and the 16-layer
+//    step at 32K measured 0.528 ms against 0.537 ms); groups
 //    of 1 and 2 run 6 streams x 2 stages, one warp per chunk; 8, 12 and 16
 //    heads split into head groups of 4, each warp taking a whole chunk (12
 //    heads: 13 warps, measured 54.6 us against 60 us for 2 groups of 6 with
@@ -87,7 +108,7 @@ cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, co
             case 1: return launch_decode_t<256, 1, 1, 6, 2, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 0);
             case 2: return launch_decode_t<256, 2, 1, 6, 2, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 1);
             case 4: return launch_decode_t<256, 4, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 2);
-            case 6: return launch_decode_t<256, 6, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 3);
+            case 6: return launch_decode_t<256, 6, 2, 4, 3, 1, WIN, false, false, true>(tk, tv, p, grid, stream, slot0 + 3);
             case 12: return launch_decode_t<256, 12, 1, 4, 3, 3, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 9);
             case 3: return launch_decode_t<256, 3, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 11);
             case 5: return launch_decode_t<256, 5, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 12);

@@ -76,13 +76,15 @@ struct DecodeParams {
 // for groups too wide for one warp's registers).  NST: chunk streams
 // (consumer warps = TS * HG * NST).  SPS: stages owned by each stream (NS =
 // NST * SPS in all).  KVB: bytes per cached element (2 bf16, 1 fp8 e4m3).
+// PW: warps beside the consumers (1: the producer warp; 4: a producer
+// warpgroup whose registers go to the consumers, see RB below).
 //
 // Stage ownership matters for correctness: an mbarrier wait tests the parity
 // of a phase, so a waiter must never run two phases ahead of the barrier.
 // Each stream therefore owns SPS stages and cycles through them in order; it
 // has consumed every earlier phase of a stage before it waits on the next,
 // and the producer waits on every phase of a stage's empty barrier in order.
-template <int D, int G, int TS, int NST, int SPS, int HG, int KVB = 2>
+template <int D, int G, int TS, int NST, int SPS, int HG, int KVB = 2, int PW = 1>
 struct DecodeCfg {
     static constexpr int NS = NST * SPS;
     static constexpr int E = D / 32;
@@ -103,7 +105,14 @@ struct DecodeCfg {
     static constexpr int OFF_FLAGS = OFF_BAR + 2 * NS * 8;
     static constexpr int OFF_PT = OFF_FLAGS + 16;
     static constexpr int SMEM_BYTES = OFF_PT + kPageTab * 4 + 1024;  // + slack to align the base to 1 KiB
-    static constexpr int THREADS = (NWC + 1) * 32;
+    static constexpr int THREADS = (NWC + PW) * 32;
+    // register budgets with a producer warpgroup (PW = 4): the launch gives
+    // every thread REG_LAUNCH registers; the producer warpgroup keeps
+    // REG_PRODUCER and the consumer warpgroups take the rest
+    static constexpr int REG_LAUNCH = (65536 / THREADS) & ~7;
+    static constexpr int REG_PRODUCER = 40;
+    static constexpr int REG_CONSUMER = ((REG_LAUNCH * THREADS - 128 * REG_PRODUCER) / (NWC * 32)) & ~7;
+    static_assert(PW == 1 || (PW == 4 && NWC % 4 == 0 && REG_CONSUMER <= 256), "whole warpgroups");
     static_assert(D % 32 == 0 && (E == 8 || E == 4), "head_dim 256 or 128");
     static_assert(TS == 1 || TS == 2, "a chunk is consumed by one warp or split in token halves");
     static_assert(G % HG == 0, "heads split evenly over the head groups");
@@ -170,12 +179,16 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
 // e4m3 codes with one scale per KV head for K and for V; the K scale is folded
 // into q and the V scale into the merge weights, so the inner loops only
 // widen codes instead of bf16 values.  LP: one producer lane per chunk stream
-// (else one lane serves all streams).
-template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8 = false, bool LP = false>
-__global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
+// (else one lane serves all streams).  RB: the producer is the first warp of
+// a warpgroup of its own that lowers its register budget (setmaxnreg) so the
+// consumer warpgroups run with more registers than an even split of the
+// register file allows; its three other warps have no work.
+template <int D, int G, int TS, int NST, int SPS, int HG, bool WIN, bool F8 = false, bool LP = false,
+          bool RB = false>
+__global__ void __launch_bounds__((TS * HG * NST + (RB ? 4 : 1)) * 32, 1)
     pa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecodeParams p) {
-    using C = DecodeCfg<D, G, TS, NST, SPS, HG, F8 ? 1 : 2>;
+    using C = DecodeCfg<D, G, TS, NST, SPS, HG, F8 ? 1 : 2, RB ? 4 : 1>;
     constexpr int E = C::E, MB = C::MB, NWC = C::NWC, NS = C::NS, GW = C::GW, WPC = C::WPC, NWH = C::NWH;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -260,7 +273,15 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
     const int stream = warp / WPC, wh = (warp % WPC) % TS, hg = (warp % WPC) / TS;
     float m_run[GW], l_run[GW];
     float2 acc[GW][E / 2];
-    if (warp == NWC) {
+    // With RB each role's register budget is set inside its own branch, and
+    // neither branch rejoins the other before its budget ends: the compiler
+    // allocates registers per region, and code reachable under both budgets
+    // gets the smaller one.
+    if (warp >= NWC) {
+        if constexpr (RB) {
+            setmaxnreg_dec<C::REG_PRODUCER>();
+            if (warp > NWC) return;  // the producer warpgroup's idle warps
+        }
         // ---------------- producer: PL lanes issue the copies ----------------
         // Lane c0 < PL serves streams c0, c0 + PL, ... (PL = NST: a lane per
         // stream; PL = 1: one lane for all).  A lane polls its streams' next
@@ -357,7 +378,15 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
                 if (lane == 0) set_status(p.status, PA_DEV_TIMEOUT);
             }
         }
+        // With RB the producer leaves here: its copies have all landed (the
+        // consumers wait for every chunk, or it waited for its own copies
+        // before giving up), and the merge below synchronises the consumers
+        // only.  A bad page index it met reaches the consumers through the
+        // full barrier of that chunk, which orders its flag write before
+        // their wait returns.
+        if constexpr (RB) return;
     } else {
+        if constexpr (RB) setmaxnreg_inc<C::REG_CONSUMER>();
         // ---------------- consumers ----------------
         // Arithmetic runs on fp32 pairs (packed FFMA2): dot products pair
         // adjacent dims (even/odd partial sums), the P.V update pairs adjacent
@@ -561,7 +590,14 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
         }
     }
 
-    __syncthreads();  // every chunk is consumed: the stage buffers become the merge area
+    auto cta_sync = [&]() {
+        if constexpr (RB)
+            named_bar_sync(1, NWC * 32);
+        else
+            __syncthreads();
+    };
+    constexpr int MT = RB ? NWC * 32 : C::THREADS;  // threads taking part in the merge
+    cta_sync();  // every chunk is consumed: the stage buffers become the merge area
     const bool aborted = flags[0] != 0;
     // Merge the warp states of this split (same log-sum-exp rule as the split
     // reduce) and write the split result: the warps store their states
@@ -585,7 +621,7 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
             if (lane == 0) merge_ml[warp * GW + g] = make_float2(m_run[g], l_run[g]);
         }
     }
-    __syncthreads();
+    cta_sync();
     if (warp == 0) {
         // lane groups of NWP >= NWH lanes, one group per head; surplus lanes hold empty states
         constexpr int NWP = NWH <= 8 ? 8 : (NWH <= 16 ? 16 : 32);
@@ -613,8 +649,8 @@ __global__ void __launch_bounds__((TS * HG * NST + 1) * 32, 1)
             }
         }
     }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < G * D / 4; idx += C::THREADS) {
+    cta_sync();
+    for (int idx = threadIdx.x; idx < G * D / 4; idx += MT) {
         const int h = (4 * idx) / D, d = 4 * idx - h * D;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 2

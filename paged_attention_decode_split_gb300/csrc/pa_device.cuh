@@ -141,6 +141,25 @@ __device__ __forceinline__ void pdl_wait_primary() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Per-warpgroup register budget (all 128 threads of the warpgroup execute it):
+// dec returns registers to the CTA's pool, inc waits until the pool holds
+// enough.  The sum over warpgroups must stay within what the CTA was launched
+// with (threads x registers per thread at launch); the host checks the
+// kernel's launch register count before it launches a kernel that uses these.
+template <int R>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+// Named barrier over the first `threads` threads of the CTA (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ void set_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
 }
