@@ -51,10 +51,12 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
 // Per (head_dim, group): token halves (TS), chunk streams (NST), stages per
 // stream (SPS), head groups (HG), a producer lane per stream (LP).
 //  * D = 256: groups of 3 to 6 heads run 4 streams x 3 stages x 16 KiB with
-//    each chunk's tokens split over 2 warps (9 warps, 168 registers; for 6
-//    heads the producer sits in a warpgroup of its own that hands its
-//    registers to the 8 consumers, 232 each: no spills, and the 16-layer
-//    step at 32K measured 0.528 ms against 0.537 ms); groups
+//    each chunk's tokens split over 2 warps (9 warps, 168 registers; for 4
+//    and 6 heads the producer sits in a warpgroup of its own that hands its
+//    registers to the 8 consumers, 232 each: no spills, the 16-layer step at
+//    32K measured 0.528 ms against 0.537 ms, and a 4-head call 28.7 us
+//    against 29.2 us; for 3, 5, 8, 12 and 16 heads the same change measured
+//    within noise or slower, so they keep the even split); groups
 //    of 1 and 2 run 6 streams x 2 stages, one warp per chunk; 8, 12 and 16
 //    heads split into head groups of 4, each warp taking a whole chunk (12
 //    heads: 13 warps, measured 54.6 us against 60 us for 2 groups of 6 with
@@ -69,7 +71,8 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
 //    the same bytes in flight per SM.  At D = 256, groups of up to 4 heads
 //    take a producer lane per stream (1 head: 21.3 -> 17.5 us at 32K); wider
 //    groups, whose widening arithmetic bounds them, measured 0-1 % faster
-//    with one lane.
+//    with one lane.  The 6-head fp8 kernel also takes the producer
+//    warpgroup (33.9 -> 32.6 us at 32K).
 template <bool WIN, bool F8>
 cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                               const DecodeParams &p, dim3 grid, cudaStream_t stream) {
@@ -81,7 +84,7 @@ cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, co
                 case 1: return launch_decode_t<256, 1, 1, 6, 4, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 0);
                 case 2: return launch_decode_t<256, 2, 1, 6, 4, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 1);
                 case 4: return launch_decode_t<256, 4, 2, 4, 6, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 2);
-                case 6: return launch_decode_t<256, 6, 2, 4, 6, 1, WIN, F8, false>(tk, tv, p, grid, stream, slot0 + 3);
+                case 6: return launch_decode_t<256, 6, 2, 4, 6, 1, WIN, F8, false, true>(tk, tv, p, grid, stream, slot0 + 3);
                 case 12: return launch_decode_t<256, 12, 1, 4, 6, 3, WIN, F8, false>(tk, tv, p, grid, stream, slot0 + 9);
                 case 3: return launch_decode_t<256, 3, 2, 4, 6, 1, WIN, F8, true>(tk, tv, p, grid, stream, slot0 + 11);
                 case 5: return launch_decode_t<256, 5, 2, 4, 6, 1, WIN, F8, false>(tk, tv, p, grid, stream, slot0 + 12);
@@ -107,7 +110,7 @@ cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, co
         switch (group) {
             case 1: return launch_decode_t<256, 1, 1, 6, 2, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 0);
             case 2: return launch_decode_t<256, 2, 1, 6, 2, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 1);
-            case 4: return launch_decode_t<256, 4, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 2);
+            case 4: return launch_decode_t<256, 4, 2, 4, 3, 1, WIN, false, false, true>(tk, tv, p, grid, stream, slot0 + 2);
             case 6: return launch_decode_t<256, 6, 2, 4, 3, 1, WIN, false, false, true>(tk, tv, p, grid, stream, slot0 + 3);
             case 12: return launch_decode_t<256, 12, 1, 4, 3, 3, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 9);
             case 3: return launch_decode_t<256, 3, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 11);
