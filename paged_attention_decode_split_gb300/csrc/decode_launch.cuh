@@ -55,12 +55,14 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
 //    and 6 heads the producer sits in a warpgroup of its own that hands its
 //    registers to the 8 consumers, 232 each: no spills, the 16-layer step at
 //    32K measured 0.528 ms against 0.537 ms, and a 4-head call 28.7 us
-//    against 29.2 us; for 3, 5, 8, 12 and 16 heads the same change measured
-//    within noise or slower, so they keep the even split); groups
-//    of 1 and 2 run 6 streams x 2 stages, one warp per chunk; 8, 12 and 16
-//    heads split into head groups of 4, each warp taking a whole chunk (12
-//    heads: 13 warps, measured 54.6 us against 60 us for 2 groups of 6 with
-//    split tokens at 32K).  One producer lane serves all streams.
+//    against 29.2 us; for 3 and 5 heads the same change measured within
+//    noise or slower, so they keep the even split); groups of 1 and 2 run
+//    6 streams x 2 stages, one warp per chunk.  8, 12 and 16 heads also take
+//    the producer warpgroup, whose registers let a warp hold more heads:
+//    8 heads in one warp with split tokens (40.65 -> 40.36 us at 32K), 12
+//    and 16 heads in 2 head groups of 6 and 8, each warp taking a whole chunk
+//    (54.7 -> 52.8 us and 69.7 -> 68.6 us against 3 and 4 groups of 4 at
+//    the even split).  One producer lane serves all streams.
 //  * D = 128 (8 KiB stages): every stream has its own producer lane.  Up to 4
 //    heads: 12 streams x 2 stages (1 and 2 heads) or 6 x 4 with split tokens;
 //    5 and 6 heads: 6 x 4 with split tokens; 8, 12 and 16 heads: head groups
@@ -112,11 +114,11 @@ cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, co
             case 2: return launch_decode_t<256, 2, 1, 6, 2, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 1);
             case 4: return launch_decode_t<256, 4, 2, 4, 3, 1, WIN, false, false, true>(tk, tv, p, grid, stream, slot0 + 2);
             case 6: return launch_decode_t<256, 6, 2, 4, 3, 1, WIN, false, false, true>(tk, tv, p, grid, stream, slot0 + 3);
-            case 12: return launch_decode_t<256, 12, 1, 4, 3, 3, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 9);
+            case 12: return launch_decode_t<256, 12, 1, 4, 3, 2, WIN, false, false, true>(tk, tv, p, grid, stream, slot0 + 9);
             case 3: return launch_decode_t<256, 3, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 11);
             case 5: return launch_decode_t<256, 5, 2, 4, 3, 1, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 12);
-            case 8: return launch_decode_t<256, 8, 1, 4, 3, 2, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 13);
-            case 16: return launch_decode_t<256, 16, 1, 3, 4, 4, WIN, false, false>(tk, tv, p, grid, stream, slot0 + 14);
+            case 8: return launch_decode_t<256, 8, 2, 4, 3, 1, WIN, false, false, true>(tk, tv, p, grid, stream, slot0 + 13);
+            case 16: return launch_decode_t<256, 16, 1, 4, 3, 2, WIN, false, false, true>(tk, tv, p, grid, stream, slot0 + 14);
         }
     } else if (head_dim == 128) {
         switch (group) {
