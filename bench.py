@@ -225,7 +225,7 @@ def bench_reference(args, world, rank):
     threads = os.cpu_count() or 1
     times = []
     t_start = time.perf_counter()
-    warm = min(args.warmup, 1)
+    warm = max(3, args.warmup)
     for i in range(warm + args.steps):
         q, kc, vc = layers[0]
         t0 = time.perf_counter()
