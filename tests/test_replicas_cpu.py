@@ -55,3 +55,23 @@ def test_two_gloo_replicas(tmp_path):
         assert rec["slowest"] == 11.0  # the max over ranks, seen by every rank
         assert rec["gbs"] == pytest.approx(2 * (1 << 30) / 11e-3 / 1e9)
     assert recs[1]["reference_returned"] is True
+
+
+def test_reference_arm_line(tmp_path):
+    """The reference arm (the oracle on the host cores) prints one JSON line
+    with the contract's keys, runs at least 3 warm-up steps and reports the
+    metric of the decode arm."""
+    import subprocess
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1", "--warmup", "0",
+           "--reference-budget", "5"]
+    res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 1 and rec["warmup"] >= 3
+    assert rec["unit"] == "GB/s" and rec["higher_is_better"] is True and rec["value"] > 0
+    assert rec["config"]["workload"] == "hybrid_step_l32768_bs784_x16"
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
+    assert rec["cpu_baseline"]["value"] == rec["value"]
+    assert rec["e2e"] == {"value": rec["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
