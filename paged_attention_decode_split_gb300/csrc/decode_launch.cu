@@ -42,7 +42,7 @@ cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, cudaStr
         if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_split_reduce_small_kernel<128>, p, pairs);
         return cudaErrorInvalidValue;
     }
-    cfg.gridDim = dim3(p.num_q_heads, rows, head_dim / 64);
+    cfg.gridDim = dim3(p.num_q_heads, rows, head_dim / 32);
     cfg.blockDim = dim3(128);
     if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_split_reduce_kernel<256>, p);
     if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_split_reduce_kernel<128>, p);

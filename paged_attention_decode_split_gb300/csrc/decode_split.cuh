@@ -693,16 +693,18 @@ struct ReduceParams {
 };
 
 
-// Grid (Hq, rows, D / 64), 128 threads: each CTA merges a 64-wide slice of
-// one (row, head) output.  Its threads split the splits 8 ways; every thread
+// Grid (Hq, rows, D / 32), 128 threads: each CTA merges a 32-wide slice of
+// one (row, head) output.  Its threads split the splits 16 ways; every thread
 // issues the loads of all its splits' statistics and partial outputs at once,
-// folds them with a running log-sum-exp, and a single exchange merges the 8
-// per-group states.
+// folds them with a running log-sum-exp, and a single exchange merges the 16
+// per-group states.  (32-wide slices measured 0.56 us faster per 32K call than
+// 64-wide ones and 0.17 us faster than 16-wide ones: more CTAs, fewer loads
+// per thread.)
 template <int D>
 __global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams p) {
-    constexpr int QD = 16;  // float4 columns of the 64-wide slice
-    constexpr int SG = 8;   // split groups
-    constexpr int UNROLL = 8;
+    constexpr int QD = 8;   // float4 columns of the 32-wide slice
+    constexpr int SG = 16;  // split groups
+    constexpr int UNROLL = 4;
     __shared__ float4 red_o[SG][QD];
     __shared__ float2 red_ml[SG];
     __shared__ int red_bad;
@@ -717,7 +719,7 @@ __global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams
     const size_t r = (size_t)row * p.num_q_heads + hq;
     const float2 *ml = p.part_ml + r * p.num_splits;
     const int qd = threadIdx.x % QD, sg = threadIdx.x / QD;
-    const float *po = p.part_o + r * p.num_splits * D + slice * 64 + qd * 4;
+    const float *po = p.part_o + r * p.num_splits * D + slice * 32 + qd * 4;
 
     float M = -INFINITY, W = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -767,7 +769,7 @@ __global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams
         }
         const bool zero = red_bad != 0 || !(Wt > 0.f);
         const float inv = zero ? 0.f : 1.f / Wt;
-        const size_t base = r * D + slice * 64 + qd * 4;
+        const size_t base = r * D + slice * 32 + qd * 4;
         store_out(p.out, base + 0, at.x * inv, p.out_bf16);
         store_out(p.out, base + 1, at.y * inv, p.out_bf16);
         store_out(p.out, base + 2, at.z * inv, p.out_bf16);
