@@ -131,8 +131,9 @@ typedef struct {
     int32_t reduce_launched;   /* 1 if the partition-reduce kernel ran */
 } pa_plan_info;
 
-#define PA_PATH_DECODE_CUDA_CORE 1  /* split-KV decode, CUDA cores, TMA-staged chunks */
-#define PA_PATH_VERIFY_TCGEN05 3    /* multi-row verify, tcgen05 + TMEM (2 is not used) */
+#define PA_PATH_DECODE_CUDA_CORE 1  /* retired: split-KV decode on the CUDA cores (no longer reported) */
+#define PA_PATH_DECODE_MMA 2        /* split-KV decode, both products on the tensor cores (mma.sync) */
+#define PA_PATH_VERIFY_TCGEN05 3    /* multi-row verify, tcgen05 + TMEM */
 
 /* Bytes of device workspace an attention call with this description needs
  * (split partials: out vectors, max and sum per split).  0 when the plan does

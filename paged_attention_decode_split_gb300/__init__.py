@@ -21,14 +21,14 @@ __all__ = [
     "reshape_and_cache", "paged_attention_decode", "paged_attention_verify", "last_plan",
     "status_string", "PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_WORKSPACE",
     "PA_ERR_CUDA", "PA_OUT_F32", "PA_OUT_BF16", "PA_DEV_BAD_SEQLEN", "PA_DEV_BAD_PAGE",
-    "PA_DEV_BAD_SLOT", "PA_DEV_TIMEOUT", "PA_PATH_DECODE_CUDA_CORE",
+    "PA_DEV_BAD_SLOT", "PA_DEV_TIMEOUT", "PA_PATH_DECODE_CUDA_CORE", "PA_PATH_DECODE_MMA",
     "PA_PATH_VERIFY_TCGEN05", "PA_FLAG_EARLY_KV_READ", "PA_NOALLOC_SCRATCH_BYTES", "paged_attention_decode_noalloc",
 ]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, 1, 2, 3, 4
 PA_OUT_F32, PA_OUT_BF16 = 0, 1
 PA_DEV_BAD_SEQLEN, PA_DEV_BAD_PAGE, PA_DEV_BAD_SLOT, PA_DEV_TIMEOUT = 1, 2, 4, 8
-PA_PATH_DECODE_CUDA_CORE, PA_PATH_VERIFY_TCGEN05 = 1, 3
+PA_PATH_DECODE_CUDA_CORE, PA_PATH_DECODE_MMA, PA_PATH_VERIFY_TCGEN05 = 1, 2, 3
 PA_FLAG_EARLY_KV_READ = 1
 PA_NOALLOC_SCRATCH_BYTES = 8 << 20
 

@@ -160,6 +160,56 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// x = head + residual with both parts in bf16 (packed pairs for elements a, b).
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t &head, uint32_t &resid) {
+    head = pack_bf16(a, b);
+    const float2 h = make_float2(__uint_as_float(head << 16), __uint_as_float(head & 0xffff0000u));
+    const float2 r = __ffma2_rn(h, make_float2(-1.f, -1.f), make_float2(a, b));  // (a, b) - head, exact
+    resid = pack_bf16(r.x, r.y);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// The same split with both parts in f16.
+__device__ __forceinline__ void split_f16(float a, float b, uint32_t &head, uint32_t &resid) {
+    head = pack_f16(a, b);
+    const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&head));
+    const float2 r = __ffma2_rn(h, make_float2(-1.f, -1.f), make_float2(a, b));
+    resid = pack_f16(r.x, r.y);
+}
+
+// The fp8-cache kernels multiply in f16, so q (bf16, 8 exponent bits) is
+// brought into f16's range first: the row (or head) is scaled by the power of
+// two 2^e that puts its largest |element| in [2^14, 2^15), and 2^-e joins the
+// softmax scale.  `amax` is the largest bf16 bit pattern of the row with the
+// sign cleared (for non-NaN values the integer order is the order of the
+// magnitudes), E its exponent field, e = 141 - E, kept in [-100, 64] so that
+// both 2^e and scale * 2^-e are normal binary32 numbers.  Every element
+// within 2^38 of the largest keeps all its bits (f16 subnormals reach 2^-24).
+__device__ __forceinline__ float f16_prescale(uint32_t amax) {
+    const int e = min(64, max(-100, 141 - (int)(amax >> 7)));
+    return __uint_as_float((uint32_t)(127 + e) << 23);
+}
+
+// The larger magnitude of a bf16 pair, as a bit pattern with the sign cleared.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t w) {
+    return max(w & 0x7fffu, (w >> 16) & 0x7fffu);
+}
+
+// Two bf16 (packed) times a power of two -> two f16 (packed), exact when the
+// scaled values lie in f16's normal range.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s) {
+    return pack_f16(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xffff0000u) * s);
+}
+
 __device__ __forceinline__ void set_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
 }

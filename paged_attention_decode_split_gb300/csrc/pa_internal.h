@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "decode_mma.cuh"
 #include "decode_split.cuh"
 #include "verify_tc.cuh"
 

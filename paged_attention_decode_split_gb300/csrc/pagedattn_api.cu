@@ -164,7 +164,7 @@ EncodeTiledFn get_encode_fn() {
 struct MapKey {
     const void *base;
     int64_t num_pages;
-    int32_t block_size, num_kv_heads, head_dim, box_d, kind;  // kind: 0 chunk box, 1 whole-tile 5-D box
+    int32_t block_size, num_kv_heads, head_dim, box_d, kind;  // kind 0: chunk box of box_d dims; 1: 5-D column-block box of box_d tokens
     bool swizzle128, fp8;
     bool operator==(const MapKey &o) const {
         return base == o.base && num_pages == o.num_pages && block_size == o.block_size &&
@@ -215,12 +215,15 @@ bool encode_cache_map_uncached(CUtensorMap *map, const void *base, const pa_attn
     return r == CUDA_SUCCESS;
 }
 
-// 5-D view for the tensor-core path: {128-byte column block, tokens, blocks,
-// head, page}; one box of {block, 64 tokens, all blocks, 1, 1} lands in
-// shared memory as [blocks][64 tokens][128 B] with the 128-byte swizzle -- the
-// K-major (and MN-major) operand layout the MMA reads -- in a single copy.
-// bf16: 64-dim blocks; fp8: 128-code blocks.
-bool encode_cache_map_blocks_uncached(CUtensorMap *map, const void *base, const pa_attn_desc *d, bool fp8) {
+// 5-D view for the tensor-core paths: {128-byte column block, tokens, blocks,
+// head, page}; one box of {block, `tokens` tokens, all blocks, 1, 1} lands in
+// shared memory as [blocks][tokens][128 B] with the 128-byte swizzle -- the
+// K-major (and MN-major) operand layout the tcgen05 MMA reads, and the layout
+// in which ldmatrix rows never share a bank group -- in a single copy.
+// Verify copies 64-token tiles, decode 16-token chunks.  bf16: 64-dim blocks;
+// fp8: 128-code blocks.
+bool encode_cache_map_blocks_uncached(CUtensorMap *map, const void *base, const pa_attn_desc *d, bool fp8,
+                                      int tokens) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
     const int esz = fp8 ? 1 : 2, blk = 128 / esz;
@@ -228,7 +231,7 @@ bool encode_cache_map_blocks_uncached(CUtensorMap *map, const void *base, const 
     const cuuint64_t dims[5] = {(cuuint64_t)blk, (cuuint64_t)d->block_size, (cuuint64_t)(d->head_dim / blk),
                                 (cuuint64_t)d->num_kv_heads, (cuuint64_t)d->num_pages};
     const cuuint64_t strides[4] = {row * d->num_kv_heads, 128, row, row * d->num_kv_heads * d->block_size};
-    const cuuint32_t box[5] = {(cuuint32_t)blk, 64, (cuuint32_t)(d->head_dim / blk), 1, 1};
+    const cuuint32_t box[5] = {(cuuint32_t)blk, (cuuint32_t)tokens, (cuuint32_t)(d->head_dim / blk), 1, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
                     const_cast<void *>(base), dims, strides, box, estr,
@@ -245,9 +248,11 @@ bool encode_cache_map(CUtensorMap *map, const void *base, const pa_attn_desc *d,
     });
 }
 
-bool encode_cache_map_blocks(CUtensorMap *map, const void *base, const pa_attn_desc *d, bool fp8 = false) {
-    const MapKey key{base, d->num_pages, d->block_size, d->num_kv_heads, d->head_dim, 0, 1, true, fp8};
-    return cached_map(map, key, [&](CUtensorMap *m) { return encode_cache_map_blocks_uncached(m, base, d, fp8); });
+bool encode_cache_map_blocks(CUtensorMap *map, const void *base, const pa_attn_desc *d, bool fp8 = false,
+                             int tokens = 64) {
+    const MapKey key{base, d->num_pages, d->block_size, d->num_kv_heads, d->head_dim, tokens, 1, true, fp8};
+    return cached_map(map, key,
+                      [&](CUtensorMap *m) { return encode_cache_map_blocks_uncached(m, base, d, fp8, tokens); });
 }
 
 void record_plan(int path, const Plan &pl, const pa_attn_desc *d, int ctas) {
@@ -531,9 +536,10 @@ pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, c
     st = check_workspace(pl, workspace, workspace_bytes);
     if (st != PA_OK) return st;
 
+    // 16-token chunks as [column blocks][16 tokens][128 B], 128-byte swizzle
     CUtensorMap tk, tv;
-    if (!encode_cache_map(&tk, k_cache, desc, desc->head_dim, false, fp8) ||
-        !encode_cache_map(&tv, v_cache, desc, desc->head_dim, false, fp8))
+    if (!encode_cache_map_blocks(&tk, k_cache, desc, fp8, kChunk) ||
+        !encode_cache_map_blocks(&tv, v_cache, desc, fp8, kChunk))
         return PA_ERR_CUDA;
 
     const int group = desc->num_q_heads / desc->num_kv_heads;
@@ -575,7 +581,7 @@ pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, c
         if (launch_reduce(desc->head_dim, r, desc->num_seqs, s) != cudaSuccess)
             return PA_ERR_CUDA;
     }
-    record_plan(PA_PATH_DECODE_CUDA_CORE, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
+    record_plan(PA_PATH_DECODE_MMA, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
     return PA_OK;
 }
 

@@ -48,7 +48,9 @@
 // -- exact, since every e4m3 value is an f16 value -- zeroing rows past the
 // tile's last key.  Q and P then enter the products as f16 (kind::f16 with
 // f16 A and B), the K scale joins the softmax scale and the V scale the final
-// normaliser.
+// normaliser.  A q row enters scaled by a power of two that brings its
+// largest element into [2^14, 2^15), so any finite bf16 q fits f16; the
+// inverse power joins the softmax scale.
 #pragma once
 
 #include "decode_split.cuh"
@@ -85,37 +87,6 @@ struct VerifyParams {
 // tile written with the 128-byte swizzle (chunk index XOR row % 8).
 __device__ __forceinline__ uint32_t swz_off(int t, int c, int rows) {
     return (uint32_t)((c >> 3) * rows * 128 + t * 128 + (((c & 7) ^ (t & 7)) << 4));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
-// x = head + residual with both parts in bf16 (packed pairs for elements a, b).
-__device__ __forceinline__ void split_bf16(float a, float b, uint32_t &head, uint32_t &resid) {
-    head = pack_bf16(a, b);
-    const float2 h = make_float2(__uint_as_float(head << 16), __uint_as_float(head & 0xffff0000u));
-    const float2 r = __ffma2_rn(h, make_float2(-1.f, -1.f), make_float2(a, b));  // (a, b) - head, exact
-    resid = pack_bf16(r.x, r.y);
-}
-
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-    const __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
-// The same split with both parts in f16.
-__device__ __forceinline__ void split_f16(float a, float b, uint32_t &head, uint32_t &resid) {
-    head = pack_f16(a, b);
-    const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&head));
-    const float2 r = __ffma2_rn(h, make_float2(-1.f, -1.f), make_float2(a, b));
-    resid = pack_f16(r.x, r.y);
-}
-
-// Two bf16 (packed) -> two f16 (packed); exact for the magnitudes q takes.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-    return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 // Eight e4m3 codes (one 32-bit word each of four) -> eight f16 in 16 bytes.
@@ -472,11 +443,26 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
     // Q block -> tensor memory, the A operand of S = Q K^T: row rho in lane
     // rho, dims packed two per column; padding rows are zero.  The softmax
     // warps store it while the producer already streams K and V; only the
-    // MMA warp waits for it (named barrier 1: warps 0-4).
+    // MMA warp waits for it (named barrier 1: warps 0-4).  Over an fp8 cache
+    // the products run in f16, and each row enters scaled by q_pre, the power
+    // of two that brings its largest element into [2^14, 2^15) (f16_prescale).
+    float q_pre = 1.f;
     if (warp < 4) {
         const int rho = row0 + threadIdx.x;  // rows past R are zero padding
         const __nv_bfloat16 *qrow =
             p.q + (((size_t)b * p.q_len + rho / G) * p.num_q_heads + kvh * G + rho % G) * D;
+        if constexpr (F8) {
+            uint32_t amax = 0;
+            if ((int)threadIdx.x < R) {
+#pragma unroll 4
+                for (int v = 0; v < D / 8; ++v) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 8 * v);
+                    amax = max(max(amax, max(bf16x2_absmax(w.x), bf16x2_absmax(w.y))),
+                               max(bf16x2_absmax(w.z), bf16x2_absmax(w.w)));
+                }
+            }
+            q_pre = f16_prescale(amax);
+        }
 #pragma unroll 1
         for (int c0 = 0; c0 < D / 2; c0 += 64) {
             uint32_t r[2][32];
@@ -485,8 +471,8 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
                 uint4 w = (int)threadIdx.x < R ? *reinterpret_cast<const uint4 *>(qrow + 2 * c0 + 8 * v)
                                                : make_uint4(0u, 0u, 0u, 0u);
                 if constexpr (F8)  // the products run in f16: Q too
-                    w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
-                                   bf16x2_to_f16x2(w.w));
+                    w = make_uint4(bf16x2_to_f16x2_scaled(w.x, q_pre), bf16x2_to_f16x2_scaled(w.y, q_pre),
+                                   bf16x2_to_f16x2_scaled(w.z, q_pre), bf16x2_to_f16x2_scaled(w.w, q_pre));
                 r[v >> 3][4 * (v & 7)] = w.x;
                 r[v >> 3][4 * (v & 7) + 1] = w.y;
                 r[v >> 3][4 * (v & 7) + 2] = w.z;
@@ -688,7 +674,8 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
         const int t_end = min(L, (c_begin + n_my) * kChunk);
         const int lim = live ? min(L - p.q_len + rho / G, t_end - 1) : -1;
         const int lo = p.window > 0 ? L - p.q_len + rho / G - p.window + 1 : 0;  // first key of the row's window
-        const float sl = F8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;  // fp8: K's scale joins q's
+        // fp8: K's scale and the inverse of q's pre-scale (a power of two) join the softmax scale
+        const float sl = F8 ? p.scale_log2 * p.k_scale[kvh] * (1.f / q_pre) : p.scale_log2;
         float m_ref = -INFINITY, l_sum = 0.f;
         bool ok = true;
         // O += P_k V_k of tile k is waited for in order per barrier (tile k +

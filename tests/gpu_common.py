@@ -79,6 +79,19 @@ def oracle_out(oracle_mod, prob, layer=0, rows=None, window=0):
                                       sl.numpy(), prob.scale, q_len=prob.q_len, window=window)
 
 
+def assert_cache_written(oracle_mod, k_before, v_before, k_new, v_new, slots, k_dev, v_dev):
+    """The bf16 caches that the GPU's reshape_and_cache wrote (k_dev, v_dev)
+    equal, bit for bit, the oracle's scatter of the same new rows into CPU
+    copies of the caches as they were before the call.  Tests that hand a
+    GPU-written cache to the oracle check it with this first, so a slot
+    error cannot be read identically by both sides."""
+    from tests.helpers import bits
+    k_ref, v_ref = bits(k_before).copy(), bits(v_before).copy()
+    oracle_mod.reshape_and_cache(bits(k_new), bits(v_new), k_ref, v_ref, np.asarray(slots.cpu().numpy(), np.int64))
+    assert np.array_equal(bits(k_dev), k_ref), "reshape_and_cache wrote K differently from the oracle"
+    assert np.array_equal(bits(v_dev), v_ref), "reshape_and_cache wrote V differently from the oracle"
+
+
 def parity_report(gpu: torch.Tensor, ref: np.ndarray) -> dict:
     g = gpu.double().numpy()
     err = np.abs(g - ref)

@@ -12,7 +12,8 @@ import torch
 import paged_attention_decode_split_gb300 as pa
 from paged_attention_decode_split_gb300 import _build
 from paged_attention_decode_split_gb300.inputs import make_new_tokens, make_problem
-from tests.gpu_common import REL_L2_VERIFY, assert_parity, desc_for, oracle_out, run_attention, to_dev
+from tests.gpu_common import (REL_L2_VERIFY, assert_cache_written, assert_parity, desc_for, oracle_out, run_attention,
+                              to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -89,6 +90,8 @@ def chained(prob, seed, flags):
         pa.reshape_and_cache(kn, vn, kc, vc, slots)
         out, status = call(prob, (q, kc, vc, bt, sl), flags)
     torch.cuda.synchronize()
+    import oracle
+    assert_cache_written(oracle, prob.k_cache[0], prob.v_cache[0], k_new, v_new, slots, kc, vc)
     prob.k_cache[0], prob.v_cache[0] = kc.cpu(), vc.cpu()
     return out.cpu(), status.item(), prob
 

@@ -14,7 +14,8 @@ import torch
 import paged_attention_decode_split_gb300 as pa
 from paged_attention_decode_split_gb300 import _build
 from paged_attention_decode_split_gb300.inputs import WORKLOADS, make_new_tokens, make_problem
-from tests.gpu_common import REL_L2_VERIFY, assert_parity, desc_for, oracle_out, run_attention, scales_dev, to_dev
+from tests.gpu_common import (REL_L2_DECODE, REL_L2_VERIFY, assert_parity, desc_for, oracle_out, run_attention,
+                              scales_dev, to_dev)
 from tests.helpers import bits
 
 pytestmark = pytest.mark.gpu
@@ -114,7 +115,7 @@ def test_reshape_and_cache_fp8_bad_slot_flagged(oracle_mod):
 def test_decode_fp8_ragged_tails_nan_poisoned(oracle_mod, bs):
     prob = hybrid(501 + bs, TAIL_LENGTHS, bs, poison_unused=True)
     out, status, plan = run_attention(prob)
-    assert status == 0 and plan["path_id"] == pa.PA_PATH_DECODE_CUDA_CORE
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_DECODE_MMA
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"fp8 tails bs={bs}")
 
 
@@ -283,3 +284,118 @@ def test_verify_fp8_wide_group_g12(oracle_mod):
     out, status, _ = run_attention(prob)
     assert status == 0
     assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY, what="fp8 verify G=12")
+
+
+# -- the range of q over an fp8 cache ---------------------------------------------------
+# Over an fp8 cache the products run in f16, whose range (about 6e-8 .. 65504)
+# is far narrower than bf16's.  Each q row (verify) or head (decode) enters f16
+# scaled by a power of two that puts its largest element in [2^14, 2^15), so
+# any finite bf16 q keeps its bits.  These problems give the query heads
+# magnitudes from 1e-6 to 1e5: logits from ~1e-5 (a near-uniform softmax) to
+# ~1e5 nats (a one-hot one).
+#
+# At 1e5 nats the fp32 logits themselves carry rounding errors of a fraction
+# of a nat, so a row whose top keys tie to within that error has an output
+# that any fp32 kernel gets only to within the softmax's sensitivity.  The
+# tolerance is therefore derived per (row, head) from the inputs:
+#   dx    = 2^-19 * max_t scale log2(e) sum_d |q_d K_td|   (the products are
+#           exact; the tensor core rounds each 16-dim step's sum into the fp32
+#           accumulator, D / 16 <= 16 roundings of at most 2 ulps each
+#           (truncation allowed): below 2^-19 of the sum of the products'
+#           magnitudes, in log2 units)
+#   extra = 2 ln 2 * dx * sum_t p_t |V_t - o|_inf           (first-order change
+#           of o = sum_t p_t V_t when every logit moves by up to dx)
+# and every element must satisfy |gpu - oracle| <= 2e-3 + extra.  Rows with
+# extra < 1e-6 -- the near-uniform rows of the small magnitudes and the
+# one-hot rows of the large ones, all but the near-ties -- must also pass the
+# full gate, relative L2 included.
+
+Q_MAGNITUDES = [1e-6, 1e-4, 1e-2, 1.0, 30.0, 1e3, 2e4, 1e5]
+
+
+def scale_q_heads(prob):
+    hq = prob.num_q_heads
+    mags = torch.tensor([Q_MAGNITUDES[h % len(Q_MAGNITUDES)] for h in range(hq)], dtype=torch.float32)
+    prob.q[0] = (prob.q[0].float() * mags[None, :, None]).to(torch.bfloat16)
+    assert torch.isfinite(prob.q[0].float()).all()
+    return prob
+
+
+def q_range_problem(seed, lens, bs, q_len=1, fp8=True):
+    prob = hybrid(seed, lens, bs, q_len=q_len, num_q_heads=24, poison_unused=True, kv_fp8=fp8)
+    return scale_q_heads(prob)
+
+
+def rounding_sensitivity(prob):
+    """extra[row, head] of the derivation above, from the inputs in float64
+    (torch decodes the e4m3 codes exactly)."""
+    def values(c, s):
+        if prob.kv_fp8:
+            return c.view(torch.float8_e4m3fn).double() * s.double()[None, None, :, None]
+        return c.double()
+    kc = values(prob.k_cache[0], prob.k_scale[0] if prob.kv_fp8 else None)
+    vc = values(prob.v_cache[0], prob.v_scale[0] if prob.kv_fp8 else None)
+    G = prob.num_q_heads // prob.num_kv_heads
+    extra = np.zeros((prob.num_seqs * prob.q_len, prob.num_q_heads))
+    for b in range(prob.num_seqs):
+        L = int(prob.seq_lens[b])
+        t = torch.arange(L)
+        pages = prob.block_table[b, t // prob.block_size].long()
+        K, V = kc[pages, t % prob.block_size], vc[pages, t % prob.block_size]  # [L, Hkv, D]
+        for r in range(prob.q_len):
+            n = L - prob.q_len + r + 1
+            if n <= 0:
+                continue
+            q = prob.q[0][b * prob.q_len + r].double()  # [Hq, D]
+            for h in range(prob.num_q_heads):
+                Kh, Vh = K[:n, h // G], V[:n, h // G]
+                s = prob.scale * (Kh @ q[h])
+                dx = 2.0 ** -19 * (prob.scale * math.log2(math.e) * (Kh.abs() @ q[h].abs())).max()
+                p = torch.softmax(s, 0)
+                o = p @ Vh
+                spread = (p * (Vh - o).abs().max(dim=1).values).sum()
+                extra[b * prob.q_len + r, h] = float(2 * math.log(2) * dx * spread)
+    return extra
+
+
+def assert_q_range_parity(out, ref, extra, rel_l2, what):
+    g = out.double().numpy()
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - ref).max(axis=2)  # [rows, heads]
+    assert (err <= 2e-3 + extra).all(), f"{what}: max excess {(err - 2e-3 - extra).max():.3g}"
+    ok = extra < 1e-6
+    assert ok.mean() > 0.4, f"{what}: too few well-conditioned rows ({ok.mean():.2f})"
+    assert_parity(out[torch.from_numpy(ok)][:, None, :], ref[ok][:, None, :], rel_l2=rel_l2,
+                  what=f"{what} (well-conditioned rows)")
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_decode_fp8_q_range(oracle_mod, splits):
+    prob = q_range_problem(581, [3000, 77], 784)
+    out, status, _ = run_attention(prob, num_splits=splits)
+    assert status == 0
+    assert_q_range_parity(out, oracle_out(oracle_mod, prob), rounding_sensitivity(prob), REL_L2_DECODE,
+                          f"fp8 decode q from 1e-6 to 1e5, splits={splits}")
+
+
+@pytest.mark.parametrize("D", [256, 128])
+def test_verify_fp8_q_range(oracle_mod, D):
+    if D == 256:
+        prob = q_range_problem(591, [2000, 40], 832, q_len=16)
+    else:
+        prob = scale_q_heads(make_problem(592, num_seqs=2, seq_lens=[2000, 40], num_q_heads=32, num_kv_heads=8,
+                                          head_dim=128, block_size=16, q_len=16, scale=1 / math.sqrt(128),
+                                          kv_fp8=True, poison_unused=True))
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
+    assert_q_range_parity(out, oracle_out(oracle_mod, prob), rounding_sensitivity(prob), REL_L2_VERIFY,
+                          f"fp8 verify q range D={D}")
+
+
+def test_decode_bf16_q_range(oracle_mod):
+    """The same magnitudes over a bf16 cache (bf16 products, no pre-scale)."""
+    prob = q_range_problem(601, [3000, 77], 784, fp8=False)
+    out, status, _ = run_attention(prob, num_splits=3)
+    assert status == 0
+    assert_q_range_parity(out, oracle_out(oracle_mod, prob), rounding_sensitivity(prob), REL_L2_DECODE,
+                          "bf16 decode q from 1e-6 to 1e5")

@@ -60,6 +60,6 @@ def test_random_case(oracle_mod, i):
                         scale=1 / math.sqrt(c["d"]), poison_unused=True, kv_fp8=c["fp8"])
     out, status, plan = run_attention(prob, num_splits=c["splits"], window=c["window"], flags=c["flags"])
     assert status == 0, c
-    want = pa.PA_PATH_DECODE_CUDA_CORE if c["q_len"] == 1 else pa.PA_PATH_VERIFY_TCGEN05
+    want = pa.PA_PATH_DECODE_MMA if c["q_len"] == 1 else pa.PA_PATH_VERIFY_TCGEN05
     assert plan["path_id"] == want, c
     assert_parity(out, oracle_out(oracle_mod, prob, window=c["window"]), rel_l2=REL_L2_VERIFY, what=str(c))

@@ -14,8 +14,10 @@ import torch
 
 import paged_attention_decode_split_gb300 as pa
 from paged_attention_decode_split_gb300 import _build
-from paged_attention_decode_split_gb300.inputs import WORKLOADS, make_new_tokens, make_problem, sweep_workload
-from tests.gpu_common import (REL_L2_DECODE, REL_L2_VERIFY, assert_parity, oracle_out, run_attention, to_dev)
+from paged_attention_decode_split_gb300.inputs import (SWEEP_DEPTHS, WORKLOADS, make_new_tokens, make_problem,
+                                                       sweep_workload)
+from tests.gpu_common import (REL_L2_DECODE, REL_L2_VERIFY, assert_cache_written, assert_parity, oracle_out,
+                               run_attention, to_dev)
 from tests.helpers import bits
 
 pytestmark = pytest.mark.gpu
@@ -43,7 +45,7 @@ def hybrid(seed, lens, bs, **kw):
 def test_decode_l512_bs16_workload(oracle_mod):
     prob = make_problem(1001, **WORKLOADS["decode_l512_bs16"])
     out, status, plan = run_attention(prob)
-    assert status == 0 and plan["path_id"] == pa.PA_PATH_DECODE_CUDA_CORE
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_DECODE_MMA
     assert_parity(out, oracle_out(oracle_mod, prob), what="512-token decode")
 
 
@@ -101,7 +103,7 @@ def test_decode_wide_group_g12(oracle_mod, splits):
     prob = hybrid(251 + splits, TAIL_LENGTHS[:7] + [5000], 784, num_q_heads=48, num_kv_heads=4,
                   poison_unused=True)
     out, status, plan = run_attention(prob, num_splits=splits)
-    assert status == 0 and plan["path_id"] == pa.PA_PATH_DECODE_CUDA_CORE
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_DECODE_MMA
     assert_parity(out, oracle_out(oracle_mod, prob), what=f"G=12 splits={splits}")
 
 
@@ -232,9 +234,10 @@ def test_hybrid_step_l32768_bs784_x16_layers(oracle_mod):
         assert_parity(out, oracle_out(oracle_mod, prob, layer), what=f"32K layer {layer}")
 
 
-@pytest.mark.parametrize("depth", [500, 4096, 32768])
+@pytest.mark.parametrize("depth", SWEEP_DEPTHS)
 @pytest.mark.parametrize("dense", [False, True])
 def test_context_sweep_depths(oracle_mod, depth, dense):
+    """Every depth of the context sweep, both shapes, in the benchmark's plan."""
     prob = make_problem(1003 + depth + dense, **sweep_workload(depth, dense, num_layers=1))
     out, status, _ = run_attention(prob)
     assert status == 0
@@ -253,12 +256,16 @@ def test_batch32_uniform_bs784_sampled(oracle_mod):
 # -- verify ----------------------------------------------------------------------
 
 def write_new_rows(prob, seed):
-    """reshape_and_cache of the q_len newest tokens of every sequence (GPU)."""
+    """reshape_and_cache of the q_len newest tokens of every sequence (GPU),
+    checked bit for bit against the oracle's scatter before the oracle and
+    the kernels read the cache."""
+    import oracle
     k_new, v_new = make_new_tokens(seed, prob.num_seqs * prob.q_len, prob.num_kv_heads, prob.head_dim)
     slots = prob.new_token_slots()
     kc, vc = prob.k_cache[0].cuda(), prob.v_cache[0].cuda()
     pa.reshape_and_cache(k_new.cuda(), v_new.cuda(), kc, vc, slots.cuda())
     torch.cuda.synchronize()
+    assert_cache_written(oracle, prob.k_cache[0], prob.v_cache[0], k_new, v_new, slots, kc, vc)
     prob.k_cache[0], prob.v_cache[0] = kc.cpu(), vc.cpu()
 
 
