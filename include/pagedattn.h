@@ -138,7 +138,9 @@ typedef struct {
 /* Bytes of device workspace an attention call with this description needs
  * (split partials: out vectors, max and sum per split).  0 when the plan does
  * not split.  Returns (size_t)-1 if the description is invalid.  Host only;
- * queries the device SM count unless desc->num_sms > 0. */
+ * queries the device SM count unless desc->num_sms > 0.  The workspace may
+ * hold anything before a call: every split writes the record the merge reads,
+ * so one workspace serves any calls whose descriptions fit, without clearing. */
 size_t pa_workspace_bytes(const pa_attn_desc *desc);
 
 /* Page length, in tokens, for a hybrid model whose attention KV cache and
@@ -179,7 +181,11 @@ pa_status pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cac
  * (block_table[b, t / BS], t % BS).  L_b = seq_lens[b] counts every cached
  * token, including the one just written.  L_b == 0 gives a zero row.
  * The context is cut into desc-planned splits per (sequence, KV head); each
- * split runs on its own CTA and a log-sum-exp reduce merges them.
+ * split runs on its own CTA ("Hybrid SSM decode rate on dual Radeon under
+ * vLLM", the split-KV fix: the KV range cut across workgroups, then
+ * reduced); a log-sum-exp reduce merges them.  The arithmetic per split is
+ * the tiled loop of "DCU page832 attention", Sec.5, over the page walk of its
+ * Sec.7.
  *   q            device bf16 [B, Hq, D]
  *   k_cache,
  *   v_cache      device bf16 [P, BS, Hkv, D]
@@ -187,7 +193,8 @@ pa_status pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cac
  *                page a sequence uses are never read
  *   seq_lens     device int32 [B]
  *   out          device [B, Hq, D] of desc->out_dtype
- *   workspace    device, >= pa_workspace_bytes(desc) bytes (may be NULL if 0)
+ *   workspace    device, >= pa_workspace_bytes(desc) bytes (may be NULL if 0);
+ *                calls that share a workspace must not overlap on the GPU
  *   device_status nullable device int32, PA_DEV_* bits are OR-ed in */
 pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
                                     const int32_t *block_table, const int32_t *seq_lens,
@@ -195,7 +202,8 @@ pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const vo
                                     size_t workspace_bytes, int32_t *device_status, void *stream);
 
 /* paged_attention_verify -- desc->q_len > 1 new rows per sequence, causal among
- * them (speculative verify).  Rows are ordered (sequence, new row): q and out
+ * them (speculative verify: "Qwen3.8 on MI350P", Lektion 3, the verify rows
+ * of one request sharing every K/V tile under a per-row causal mask).  Rows are ordered (sequence, new row): q and out
  * are [B * q_len, Hq, D].  Row r (0-based) of sequence b attends to keys
  * 0 .. L_b - q_len + r inclusive; the q_len new rows must already be in the
  * cache (L_b >= q_len, else PA_DEV_BAD_SEQLEN and zero rows).  The G * q_len
@@ -279,6 +287,9 @@ pa_status pa_paged_attention_verify_fp8(const void *q, const void *k_cache, cons
  *     writes every partial it later reads.  Calls whose kernels overlap on the
  *     GPU (different streams, no ordering between them) race on the array and
  *     give wrong results: order them.
+ *   - The array's address is cached per device ordinal for the life of the
+ *     process: a device reset (cudaDeviceReset) after the first call on that
+ *     device is not supported.
  * Other arguments, results and errors as for pa_paged_attention_decode. */
 pa_status pa_paged_attention_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                             const int32_t *block_table, const int32_t *seq_lens,

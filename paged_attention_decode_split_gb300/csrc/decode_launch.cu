@@ -1,6 +1,7 @@
 // decode_launch.cu -- launches the split-KV decode kernel (full attention
-// here, sliding window in decode_launch_window.cu) and the partition-reduce
-// kernel as a programmatic dependent of it.
+// here, sliding window and fp8 in their own translation units) and the
+// partition-reduce kernel, a programmatic dependent of the split kernel of a
+// decode or verify call.
 #include "decode_launch.cuh"
 
 namespace pa {

@@ -6,8 +6,8 @@
 // under vLLM"): for one (sequence, KV head) split of whole 16-token chunks,
 // the online softmax of the G query heads of the group over the split's keys,
 // written as the split's normalised output with its max logit and exponential
-// sum (or as the final output when the plan has one split).  The same
-// partition reduce merges the splits.
+// sum (or as the final output when the plan has one split); the partition
+// reduce of decode_split.cuh merges the splits.
 //
 // Why tensor cores here: on the CUDA cores the G-head dot products, the bf16
 // widening and the cross-lane sums cost about 1,900 warp instructions per

@@ -46,7 +46,9 @@ extern "C" pa_status pa_paged_attention_decode_noalloc(const void *q, const void
                                                        const pa_attn_desc *desc, void *out, int32_t *device_status,
                                                        void *stream) {
     if (!desc) return PA_ERR_INVALID_ARG;
-    const size_t need = pa_workspace_bytes(desc);
+    // A description the ordinary decode rejects (q_len != 1 among them) gets
+    // that call's exact error before any size is compared, and nothing runs.
+    const size_t need = desc->q_len == 1 ? pa_workspace_bytes(desc) : static_cast<size_t>(-1);
     if (need == static_cast<size_t>(-1))  // invalid description: report its exact error, launch nothing
         return pa_paged_attention_decode(q, k_cache, v_cache, block_table, seq_lens, desc, out, nullptr, 0,
                                          device_status, stream);

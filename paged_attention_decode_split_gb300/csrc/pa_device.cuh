@@ -64,12 +64,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Maximum of v over the 32 lanes of the warp (one instruction on sm_100+).
-__device__ __forceinline__ float warp_max(float v) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
 
 // Waits for the phase with the given parity to complete.  Returns false if
 // the poll limit ran out or *abort became non-zero (another thread gave up).

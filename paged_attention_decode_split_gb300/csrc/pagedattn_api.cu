@@ -35,8 +35,10 @@ struct Plan {
     int num_splits;
     int chunks_per_split;
     size_t ws_bytes;
-    size_t part_o_bytes;
+    size_t off_part_ml;  // workspace: split outputs [rows, S, D] fp32, then (max, sum) [rows, S] from here
 };
+
+inline size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -127,13 +129,11 @@ pa_status make_plan(const pa_attn_desc *d, bool verify, Plan *pl) {
     pl->num_sms = sms;
     pl->num_splits = splits;
     pl->chunks_per_split = cps;
+    pl->ws_bytes = pl->off_part_ml = 0;
     if (splits > 1) {
         const size_t rows = static_cast<size_t>(d->num_seqs) * d->q_len * d->num_q_heads;
-        pl->part_o_bytes = (rows * splits * d->head_dim * sizeof(float) + 255) & ~size_t(255);
-        pl->ws_bytes = pl->part_o_bytes + rows * splits * sizeof(float2);
-    } else {
-        pl->part_o_bytes = 0;
-        pl->ws_bytes = 0;
+        pl->off_part_ml = round256(rows * splits * d->head_dim * sizeof(float));
+        pl->ws_bytes = pl->off_part_ml + rows * splits * sizeof(float2);
     }
     return PA_OK;
 }
@@ -549,7 +549,7 @@ pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, c
     p.seq_lens = seq_lens;
     p.out = out;
     p.part_o = static_cast<float *>(workspace);
-    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.off_part_ml);
     p.status = device_status;
     p.num_pages = desc->num_pages;
     p.num_q_heads = desc->num_q_heads;
@@ -634,7 +634,7 @@ pa_status verify_call(const void *q, const void *k_cache, const void *v_cache, c
     p.seq_lens = seq_lens;
     p.out = out;
     p.part_o = static_cast<float *>(workspace);
-    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.off_part_ml);
     p.status = device_status;
     p.num_pages = desc->num_pages;
     p.num_q_heads = desc->num_q_heads;

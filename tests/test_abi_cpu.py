@@ -101,6 +101,13 @@ def test_decode_rejects_bad_pointers_and_workspace(lib):
     assert call(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, need, None, None) == pa.PA_ERR_INVALID_ARG
 
 
+def test_plan_info_layout_matches_header(lib):
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct {", text.index("What the last successful")):text.index("} pa_plan_info;")]
+    fields = re.findall(r"^\s*int32_t\s+(\w+);", body, flags=re.M)
+    assert fields == [name for name, _ in pa.PlanInfo._fields_]
+
+
 def test_desc_layout_matches_header(lib):
     # the binding's mirror of pa_attn_desc: same fields, same order, 64 bytes
     text = open(HEADER).read()
@@ -204,3 +211,22 @@ def test_verify_plan_stays_at_whole_waves(lib):
     dec = hybrid_desc(num_seqs=8, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=784,
                       max_pages_per_seq=11, max_seq_len=8208, num_pages=100)
     assert pa.workspace_bytes(dec) == ((8 * 32 * 3 * 128 * 4 + 255) // 256 * 256) + 8 * 32 * 3 * 8
+
+
+def test_noalloc_rejects_on_the_host(lib):
+    """The no-allocation decode answers like the ordinary decode for a
+    description that decode rejects (a verify-shaped q_len among them), and
+    rejects a plan larger than its built-in scratch, before touching a device."""
+    fn = lib.pa_paged_attention_decode_noalloc
+    fn.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    fn.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(pa.AttnDesc), vp, vp, vp]
+    verify_shaped = hybrid_desc(q_len=16)
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(verify_shaped), FAKE, None, None) == pa.PA_ERR_INVALID_ARG
+    bad = hybrid_desc(num_q_heads=25)
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(bad), FAKE, None, None) == pa.PA_ERR_INVALID_ARG
+    big = pa.make_desc(num_seqs=64, num_q_heads=24, num_kv_heads=4, head_dim=256, block_size=784,
+                       max_pages_per_seq=42, max_seq_len=32768, num_pages=64 * 42, scale=1 / 16, num_splits=64,
+                       num_sms=152)
+    assert pa.workspace_bytes(big) > pa.PA_NOALLOC_SCRATCH_BYTES
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(big), FAKE, None, None) == pa.PA_ERR_WORKSPACE

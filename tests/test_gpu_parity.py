@@ -181,8 +181,8 @@ def test_workspace_reused_across_descriptions(oracle_mod):
     probs = [hybrid(181, [4000, 2500, 300], 784), hybrid(182, [5000], 784),
              make_problem(183, num_seqs=2, seq_lens=[3000, 40], num_q_heads=32, num_kv_heads=8, head_dim=128,
                           block_size=16, scale=1 / math.sqrt(128)),
-             hybrid(184, [700, 20], 832, q_len=8)]
-    splits = [0, 37, 0, 3]
+             hybrid(184, [700, 20], 832, q_len=8), hybrid(185, [5000], 784), hybrid(186, [4000, 2500, 300], 784)]
+    splits = [0, 37, 0, 3, 9, 0]
     from tests.gpu_common import desc_for
     need = max(pa.workspace_bytes(desc_for(p, num_splits=k)) for p, k in zip(probs, splits))
     ws = torch.full((need,), 0xff, dtype=torch.uint8, device="cuda")  # NaN in every fp32 slot
