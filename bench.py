@@ -63,9 +63,11 @@ def load_peaks():
 
 
 def kernel_source_digest() -> str:
+    """Digest of the decode kernel's source (the headline instantiation's code,
+    not the launch table of the other shapes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_attention_decode_split_gb300", "csrc")
-    for name in ("pa_device.cuh", "decode_split.cuh", "decode_launch.cuh", "decode_launch.cu"):
+    for name in ("pa_device.cuh", "decode_split.cuh", "decode_mma.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -35,17 +35,23 @@ cudaError_t launch_decode_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, co
 // Per (head_dim, cache type): chunk streams (NST), stages per stream (SPS),
 // warps per chunk (DS, splitting the d range of P.V), a producer lane per
 // stream (LP).  Every layout keeps about 192 KiB of stages per SM in flight.
-//  * bf16, D = 256: 16 KiB stages; 2 streams x 6 stages, 2 warps per chunk
-//    (32K call 23.2 us, against 24.1 with 4 x 3 and 23.4 with 3 x 4; 12 and
-//    16 heads: 3 streams x 4 stages, so that 7 warps leave each warp the
-//    registers of 16 heads' Q fragments and accumulators).
-//  * bf16, D = 128 and fp8, D = 256: 8 KiB stages; 8 streams x 3 stages, a
-//    producer lane per stream (one issuing lane caps a CTA at about one
-//    stage per 0.3 us, which stages under 16 KiB feel).
-//  * fp8, D = 128: 4 KiB stages; 12 streams x 4 stages, a lane per stream.
-//  * 12 and 16 heads over fp8 take fewer warps (3 streams x 8 stages with 2
-//    warps per chunk at D = 256, 6 x 8 with one at D = 128) for the same
-//    register reason.
+// Chosen by measurement (32K context, one layer call in a 16-layer graph):
+//  * bf16, D = 256: 16 KiB stages; 2 streams x 6 stages, 2 warps per chunk,
+//    one producer lane (23.2 us against 24.1 with 4 x 3, 23.4 with 3 x 4 and
+//    25.2 with a lane per stream).  12 and 16 heads take the same layout
+//    (12 heads: 24.4 us against 25.1 with 3 x 4); fewer streams with more
+//    stages each kept more copies in flight per stream.
+//  * bf16, D = 128: 8 KiB stages; 4 streams x 6 stages, 2 warps per chunk, a
+//    producer lane per stream (one issuing lane caps a CTA at about one stage
+//    per 0.3 us, which stages under 16 KiB feel): 23.7 us against 24.7 with
+//    8 x 3 and one warp per chunk; 12 and 16 heads: 8 x 3, one warp.
+//  * fp8, D = 256: 8 KiB stages; 4 streams x 6 stages, one warp per chunk, a
+//    lane per stream (17.0 us against 17.2 with 8 x 3, 20.0 with 2 x 12).
+//    12 and 16 heads: 3 streams x 8 stages with 2 warps per chunk, so that
+//    7 warps leave each warp the registers of 16 heads' Q fragments and
+//    accumulators.
+//  * fp8, D = 128: 4 KiB stages; 12 streams x 4 stages, a lane per stream;
+//    12 and 16 heads: 6 x 8, one warp per chunk (registers, as above).
 template <bool WIN, bool F8>
 cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                               const DecodeParams &p, dim3 grid, cudaStream_t stream) {
@@ -68,15 +74,15 @@ cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, co
     return cudaErrorInvalidValue;
     if constexpr (F8) {
         if (head_dim == 256) {
-            PA_DECODE_CASES(256, 8, 3, 1, true, 3, 8, 2, slot0)
+            PA_DECODE_CASES(256, 4, 6, 1, true, 3, 8, 2, slot0)
         } else if (head_dim == 128) {
             PA_DECODE_CASES(128, 12, 4, 1, true, 6, 8, 1, slot0 + 10)
         }
     } else {
         if (head_dim == 256) {
-            PA_DECODE_CASES(256, 2, 6, 2, false, 3, 4, 2, slot0)
+            PA_DECODE_CASES(256, 2, 6, 2, false, 2, 6, 2, slot0)
         } else if (head_dim == 128) {
-            PA_DECODE_CASES(128, 8, 3, 1, true, 8, 3, 1, slot0 + 10)
+            PA_DECODE_CASES(128, 4, 6, 2, true, 8, 3, 1, slot0 + 10)
         }
     }
 #undef PA_DECODE_CASES
