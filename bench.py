@@ -211,17 +211,20 @@ def run_oracle_sample(layers, block_table, seq_lens, scale, budget_s: float):
 
 
 def bench_reference(args, world, rank):
-    """The oracle as the reference arm: one layer per step on the host cores."""
+    """The oracle as the reference arm: the same 16-layer step as our arm (one
+    oracle call per layer over that layer's cache), timed step by step on the
+    host cores within a time budget."""
     import torch
     from paged_attention_decode_split_gb300.inputs import WORKLOADS, make_problem
     if rank != 0:
         return
     spec = dict(WORKLOADS[WORKLOAD])
-    spec["num_layers"] = 1
+    spec["num_layers"] = args.layers
     prob = make_problem(1002, **spec)
-    layers = [(_bits(prob.q[0]), _bits(prob.k_cache[0]), _bits(prob.v_cache[0]))]
+    layers = [(_bits(prob.q[l]), _bits(prob.k_cache[l]), _bits(prob.v_cache[l])) for l in range(prob.num_layers)]
+    bt, sl = prob.block_table.numpy(), prob.seq_lens.numpy()
     L = int(prob.seq_lens[0])
-    bytes_layer = L * KV_BYTES_PER_TOKEN_LAYER
+    bytes_step = prob.num_layers * L * KV_BYTES_PER_TOKEN_LAYER
     import oracle
     oracle.build()
     threads = os.cpu_count() or 1
@@ -229,25 +232,24 @@ def bench_reference(args, world, rank):
     t_start = time.perf_counter()
     warm = max(3, args.warmup)
     for i in range(warm + args.steps):
-        q, kc, vc = layers[0]
         t0 = time.perf_counter()
-        oracle.paged_attention(q, kc, vc, prob.block_table.numpy(), prob.seq_lens.numpy(), prob.scale,
-                               num_threads=threads)
+        for q, kc, vc in layers:
+            oracle.paged_attention(q, kc, vc, bt, sl, prob.scale, num_threads=threads)
         dt = time.perf_counter() - t0
         if i >= warm:
             times.append(dt)
         if time.perf_counter() - t_start > args.reference_budget and times:
             break  # keep the reference arm within a few minutes
-    per_layer = sum(times) / len(times)
-    gbs = bytes_layer / per_layer / 1e9
-    sample = (f"one of the 16 layers per step (batch 1, 24 heads, context {L}, block 784), fp64 oracle; "
-              f"ms_per_step extrapolates x16 layers")
+    per_step = sum(times) / len(times)
+    gbs = bytes_step / per_step / 1e9
+    sample = (f"{len(times)} timed steps of all {prob.num_layers} layers (batch 1, 24 heads, context {L}, "
+              f"block 784), fp64 oracle on {threads} host threads, after {warm} warm-up steps")
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
-        "steps": len(times), "steps_requested": args.steps, "warmup": warm, "ms_per_step": per_layer * 16 * 1e3,
+        "steps": len(times), "steps_requested": args.steps, "warmup": warm, "ms_per_step": per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "layers_timed_per_step": 1, "context": L, "batch": 1,
-                   "block_size": 784, "q_heads": 24, "kv_heads": 4, "head_dim": 256},
+        "config": {"workload": WORKLOAD, "layers": prob.num_layers, "batch": 1, "context": L, "block_size": 784,
+                   "q_heads": 24, "kv_heads": 4, "head_dim": 256},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -59,12 +59,17 @@ def test_two_gloo_replicas(tmp_path):
 
 def test_reference_arm_line(tmp_path):
     """The reference arm (the oracle on the host cores) prints one JSON line
-    with the contract's keys, runs at least 3 warm-up steps and reports the
-    metric of the decode arm."""
+    with the contract's keys, runs at least 3 warm-up steps, reports the
+    metric of the decode arm, and times whole steps of every layer: its
+    ms_per_step times its steps fits inside the run's own wall time (here a
+    2-layer step keeps the CPU suite short)."""
     import subprocess
-    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1", "--warmup", "0",
-           "--reference-budget", "5"]
+    import time
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2", "--warmup", "0",
+           "--reference-budget", "5", "--layers", "2"]
+    t0 = time.perf_counter()
     res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    wall = time.perf_counter() - t0
     assert res.returncode == 0, res.stderr[-2000:]
     lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1
@@ -75,3 +80,8 @@ def test_reference_arm_line(tmp_path):
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
     assert rec["cpu_baseline"]["value"] == rec["value"]
     assert rec["e2e"] == {"value": rec["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert rec["config"]["layers"] == 2 and 1 <= rec["steps"] <= 2
+    assert (rec["steps"] + rec["warmup"]) * rec["ms_per_step"] * 1e-3 <= wall
+    # the value is the bytes of a whole step over the measured step time
+    bytes_step = 2 * 32768 * 4096
+    assert rec["value"] == pytest.approx(bytes_step / (rec["ms_per_step"] * 1e-3) / 1e9, rel=1e-9)
