@@ -21,7 +21,8 @@ layers' decode calls alone (no events inside the graphs, which would break
 the launch overlap between kernels).
 
 After the headline line's measurements, the other workloads of the pages are
-timed as graph replays (`workloads`): the 512-token case (L2-warm and
+timed as graph replays of attention calls with PA_FLAG_EARLY_KV_READ set (the
+graphs hold nothing that writes the caches) (`workloads`): the 512-token case (L2-warm and
 L2-flushed), the 11-depth context sweep for the hybrid and dense shapes with a
 fitted per-token slope and a flatness check, batch-32 decode, verify, a
 chunked-prefill step, sliding-window decode, 12-heads-per-KV-head decode and
@@ -471,6 +472,12 @@ def _time_graph(calls, stream, reps, warm=3):
     return e0.elapsed_time(e1) / reps
 
 
+# The suite's graphs hold attention calls only, so nothing still running
+# writes the block table, seq_lens or cached K/V ahead of a call: like the
+# headline step they set PA_FLAG_EARLY_KV_READ (1).
+SUITE_FLAGS = 1
+
+
 def _attention_calls(pa, prob, dev):
     """One decode (or verify) call per layer of the problem, with its buffers."""
     import torch
@@ -478,7 +485,7 @@ def _attention_calls(pa, prob, dev):
     desc = pa.make_desc(num_seqs=prob.num_seqs, q_len=prob.q_len, num_q_heads=prob.num_q_heads,
                         num_kv_heads=prob.num_kv_heads, head_dim=prob.head_dim, block_size=prob.block_size,
                         max_pages_per_seq=prob.max_pages_per_seq, max_seq_len=prob.max_seq_len,
-                        num_pages=prob.num_pages, scale=prob.scale)
+                        num_pages=prob.num_pages, scale=prob.scale, flags=SUITE_FLAGS)
     ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=dev)
     out = torch.empty((prob.num_seqs * prob.q_len, prob.num_q_heads, prob.head_dim), dtype=torch.float32,
                       device=dev)
@@ -537,7 +544,7 @@ def _fp8_decode(pa, dev, stream, peak, res, WORKLOADS, make_problem):
     bt, sl = prob.block_table.to(dev), prob.seq_lens.to(dev)
     desc = pa.make_desc(num_seqs=prob.num_seqs, num_q_heads=prob.num_q_heads, num_kv_heads=prob.num_kv_heads,
                         head_dim=prob.head_dim, block_size=prob.block_size, max_pages_per_seq=prob.max_pages_per_seq,
-                        max_seq_len=prob.max_seq_len, num_pages=prob.num_pages, scale=prob.scale)
+                        max_seq_len=prob.max_seq_len, num_pages=prob.num_pages, scale=prob.scale, flags=SUITE_FLAGS)
     import torch
     ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=dev)
     out = torch.empty((prob.num_seqs, prob.num_q_heads, prob.head_dim), dtype=torch.float32, device=dev)
@@ -560,7 +567,7 @@ def _verify_fp8(pa, dev, stream, peak, res, WORKLOADS, make_problem):
     desc = pa.make_desc(num_seqs=prob.num_seqs, q_len=prob.q_len, num_q_heads=prob.num_q_heads,
                         num_kv_heads=prob.num_kv_heads, head_dim=prob.head_dim, block_size=prob.block_size,
                         max_pages_per_seq=prob.max_pages_per_seq, max_seq_len=prob.max_seq_len,
-                        num_pages=prob.num_pages, scale=prob.scale)
+                        num_pages=prob.num_pages, scale=prob.scale, flags=SUITE_FLAGS)
     ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=dev)
     out = torch.empty((prob.num_seqs * prob.q_len, prob.num_q_heads, prob.head_dim), dtype=torch.float32, device=dev)
     calls = [(lambda l=l: pa.paged_attention_verify_fp8(prob.q[l], prob.k_cache[l], prob.v_cache[l], prob.k_scale[l],
@@ -684,7 +691,7 @@ def _window(pa, dev, stream, peak, res, WORKLOADS, make_problem):
     bt, sl = prob.block_table.to(dev), prob.seq_lens.to(dev)
     desc = pa.make_desc(num_seqs=1, num_q_heads=24, num_kv_heads=4, head_dim=256, block_size=784,
                         max_pages_per_seq=prob.max_pages_per_seq, max_seq_len=32768, num_pages=prob.num_pages,
-                        scale=1 / 16, window=2048)
+                        scale=1 / 16, window=2048, flags=SUITE_FLAGS)
     ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device=dev)
     out = torch.empty((1, 24, 256), dtype=torch.float32, device=dev)
     calls = [(lambda l=l: pa.paged_attention_decode(prob.q[l], prob.k_cache[l], prob.v_cache[l], bt, sl, desc,

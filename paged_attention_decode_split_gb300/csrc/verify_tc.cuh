@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
         if constexpr (F8) {
             uint32_t amax = 0;
             if ((int)threadIdx.x < R) {
-#pragma unroll 4
+#pragma unroll  // every load in flight at once: one global round trip
                 for (int v = 0; v < D / 8; ++v) {
                     const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 8 * v);
                     amax = max(max(amax, max(bf16x2_absmax(w.x), bf16x2_absmax(w.y))),
