@@ -6,9 +6,12 @@ paged-attention decode: batch 1, 24 query / 4 KV heads, head_dim 256, bf16
 N(0,1) data, context 32768, 784-token pages scattered at random through a
 pool 1.1x the context.  Every layer has its own 128 MiB cache (2 GiB per
 step, far larger than the 129 MB L2), so no L2 flush is needed between steps.
-The calls carry PA_FLAG_EARLY_KV_READ (the step satisfies its contract: only
-the new row is written ahead of each decode), which streams the old context
-ahead of each call's stream dependency and leaves the outputs bit-identical.
+Each layer is one pa_paged_attention_decode_append call, which does both in
+one kernel (the same result as the two calls; `step_two_calls_ms` times the
+step as two calls per layer).  The calls carry PA_FLAG_EARLY_KV_READ (the
+step satisfies its contract: only the new row is written ahead of each
+decode), which streams the old context ahead of each call's stream
+dependency and leaves the outputs bit-identical.
 
 `value` is whole-job KV-read GB/s (algorithmic bytes: 4096 B per context token
 per layer) with all inputs resident in HBM; the step runs as a CUDA graph and
@@ -290,6 +293,12 @@ def bench_gpu(args, world, rank, local):
     out = torch.empty((n_layers, B, 24, 256), dtype=torch.float32, device=dev)
 
     def layer_call(l):
+        # one call per layer: the new token's K/V appended (reshape_and_cache)
+        # and the decode that reads it, fused in one kernel
+        pa.paged_attention_decode_append(prob.q[l], k_new[l], v_new[l], prob.k_cache[l], prob.v_cache[l], bt, sl,
+                                         desc, out[l], ws, status=status)
+
+    def layer_two_calls(l):
         pa.reshape_and_cache(k_new[l], v_new[l], prob.k_cache[l], prob.v_cache[l], slots, status=status)
         pa.paged_attention_decode(prob.q[l], prob.k_cache[l], prob.v_cache[l], bt, sl, desc, out[l], ws,
                                   status=status)
@@ -302,11 +311,16 @@ def bench_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     plan = pa.last_plan()
 
-    # The step graph: 16 x (reshape_and_cache, decode split kernel, reduce).
+    # The step graph: 16 x (fused append + decode split kernel, reduce).
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for l in range(n_layers):
             layer_call(l)
+    # The same step as two calls per layer (reshape_and_cache, then decode).
+    graph2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph2, stream=stream):
+        for l in range(n_layers):
+            layer_two_calls(l)
     # The decode calls alone (same launches, no reshape) for the kernel's roofline.
     dec_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(dec_graph, stream=stream):
@@ -314,11 +328,12 @@ def bench_gpu(args, world, rank, local):
             pa.paged_attention_decode(prob.q[l], prob.k_cache[l], prob.v_cache[l], bt, sl, desc, out[l], ws,
                                       status=status)
     torch.cuda.synchronize()
-    launches_per_step = n_layers * (2 + (1 if plan["reduce_launched"] else 0))
+    launches_per_step = n_layers * (1 + (1 if plan["reduce_launched"] else 0))
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             graph.replay()
+            graph2.replay()
             dec_graph.replay()
     barrier(world)
 
@@ -340,6 +355,14 @@ def bench_gpu(args, world, rank, local):
             for k in range(dec_reps):
                 dec_graph.replay()
                 dec_events[k + 1].record()
+        torch.cuda.synchronize()
+        # the unfused step (reshape_and_cache and decode as two calls per layer)
+        two_events = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            two_events[0].record()
+            for k in range(dec_reps):
+                graph2.replay()
+            two_events[1].record()
         torch.cuda.synchronize()
         barrier(world)
     per_step_ms = [step_events[k].elapsed_time(step_events[k + 1]) for k in range(args.steps)]
@@ -381,10 +404,8 @@ def bench_gpu(args, world, rank, local):
     def e2e_step():
         in_dev.copy_(in_host, non_blocking=True)
         for l in range(n_layers):
-            pa.reshape_and_cache(kn_dev[l], vn_dev[l], prob.k_cache[l], prob.v_cache[l], slots_dev, status=status,
-                                 stream=sh)
-            pa.paged_attention_decode(q_dev[l], prob.k_cache[l], prob.v_cache[l], bt_dev, sl_dev, desc, out[l],
-                                      ws, status=status, stream=sh)
+            pa.paged_attention_decode_append(q_dev[l], kn_dev[l], vn_dev[l], prob.k_cache[l], prob.v_cache[l], bt_dev,
+                                             sl_dev, desc, out[l], ws, status=status, stream=sh)
         out_host.copy_(out, non_blocking=True)
 
     e2e_steps = max(5, min(args.steps, 200))
@@ -422,13 +443,18 @@ def bench_gpu(args, world, rank, local):
         "config": {"workload": WORKLOAD, "layers": n_layers, "batch": B, "context": L, "block_size": prob.block_size,
                    "q_heads": 24, "kv_heads": 4, "head_dim": 256, "num_pages_per_layer": prob.num_pages,
                    "l2": "no flush: 16 distinct 128 MiB layer caches (2 GiB per step) exceed the 129 MB L2",
-                   "parallelism": f"replicas x{world}", "plan": plan, "flags": "PA_FLAG_EARLY_KV_READ"},
+                   "parallelism": f"replicas x{world}", "plan": plan, "flags": "PA_FLAG_EARLY_KV_READ",
+                   "step": "per layer one pa_paged_attention_decode_append: the new token's K/V written into its "
+                           "slot (reshape_and_cache) and the split-KV decode, in one kernel, plus the reduce"},
         "us_per_call": ms_per_step * 1e3 / n_layers,
         "us_per_context_token": ms_per_step * 1e3 / L,
         "ms_per_step_range": [min(per_step_ms), statistics.median(per_step_ms), max(per_step_ms)],
         "decode_call_us": {"mean": avg_call_us, "min": min(call_us), "max": max(call_us),
                            "how": f"CUDA events around {dec_reps} replays of a graph of the {n_layers} layers' "
                                   "decode calls (split kernel + reduce), timed after the step region"},
+        "step_two_calls_ms": {"mean": two_events[0].elapsed_time(two_events[1]) / dec_reps,
+                              "how": "the same step with reshape_and_cache and decode as two calls per layer "
+                                     f"(graph of {n_layers} x 3 launches), CUDA events around {dec_reps} replays"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": load_traffic(),
                      "algorithmic_bytes_per_call": B * L * KV_BYTES_PER_TOKEN_LAYER,

@@ -201,6 +201,30 @@ pa_status pa_paged_attention_decode(const void *q, const void *k_cache, const vo
                                     const pa_attn_desc *desc, void *out, void *workspace,
                                     size_t workspace_bytes, int32_t *device_status, void *stream);
 
+/* paged_attention_decode_append -- the decode step's two calls in one kernel:
+ * reshape_and_cache of each sequence's new token, then paged_attention_decode.
+ * For every sequence b with L_b = seq_lens[b] >= 1, the new token is position
+ * L_b - 1; its rows k_new[b], v_new[b] are written into the cache slot of that
+ * position, (block_table[b, (L_b - 1) / BS], (L_b - 1) % BS) -- the address
+ * math of "DCU page832 attention", Sec.1 -- bit-exactly as pa_reshape_and_cache
+ * with that slot would, and the decode then reads them ("Qwen3.5-27B 6x faster
+ * on one RTX 3090": new K/V rows are copied into the cache before attention
+ * reads it).  The CTA whose split holds position L_b - 1 writes the rows before
+ * it copies the chunk that holds them, so the step needs no separate kernel.
+ * The result (output and caches) equals pa_reshape_and_cache followed by
+ * pa_paged_attention_decode on the same stream.
+ *   k_new, v_new  device bf16 [B, Hkv, D], 16-byte aligned; read after the
+ *                 stream dependency (PA_FLAG_EARLY_KV_READ does not cover them)
+ *   k_cache,
+ *   v_cache       written in place (the new rows) and read
+ * A position L_b - 1 whose page index lies outside [0, P) is not written
+ * (PA_DEV_BAD_PAGE, zero row, as for decode); L_b == 0 writes nothing.  Other
+ * arguments, results and errors as for pa_paged_attention_decode. */
+pa_status pa_paged_attention_decode_append(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                           void *v_cache, const int32_t *block_table, const int32_t *seq_lens,
+                                           const pa_attn_desc *desc, void *out, void *workspace,
+                                           size_t workspace_bytes, int32_t *device_status, void *stream);
+
 /* paged_attention_verify -- desc->q_len > 1 new rows per sequence, causal among
  * them (speculative verify: "Qwen3.8 on MI350P", Lektion 3, the verify rows
  * of one request sharing every K/V tile under a per-row causal mask).  Rows are ordered (sequence, new row): q and out
@@ -253,6 +277,16 @@ pa_status pa_paged_attention_decode_fp8(const void *q, const void *k_cache, cons
                                         const int32_t *block_table, const int32_t *seq_lens,
                                         const pa_attn_desc *desc, void *out, void *workspace,
                                         size_t workspace_bytes, int32_t *device_status, void *stream);
+
+/* paged_attention_decode_append over an fp8 cache: the new rows quantised as
+ * pa_reshape_and_cache_fp8 does (bit-exact), then the decode of
+ * pa_paged_attention_decode_fp8.  Arguments as for pa_paged_attention_decode_append
+ * plus the scales of pa_paged_attention_decode_fp8. */
+pa_status pa_paged_attention_decode_append_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                               void *v_cache, const float *k_scale, const float *v_scale,
+                                               const int32_t *block_table, const int32_t *seq_lens,
+                                               const pa_attn_desc *desc, void *out, void *workspace,
+                                               size_t workspace_bytes, int32_t *device_status, void *stream);
 
 /* paged_attention_verify over an fp8 cache: out as pa_paged_attention_verify
  * with K and V decoded as for pa_paged_attention_decode_fp8.  The tensor-core

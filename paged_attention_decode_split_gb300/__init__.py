@@ -7,7 +7,8 @@ in the library's CUDA kernels.  If the library is missing or cannot be loaded,
 every call raises -- there is no fallback.
 
 Names follow the C ABI: ``reshape_and_cache``, ``paged_attention_decode``,
-``paged_attention_verify``, ``workspace_bytes``, ``last_plan``.
+``paged_attention_decode_append``, ``paged_attention_verify``,
+``workspace_bytes``, ``last_plan``.
 """
 from __future__ import annotations
 
@@ -19,6 +20,7 @@ __all__ = [
     "AttnDesc", "PlanInfo", "PagedAttnError", "load_library", "make_desc", "workspace_bytes",
     "hybrid_page_tokens", "reshape_and_cache_fp8", "paged_attention_decode_fp8", "paged_attention_verify_fp8",
     "reshape_and_cache", "paged_attention_decode", "paged_attention_verify", "last_plan",
+    "paged_attention_decode_append", "paged_attention_decode_append_fp8",
     "status_string", "PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_WORKSPACE",
     "PA_ERR_CUDA", "PA_OUT_F32", "PA_OUT_BF16", "PA_DEV_BAD_SEQLEN", "PA_DEV_BAD_PAGE",
     "PA_DEV_BAD_SLOT", "PA_DEV_TIMEOUT", "PA_PATH_DECODE_CUDA_CORE", "PA_PATH_DECODE_MMA",
@@ -100,6 +102,13 @@ def load_library(path: str | None = None):
             fn.restype = ctypes.c_int
             fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc), _vp, _vp, ctypes.c_size_t,
                            _vp, _vp]
+        lib.pa_paged_attention_decode_append.restype = ctypes.c_int
+        lib.pa_paged_attention_decode_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc),
+                                                         _vp, _vp, ctypes.c_size_t, _vp, _vp]
+        lib.pa_paged_attention_decode_append_fp8.restype = ctypes.c_int
+        lib.pa_paged_attention_decode_append_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                                             ctypes.POINTER(AttnDesc), _vp, _vp, ctypes.c_size_t,
+                                                             _vp, _vp]
         lib.pa_paged_attention_decode_noalloc.restype = ctypes.c_int
         lib.pa_paged_attention_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc), _vp,
                                                           _vp, _vp]
@@ -188,6 +197,30 @@ def paged_attention_decode(q, k_cache, v_cache, block_table, seq_lens, desc: Att
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
         _ptr(workspace), ws, _ptr(status), _stream(stream))
     _check(rc, "pa_paged_attention_decode")
+
+
+def paged_attention_decode_append(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out,
+                                  workspace=None, status=None, stream=None) -> None:
+    """reshape_and_cache of each sequence's new token (rows k_new, v_new
+    [B, Hkv, D] bf16 into the slot of token seq_lens[b] - 1) fused with the
+    decode that reads it: one kernel, the same result as the two calls."""
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().pa_paged_attention_decode_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        ctypes.byref(desc), _ptr(out), _ptr(workspace), ws, _ptr(status), _stream(stream))
+    _check(rc, "pa_paged_attention_decode_append")
+
+
+def paged_attention_decode_append_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                                      desc: AttnDesc, out, workspace=None, status=None, stream=None) -> None:
+    """The fused append and decode over an e4m3 cache (the new rows quantised
+    as reshape_and_cache_fp8 does)."""
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().pa_paged_attention_decode_append_fp8(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out), _ptr(workspace), ws, _ptr(status),
+        _stream(stream))
+    _check(rc, "pa_paged_attention_decode_append_fp8")
 
 
 def paged_attention_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, status=None,

@@ -144,6 +144,41 @@ struct MmaCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
+// The fused append (pa_paged_attention_decode_append): the CTA whose split
+// holds token L - 1 of its sequence writes that token's K and V rows of its
+// KV head into the cache slot the block table gives for it, exactly as
+// reshape_and_cache would (bf16 copied; fp8 quantised like
+// reshape_and_cache_fp8), then makes the write visible to the copy engine
+// before the chunk that holds it is copied.  Called by the producer warp.
+template <int D, bool F8>
+__device__ __forceinline__ void append_new_row(const DecodeParams &p, int b, int kvh, int L, int c_begin, int n_my,
+                                               const int32_t *page_tab, int lp_first) {
+    const int t = L - 1;
+    if (t < 0 || t / kChunk < c_begin || t / kChunk >= c_begin + n_my) return;  // not this split's token
+    const int lane = threadIdx.x & 31;
+    const int lp = t / p.block_size;
+    const int page = page_tab ? page_tab[lp - lp_first] : p.block_table[(size_t)b * p.max_pages_per_seq + lp];
+    if (page >= 0 && (int64_t)page < p.num_pages) {  // (a bad page is flagged when its chunk is copied)
+        const int hkv = gridDim.y;
+        const size_t slot = (size_t)page * p.block_size + (t - lp * p.block_size);
+        const size_t row = slot * hkv + kvh;  // [P, BS, Hkv, D]
+        const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + ((size_t)b * hkv + kvh) * D);
+        const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + ((size_t)b * hkv + kvh) * D);
+        for (int j = lane; j < D / 8; j += 32) {  // 8 elements per lane and step
+            const uint4 kw = ks[j], vw = vs[j];
+            if constexpr (F8) {
+                reinterpret_cast<uint2 *>(p.k_cache + row * D)[j] = e4m3x8_div(kw, p.k_scale[kvh]);
+                reinterpret_cast<uint2 *>(p.v_cache + row * D)[j] = e4m3x8_div(vw, p.v_scale[kvh]);
+            } else {
+                reinterpret_cast<uint4 *>(p.k_cache + row * D * 2)[j] = kw;
+                reinterpret_cast<uint4 *>(p.v_cache + row * D * 2)[j] = vw;
+            }
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes before the TMA reads
+    }
+    __syncwarp();
+}
+
 template <int D, int G, int NT, int NST, int SPS, int DS, bool WIN, bool F8, bool LP>
 __global__ void __launch_bounds__((NST * DS + 1) * 32, 1)
     pa_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -229,51 +264,59 @@ __global__ void __launch_bounds__((NST * DS + 1) * 32, 1)
         // free; within a stream, chunks and stage phases go strictly in order.
         constexpr int PL = LP ? NST : 1, SPL = NST / PL;
         static_assert(NST % PL == 0, "streams spread evenly over the producer lanes");
-        if (lane < PL) {
-            const unsigned mask = PL == 32 ? 0xffffffffu : (1u << PL) - 1u;
-            auto any = [&](bool v) {
-                if constexpr (PL == 1)
-                    return v;
-                else
-                    return __any_sync(mask, v);
-            };
-            const uint64_t policy = l2_policy_evict_first();
-            auto issue = [&](int cs, int k) {  // chunk cs + k * NST into stream cs's stage k % SPS
-                const int i = cs + k * NST, s = cs * SPS + k % SPS;
-                const int t0 = (c_begin + i) * kChunk;
-                const int lp = t0 / p.block_size;
-                const int page = staged ? page_tab[lp - lp_first] : bt[lp];
-                if (page < 0 || (int64_t)page >= p.num_pages) {
-                    flags[1] = 1;  // the copy below reads zeros (box outside the tensor)
-                    set_status(p.status, PA_DEV_BAD_PAGE);
-                }
-                const int off = t0 - lp * p.block_size;
-                uint8_t *st = smem + s * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-                tma_load_5d(st, &tm_k, &full[s], 0, off, 0, kvh, page, policy);
-                tma_load_5d(st + C::CHUNK_BYTES, &tm_v, &full[s], 0, off, 0, kvh, page, policy);
-            };
-            int next[SPL];
-            int remaining = PL == 1 ? n_my : 0;
-#pragma unroll
-            for (int j = 0; j < SPL; ++j) {
-                next[j] = 0;
-                if constexpr (PL > 1) remaining += max(0, (n_my - lane - j * PL + NST - 1) / NST);
+        const unsigned mask = PL == 32 ? 0xffffffffu : (1u << PL) - 1u;
+        auto any = [&](bool v) {  // over the producer lanes
+            if constexpr (PL == 1)
+                return v;
+            else
+                return __any_sync(mask, v);
+        };
+        const uint64_t policy = l2_policy_evict_first();
+        auto issue = [&](int cs, int k) {  // chunk cs + k * NST into stream cs's stage k % SPS
+            const int i = cs + k * NST, s = cs * SPS + k % SPS;
+            const int t0 = (c_begin + i) * kChunk;
+            const int lp = t0 / p.block_size;
+            const int page = staged ? page_tab[lp - lp_first] : bt[lp];
+            if (page < 0 || (int64_t)page >= p.num_pages) {
+                flags[1] = 1;  // the copy below reads zeros (box outside the tensor)
+                set_status(p.status, PA_DEV_BAD_PAGE);
             }
-            if (p.early_kv) {
-                // first use of every stage: the chunks i < n_pre end before the
-                // new row (token L - 1); n_pre <= NS, so none waits for a stage
-                const int n_pre = max(0, min(min(NS, n_my), (L - 1) / kChunk - c_begin));
+            const int off = t0 - lp * p.block_size;
+            uint8_t *st = smem + s * C::STAGE_BYTES;
+            mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+            tma_load_5d(st, &tm_k, &full[s], 0, off, 0, kvh, page, policy);
+            tma_load_5d(st + C::CHUNK_BYTES, &tm_v, &full[s], 0, off, 0, kvh, page, policy);
+        };
+        int next[SPL];
+        int remaining = PL == 1 ? n_my : 0;
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) {
+            next[j] = 0;
+            if constexpr (PL > 1) remaining += max(0, (n_my - lane - j * PL + NST - 1) / NST);  // chunks c, c + NST, ...
+        }
+        if (p.early_kv) {
+            // First use of every stage: the chunks i < n_pre (those that end
+            // before the new row, token L - 1) go out before the dependency
+            // wait; chunk i is stream i % NST's (i / NST)-th, and n_pre <= NS,
+            // so none of them waits for a free stage.
+            const int n_pre = max(0, min(min(NS, n_my), (L - 1) / kChunk - c_begin));
+            if (lane < PL) {
 #pragma unroll 1
                 for (int i = lane; i < n_pre; i += PL) issue(i % NST, i / NST);
-#pragma unroll
-                for (int j = 0; j < SPL; ++j) {
-                    const int cs = lane + j * PL;
-                    next[j] = max(0, (n_pre - cs + NST - 1) / NST);
-                    remaining -= next[j];
-                }
-                pdl_wait_primary();
             }
+#pragma unroll
+            for (int j = 0; j < SPL; ++j) {
+                const int cs = lane + j * PL;
+                next[j] = max(0, (n_pre - cs + NST - 1) / NST);
+                remaining -= next[j];
+            }
+            pdl_wait_primary();
+        }
+        // Fused append: the new token's rows go into its cache slot before the
+        // chunk that holds them is copied (the whole warp; after the wait, as
+        // the rows may come from the work before this call).
+        if (p.k_new != nullptr) append_new_row<D, F8>(p, b, kvh, L, c_begin, n_my, staged ? page_tab : nullptr, lp_first);
+        if (lane < PL) {
             uint32_t idle = 0;
             bool gave_up = false;
             while (any(remaining > 0)) {

@@ -42,6 +42,13 @@ struct DecodeParams {
     int window;           // 0: full attention; W > 0: only the last W keys
     const float *k_scale; // fp8 cache: [Hkv] dequantisation scales of K and V
     const float *v_scale;
+    // Fused append (decode_append): the new token's rows [B, Hkv, D] bf16, written
+    // into the cache slot of token L_b - 1 before the chunk holding it is copied;
+    // nullptr for a plain decode.  k_cache / v_cache are the caches' base addresses.
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    uint8_t *k_cache;
+    uint8_t *v_cache;
 };
 
 __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int out_bf16) {

@@ -204,6 +204,20 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s) 
     return pack_f16(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xffff0000u) * s);
 }
 
+// Eight bf16 (one 16-byte vector) -> eight e4m3 codes of x / s: the division
+// in binary32, rounding to nearest even and saturating to +-448
+// (cvt ... satfinite); the quantiser of the fp8 cache.
+__device__ __forceinline__ uint32_t e4m3x2_div(uint32_t two_bf16, float s) {
+    const float lo = __fdiv_rn(bf16lo(two_bf16), s), hi = __fdiv_rn(bf16hi(two_bf16), s);
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint2 e4m3x8_div(uint4 w, float s) {
+    return make_uint2(e4m3x2_div(w.x, s) | (e4m3x2_div(w.y, s) << 16), e4m3x2_div(w.z, s) | (e4m3x2_div(w.w, s) << 16));
+}
+
 __device__ __forceinline__ void set_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
 }

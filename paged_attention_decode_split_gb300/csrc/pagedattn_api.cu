@@ -328,17 +328,6 @@ __global__ void __launch_bounds__(128) pa_reshape_and_cache_kernel(const uint4 *
 // fp8 variant: a thread turns 8 bf16 of a row into 8 e4m3 codes, code =
 // e4m3(x / scale[kv head]) with the division in binary32, rounding to nearest
 // even and saturating to +-448 (cvt ... satfinite).
-__device__ __forceinline__ uint32_t e4m3x2_div(uint32_t two_bf16, float s) {
-    const float lo = __fdiv_rn(bf16lo(two_bf16), s), hi = __fdiv_rn(bf16hi(two_bf16), s);
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ uint2 e4m3x8_div(uint4 w, float s) {
-    return make_uint2(e4m3x2_div(w.x, s) | (e4m3x2_div(w.y, s) << 16), e4m3x2_div(w.z, s) | (e4m3x2_div(w.w, s) << 16));
-}
-
 __global__ void __launch_bounds__(128) pa_reshape_and_cache_fp8_kernel(
     const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, uint2 *__restrict__ k_cache,
     uint2 *__restrict__ v_cache, const int64_t *__restrict__ slots, const float *__restrict__ k_scale,
@@ -366,7 +355,8 @@ __global__ void __launch_bounds__(128) pa_reshape_and_cache_fp8_kernel(
 pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
                       const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
                       const pa_attn_desc *desc, void *out, void *workspace, size_t workspace_bytes,
-                      int32_t *device_status, void *stream);
+                      int32_t *device_status, void *stream, const void *k_new = nullptr,
+                      const void *v_new = nullptr);
 pa_status verify_call(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
                       const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
                       const pa_attn_desc *desc, void *out, void *workspace, size_t workspace_bytes,
@@ -495,6 +485,27 @@ pa_status pa_paged_attention_decode_fp8(const void *q, const void *k_cache, cons
                        workspace_bytes, device_status, stream);
 }
 
+pa_status pa_paged_attention_decode_append(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                           void *v_cache, const int32_t *block_table, const int32_t *seq_lens,
+                                           const pa_attn_desc *desc, void *out, void *workspace,
+                                           size_t workspace_bytes, int32_t *device_status, void *stream) {
+    if (!k_new || !v_new) return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, nullptr, nullptr, block_table, seq_lens, desc, out, workspace,
+                       workspace_bytes, device_status, stream, k_new, v_new);
+}
+
+pa_status pa_paged_attention_decode_append_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                               void *v_cache, const float *k_scale, const float *v_scale,
+                                               const int32_t *block_table, const int32_t *seq_lens,
+                                               const pa_attn_desc *desc, void *out, void *workspace,
+                                               size_t workspace_bytes, int32_t *device_status, void *stream) {
+    if (!k_new || !v_new || !k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+        return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, desc, out, workspace,
+                       workspace_bytes, device_status, stream, k_new, v_new);
+}
+
 pa_status pa_paged_attention_verify(const void *q, const void *k_cache, const void *v_cache,
                                     const int32_t *block_table, const int32_t *seq_lens, const pa_attn_desc *desc,
                                     void *out, void *workspace, size_t workspace_bytes, int32_t *device_status,
@@ -519,17 +530,20 @@ pa_status pa_paged_attention_verify_fp8(const void *q, const void *k_cache, cons
 
 namespace pa {
 
-// Decode over a bf16 cache (k_scale == nullptr) or an fp8 e4m3 cache.
+// Decode over a bf16 cache (k_scale == nullptr) or an fp8 e4m3 cache; with
+// k_new / v_new, the fused append of each sequence's new token first.
 pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
                       const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
                       const pa_attn_desc *desc, void *out, void *workspace, size_t workspace_bytes,
-                      int32_t *device_status, void *stream) {
+                      int32_t *device_status, void *stream, const void *k_new, const void *v_new) {
     const bool fp8 = k_scale != nullptr;
     pa_status st = check_desc(desc, false);
     if (st != PA_OK) return st;
     if (desc->num_seqs == 0) return PA_OK;
     st = check_common_ptrs(q, k_cache, v_cache, block_table, seq_lens, out);
     if (st != PA_OK) return st;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID_ARG;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
     Plan pl;
     st = make_plan(desc, false, &pl);
     if (st != PA_OK) return st;
@@ -564,6 +578,10 @@ pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, c
     p.window = desc->window;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.k_cache = static_cast<uint8_t *>(const_cast<void *>(k_cache));
+    p.v_cache = static_cast<uint8_t *>(const_cast<void *>(v_cache));
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(pl.num_splits, desc->num_kv_heads, desc->num_seqs);
