@@ -11,8 +11,12 @@ template <int D, int G, int NST, int SPS, int DS, bool WIN, bool F8, bool LP>
 cudaError_t launch_decode_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, dim3 grid,
                                 cudaStream_t stream, int slot) {
     constexpr int NT = G > 8 ? 2 : 1;
+    // L2 prefetch ahead of the dependency wait: 6 chunks for the 8 KiB bf16
+    // stages of D = 128 (32K dense control: 23.4 -> 22.5 us); none elsewhere
+    // (hybrid bf16 within noise, fp8 slower, and more chunks slower for all)
+    constexpr int PF = (D == 128 && !F8) ? 6 : 0;
     using C = MmaCfg<D, NT, NST, SPS, DS, F8>;
-    auto kern = pa_decode_mma_kernel<D, G, NT, NST, SPS, DS, WIN, F8, LP>;
+    auto kern = pa_decode_mma_kernel<D, G, NT, NST, SPS, DS, WIN, F8, LP, PF>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, slot);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the kernel's set-up overlaps the previous

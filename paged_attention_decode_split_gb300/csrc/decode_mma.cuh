@@ -55,6 +55,7 @@
 #include "decode_split.cuh"
 
 namespace pa {
+
 namespace mm {
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -179,7 +180,9 @@ __device__ __forceinline__ void append_new_row(const DecodeParams &p, int b, int
     __syncwarp();
 }
 
-template <int D, int G, int NT, int NST, int SPS, int DS, bool WIN, bool F8, bool LP>
+// PF: chunks of old context a CTA prefetches into L2, beyond its stages, ahead
+// of the dependency wait (PA_FLAG_EARLY_KV_READ).
+template <int D, int G, int NT, int NST, int SPS, int DS, bool WIN, bool F8, bool LP, int PF = 0>
 __global__ void __launch_bounds__((NST * DS + 1) * 32, 1)
     pa_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const DecodeParams p) {
@@ -299,10 +302,25 @@ __global__ void __launch_bounds__((NST * DS + 1) * 32, 1)
             // before the new row, token L - 1) go out before the dependency
             // wait; chunk i is stream i % NST's (i / NST)-th, and n_pre <= NS,
             // so none of them waits for a free stage.
-            const int n_pre = max(0, min(min(NS, n_my), (L - 1) / kChunk - c_begin));
+            const int n_old = (L - 1) / kChunk - c_begin;  // chunks that end before the new row
+            const int n_pre = max(0, min(min(NS, n_my), n_old));
             if (lane < PL) {
 #pragma unroll 1
                 for (int i = lane; i < n_pre; i += PL) issue(i % NST, i / NST);
+            }
+            // The next chunks of old context go to L2 ahead of the wait as
+            // well, so the copies keep streaming while the work before this
+            // call finishes; the consumers then find them in L2.
+            const int n_l2 = max(0, min(min(n_pre + PF, n_my), n_old));
+            for (int i = n_pre + lane; i < n_l2; i += 32) {
+                const int t0 = (c_begin + i) * kChunk;
+                const int lp = t0 / p.block_size;
+                const int page = staged ? page_tab[lp - lp_first] : bt[lp];
+                if (page >= 0 && (int64_t)page < p.num_pages) {  // (a bad page is flagged when the chunk is copied)
+                    const int off = t0 - lp * p.block_size;
+                    tma_prefetch_l2_5d(&tm_k, 0, off, 0, kvh, page);
+                    tma_prefetch_l2_5d(&tm_v, 0, off, 0, kvh, page);
+                }
             }
 #pragma unroll
             for (int j = 0; j < SPL; ++j) {
