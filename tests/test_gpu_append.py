@@ -211,3 +211,13 @@ def test_append_graph_of_layers_equals_eager():
         res.append((out.cpu(), [c.cpu() for c in prob.k_cache]))
     assert torch.equal(res[0][0], res[1][0])
     assert all(torch.equal(a, b) for a, b in zip(res[0][1], res[1][1]))
+
+
+def test_append_hybrid_step_l32768_bs784_workload(oracle_mod):
+    """The benchmark's step layer in its benchmark launch (automatic plan,
+    PA_FLAG_EARLY_KV_READ): the 32K hybrid layer with its new token appended
+    and read by the fused call, against the oracle on the oracle-written cache."""
+    from paged_attention_decode_split_gb300.inputs import WORKLOADS
+    prob = make_problem(1002, **dict(WORKLOADS["hybrid_step_l32768_bs784_x16"], num_layers=1))
+    check(oracle_mod, prob, 77, flags=pa.PA_FLAG_EARLY_KV_READ)
+    assert pa.last_plan()["num_splits"] == 38
