@@ -26,7 +26,30 @@ cudaError_t launch_decode_fp8(int head_dim, int group, const CUtensorMap &tk, co
     return launch_decode_fp8_full(head_dim, group, tk, tv, p, grid, stream);
 }
 
-cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, cudaStream_t stream) {
+namespace {
+
+// The few-split merge with NSL register slots (>= S) and PPW pairs per warp.
+template <int D, int NSL, int PPW>
+cudaError_t launch_reduce_small_t(cudaLaunchConfig_t cfg, const ReduceParams &p, int pairs, int slot) {
+    auto kern = pa_split_reduce_small_kernel<D, NSL, PPW>;
+    const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(kern), kReduceSmallSmem, slot);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((pairs + 8 * PPW - 1) / (8 * PPW));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = kReduceSmallSmem;
+    return cudaLaunchKernelEx(&cfg, kern, p, pairs);
+}
+
+template <int D, int NSL>
+cudaError_t launch_reduce_small_n(cudaLaunchConfig_t cfg, const ReduceParams &p, int pairs, int ppw, int slot) {
+    if (ppw <= 1) return launch_reduce_small_t<D, NSL, 1>(cfg, p, pairs, slot);
+    if (ppw <= 2 || NSL * 4 > 16) return launch_reduce_small_t<D, NSL, 2>(cfg, p, pairs, slot + 1);
+    return launch_reduce_small_t<D, NSL, (NSL * 4 <= 16 ? 4 : 2)>(cfg, p, pairs, slot + 2);
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, int num_sms, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -36,11 +59,21 @@ cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, cudaStr
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.num_splits <= kReduceSmallMaxSplits) {
+        // pairs per warp: as few as keep the grid within one CTA per SM (up to 4)
         const int pairs = rows * p.num_q_heads;
-        cfg.gridDim = dim3((pairs + 7) / 8);
-        cfg.blockDim = dim3(256);
-        if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_split_reduce_small_kernel<256>, p, pairs);
-        if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_split_reduce_small_kernel<128>, p, pairs);
+        const int sms = num_sms > 0 ? num_sms : 1;
+        const int ppw = (pairs + 8 * sms - 1) / (8 * sms);
+        // kernel slots 110..127 for the 18 (head_dim, slots, pairs per warp) variants
+        if (head_dim == 256) {
+            if (p.num_splits <= 2) return launch_reduce_small_n<256, 2>(cfg, p, pairs, ppw, 110);
+            if (p.num_splits <= 4) return launch_reduce_small_n<256, 4>(cfg, p, pairs, ppw, 113);
+            return launch_reduce_small_n<256, 8>(cfg, p, pairs, ppw, 116);
+        }
+        if (head_dim == 128) {
+            if (p.num_splits <= 2) return launch_reduce_small_n<128, 2>(cfg, p, pairs, ppw, 119);
+            if (p.num_splits <= 4) return launch_reduce_small_n<128, 4>(cfg, p, pairs, ppw, 122);
+            return launch_reduce_small_n<128, 8>(cfg, p, pairs, ppw, 125);
+        }
         return cudaErrorInvalidValue;
     }
     cfg.gridDim = dim3(p.num_q_heads, rows, head_dim / 32);

@@ -155,61 +155,77 @@ __global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams
     }
 }
 
-// The same merge for few splits (S <= 8, e.g. verify, batched decode): one
-// warp per (row, head), a lane owning D/32 consecutive dims.  All S records
-// and partial vectors of a lane are loaded at once, so the kernel makes one
-// dependent round trip, and no CTA waits on a shared-memory exchange.
+// The same merge for few splits (S <= 8: verify, batched decode).  A warp
+// merges PPW (row, head) pairs, a lane owning D/32 consecutive dims of each;
+// every load of a warp is issued at once, so the kernel makes one dependent
+// round trip and needs no shared-memory exchange.  Its CTAs reserve more than
+// half of an SM's shared memory (kReduceSmallSmem, unused), so an SM holds at
+// most one of them and none beside a split CTA: they land on SMs as the split
+// CTAs leave, one per SM, and the grid is sized to about one CTA per SM.
+// Packed several to an SM, small CTAs of this kind queued on that SM's share
+// of L2 bandwidth while other SMs idled (the verify workload's 12.6 MB of
+// partials: 5.9 us with 4 CTAs on each of 96 SMs).
 constexpr int kReduceSmallMaxSplits = 8;
+constexpr int kReduceSmallSmem = 120 * 1024;
 
-template <int D>
-__global__ void __launch_bounds__(256) pa_split_reduce_small_kernel(const ReduceParams p, int pairs) {
+template <int D, int NSL, int PPW>
+__global__ void __launch_bounds__(256, 1) pa_split_reduce_small_kernel(const ReduceParams p, int pairs) {
+    static_assert(NSL <= kReduceSmallMaxSplits && NSL * PPW <= 16, "slots held in registers");
     constexpr int E = D / 32;  // dims per lane
     pdl_launch_dependents();   // a following attention call may start its set-up
     pdl_wait_primary();        // partials of the split kernel are complete and visible
-    const int pair = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (pair >= pairs) return;
+    const int pair0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * PPW, lane = threadIdx.x & 31;
+    if (pair0 >= pairs) return;
     const int S = p.num_splits;
-    const float2 *ml = p.part_ml + (size_t)pair * S;
-    const float *po = p.part_o + (size_t)pair * S * D + lane * E;
-    float2 v[kReduceSmallMaxSplits];
-    float4 o[kReduceSmallMaxSplits][E / 4];
+    float2 v[PPW][NSL];
+    float4 o[PPW][NSL][E / 4];
 #pragma unroll
-    for (int u = 0; u < kReduceSmallMaxSplits; ++u) {  // all loads first, none behind a branch
-        const int i = min(u, S - 1);
-        v[u] = ml[i];
+    for (int j = 0; j < PPW; ++j) {  // all loads first, none behind a branch
+        const int pair = min(pair0 + j, pairs - 1);
+        const float2 *ml = p.part_ml + (size_t)pair * S;
+        const float *po = p.part_o + (size_t)pair * S * D + lane * E;
 #pragma unroll
-        for (int e = 0; e < E / 4; ++e) o[u][e] = *reinterpret_cast<const float4 *>(po + (size_t)i * D + 4 * e);
+        for (int u = 0; u < NSL; ++u) {
+            const int i = min(u, S - 1);
+            v[j][u] = ml[i];
+#pragma unroll
+            for (int e = 0; e < E / 4; ++e) o[j][u][e] = *reinterpret_cast<const float4 *>(po + (size_t)i * D + 4 * e);
+        }
     }
-    float M = -INFINITY, W = 0.f;
-    float4 a[E / 4];
 #pragma unroll
-    for (int e = 0; e < E / 4; ++e) a[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    bool bad = false;
+    for (int j = 0; j < PPW; ++j) {
+        if (pair0 + j >= pairs) break;
+        float M = -INFINITY, W = 0.f;
+        float4 a[E / 4];
 #pragma unroll
-    for (int u = 0; u < kReduceSmallMaxSplits; ++u) {
-        if (u >= S) break;
-        bad |= v[u].y < 0.f;
-        if (!(v[u].y > 0.f)) continue;  // empty split (or poisoned, flagged above)
-        const float Mn = fmaxf(M, v[u].x);
-        const float c = fast_exp2(M - Mn), w = fast_exp2(v[u].x - Mn) * v[u].y;
-        W = fmaf(W, c, w);
+        for (int e = 0; e < E / 4; ++e) a[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool bad = false;
+#pragma unroll
+        for (int u = 0; u < NSL; ++u) {
+            if (u >= S) break;
+            bad |= v[j][u].y < 0.f;
+            if (!(v[j][u].y > 0.f)) continue;  // empty split (or poisoned, flagged above)
+            const float Mn = fmaxf(M, v[j][u].x);
+            const float c = fast_exp2(M - Mn), w = fast_exp2(v[j][u].x - Mn) * v[j][u].y;
+            W = fmaf(W, c, w);
+#pragma unroll
+            for (int e = 0; e < E / 4; ++e) {
+                a[e].x = fmaf(a[e].x, c, w * o[j][u][e].x);
+                a[e].y = fmaf(a[e].y, c, w * o[j][u][e].y);
+                a[e].z = fmaf(a[e].z, c, w * o[j][u][e].z);
+                a[e].w = fmaf(a[e].w, c, w * o[j][u][e].w);
+            }
+            M = Mn;
+        }
+        const float inv = (bad || !(W > 0.f)) ? 0.f : 1.f / W;
+        const size_t base = (size_t)(pair0 + j) * D + lane * E;
 #pragma unroll
         for (int e = 0; e < E / 4; ++e) {
-            a[e].x = fmaf(a[e].x, c, w * o[u][e].x);
-            a[e].y = fmaf(a[e].y, c, w * o[u][e].y);
-            a[e].z = fmaf(a[e].z, c, w * o[u][e].z);
-            a[e].w = fmaf(a[e].w, c, w * o[u][e].w);
+            store_out(p.out, base + 4 * e + 0, a[e].x * inv, p.out_bf16);
+            store_out(p.out, base + 4 * e + 1, a[e].y * inv, p.out_bf16);
+            store_out(p.out, base + 4 * e + 2, a[e].z * inv, p.out_bf16);
+            store_out(p.out, base + 4 * e + 3, a[e].w * inv, p.out_bf16);
         }
-        M = Mn;
-    }
-    const float inv = (bad || !(W > 0.f)) ? 0.f : 1.f / W;
-    const size_t base = (size_t)pair * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E / 4; ++e) {
-        store_out(p.out, base + 4 * e + 0, a[e].x * inv, p.out_bf16);
-        store_out(p.out, base + 4 * e + 1, a[e].y * inv, p.out_bf16);
-        store_out(p.out, base + 4 * e + 2, a[e].z * inv, p.out_bf16);
-        store_out(p.out, base + 4 * e + 3, a[e].w * inv, p.out_bf16);
     }
 }
 

@@ -227,6 +227,19 @@ __device__ __forceinline__ uint2 e4m3x8_div(uint4 w, float s) {
     return make_uint2(e4m3x2_div(w.x, s) | (e4m3x2_div(w.y, s) << 16), e4m3x2_div(w.z, s) | (e4m3x2_div(w.w, s) << 16));
 }
 
+// Bulk copy shared -> global of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned) in the calling thread's bulk group.
+__device__ __forceinline__ void bulk_store_s2g(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk copy of this thread has read its source
+// (the shared memory may then be reused; the writes complete before the grid
+// does).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 __device__ __forceinline__ void set_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
 }

@@ -21,7 +21,7 @@ cudaError_t launch_decode(int head_dim, int group, const CUtensorMap &tk, const 
                           const DecodeParams &p, dim3 grid, cudaStream_t stream);
 cudaError_t launch_decode_fp8(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                               const DecodeParams &p, dim3 grid, cudaStream_t stream);
-cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, cudaStream_t stream);
+cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, int num_sms, cudaStream_t stream);
 cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const CUtensorMap &tv,
                           const CUtensorMap &tk64, const CUtensorMap &tv64, const VerifyParams &p, dim3 grid,
                           cudaStream_t stream);

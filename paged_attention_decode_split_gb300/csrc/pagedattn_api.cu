@@ -596,7 +596,7 @@ pa_status decode_call(const void *q, const void *k_cache, const void *v_cache, c
         r.num_q_heads = desc->num_q_heads;
         r.num_splits = pl.num_splits;
         r.out_bf16 = p.out_bf16;
-        if (launch_reduce(desc->head_dim, r, desc->num_seqs, s) != cudaSuccess)
+        if (launch_reduce(desc->head_dim, r, desc->num_seqs, pl.num_sms, s) != cudaSuccess)
             return PA_ERR_CUDA;
     }
     record_plan(PA_PATH_DECODE_MMA, pl, desc, pl.num_splits * desc->num_kv_heads * desc->num_seqs);
@@ -685,7 +685,7 @@ pa_status verify_call(const void *q, const void *k_cache, const void *v_cache, c
         r.num_q_heads = desc->num_q_heads;
         r.num_splits = pl.num_splits;
         r.out_bf16 = p.out_bf16;
-        if (launch_reduce(desc->head_dim, r, desc->num_seqs * desc->q_len, s) != cudaSuccess)
+        if (launch_reduce(desc->head_dim, r, desc->num_seqs * desc->q_len, pl.num_sms, s) != cudaSuccess)
             return PA_ERR_CUDA;
     }
     record_plan(PA_PATH_VERIFY_TCGEN05, pl, desc, pl.num_splits * desc->num_kv_heads * row_blocks * desc->num_seqs);

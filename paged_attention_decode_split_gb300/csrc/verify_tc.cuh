@@ -247,6 +247,8 @@ struct VerifyTcCfg {
     static constexpr int S_COL = D;
     static constexpr int Q_COL = D + NSB * TT;
     static constexpr int CW = 2;                       // fp8: widening warps per tensor
+    static constexpr int SROW = D * 4 + 16;            // epilogue: output rows staged in the K/V rings
+    static_assert(M * SROW <= OFF_STG, "the staged output rows fit in the K/V rings");
     static constexpr int THREADS = (F8 ? 6 + 2 * CW : 6) * 32;
     static_assert(D == 256 || D == 128, "head_dim 256 or 128");
     static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor-memory columns");
@@ -324,6 +326,17 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_k64);
         prefetch_tensormap(&tm_v64);
+    }
+    // This row's q goes to L2 ahead of the dependency wait: L2 is where global
+    // memory is kept coherent, so a row the work before this call is still
+    // writing is read in its final state after the wait all the same.
+    const int rho_q = row0 + (int)threadIdx.x;  // the softmax threads' rows (rows past R are zero padding)
+    const __nv_bfloat16 *qrow =
+        p.q + (((size_t)b * p.q_len + rho_q / G) * p.num_q_heads + kvh * G + rho_q % G) * D;
+    if (warp < 4 && (int)threadIdx.x < R) {
+#pragma unroll
+        for (int o = 0; o < D * 2; o += 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(qrow) + o));
     }
     // Every global access waits for the work before this call on the stream,
     // except with early_kv: then the block table, seq_lens and the tiles that
@@ -448,38 +461,37 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
     // of two that brings its largest element into [2^14, 2^15) (f16_prescale).
     float q_pre = 1.f;
     if (warp < 4) {
-        const int rho = row0 + threadIdx.x;  // rows past R are zero padding
-        const __nv_bfloat16 *qrow =
-            p.q + (((size_t)b * p.q_len + rho / G) * p.num_q_heads + kvh * G + rho % G) * D;
-        if constexpr (F8) {
-            uint32_t amax = 0;
-            if ((int)threadIdx.x < R) {
-#pragma unroll  // every load in flight at once: one global round trip
-                for (int v = 0; v < D / 8; ++v) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 8 * v);
-                    amax = max(max(amax, max(bf16x2_absmax(w.x), bf16x2_absmax(w.y))),
-                               max(bf16x2_absmax(w.z), bf16x2_absmax(w.w)));
-                }
-            }
-            q_pre = f16_prescale(amax);
-        }
-#pragma unroll 1
-        for (int c0 = 0; c0 < D / 2; c0 += 64) {
-            uint32_t r[2][32];
+        // the whole row in one round of loads (D / 8 16-byte words), then
+        // tensor memory: column c holds elements 2c and 2c + 1
+        constexpr int NQ = D / 8;
+        uint4 qv[NQ];
+        const bool qlive = (int)threadIdx.x < R;
 #pragma unroll
-            for (int v = 0; v < 16; ++v) {
-                uint4 w = (int)threadIdx.x < R ? *reinterpret_cast<const uint4 *>(qrow + 2 * c0 + 8 * v)
-                                               : make_uint4(0u, 0u, 0u, 0u);
-                if constexpr (F8)  // the products run in f16: Q too
-                    w = make_uint4(bf16x2_to_f16x2_scaled(w.x, q_pre), bf16x2_to_f16x2_scaled(w.y, q_pre),
-                                   bf16x2_to_f16x2_scaled(w.z, q_pre), bf16x2_to_f16x2_scaled(w.w, q_pre));
-                r[v >> 3][4 * (v & 7)] = w.x;
-                r[v >> 3][4 * (v & 7) + 1] = w.y;
-                r[v >> 3][4 * (v & 7) + 2] = w.z;
-                r[v >> 3][4 * (v & 7) + 3] = w.w;
+        for (int v = 0; v < NQ; ++v)
+            qv[v] = qlive ? *reinterpret_cast<const uint4 *>(qrow + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (F8) {  // the products run in f16: Q too
+            uint32_t amax = 0;
+#pragma unroll
+            for (int v = 0; v < NQ; ++v)
+                amax = max(max(amax, max(bf16x2_absmax(qv[v].x), bf16x2_absmax(qv[v].y))),
+                           max(bf16x2_absmax(qv[v].z), bf16x2_absmax(qv[v].w)));
+            q_pre = f16_prescale(amax);
+#pragma unroll
+            for (int v = 0; v < NQ; ++v)
+                qv[v] = make_uint4(bf16x2_to_f16x2_scaled(qv[v].x, q_pre), bf16x2_to_f16x2_scaled(qv[v].y, q_pre),
+                                   bf16x2_to_f16x2_scaled(qv[v].z, q_pre), bf16x2_to_f16x2_scaled(qv[v].w, q_pre));
+        }
+#pragma unroll
+        for (int c = 0; c < NQ / 8; ++c) {
+            uint32_t r[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                r[4 * v] = qv[8 * c + v].x;
+                r[4 * v + 1] = qv[8 * c + v].y;
+                r[4 * v + 2] = qv[8 * c + v].z;
+                r[4 * v + 3] = qv[8 * c + v].w;
             }
-            tc::st32(lane_base + C::Q_COL + c0, r[0]);
-            if (c0 + 32 < D / 2) tc::st32(lane_base + C::Q_COL + c0 + 32, r[1]);
+            tc::st32(lane_base + C::Q_COL + 32 * c, r);
         }
         tc::wait_st();
         tc::fence_before();
@@ -796,27 +808,52 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
         const bool poisoned = !ok || flags[1] != 0;
         const float inv = (poisoned || !(l_sum > 0.f)) ? 0.f : (F8 ? p.v_scale[kvh] : 1.f) / l_sum;
         const size_t orow = live ? ((size_t)b * p.q_len + rho / G) * p.num_q_heads + kvh * G + rho % G : 0;
+        const bool direct = p.num_splits == 1;  // the final output, else this split's record
+        if (ok) {
+            // Every tile has been consumed by the tensor core, so the K/V rings
+            // are free: the row is staged there (rows SROW bytes apart, so the
+            // 16-byte stores of 8 consecutive rows fall in 8 different bank
+            // groups) and leaves with one bulk copy, instead of a warp's 32
+            // rows going out as 32 separate segments per store.
+            const bool bf = direct && p.out_bf16;
+            uint8_t *srow = smem + threadIdx.x * C::SROW;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 16) {
-            float ov[16];
-            if (ok) tc::ld16(lane_base + C::O_COL + c0, ov);  // ok is warp-uniform
-            if (live) {
+            for (int c0 = 0; c0 < D; c0 += 16) {
+                float ov[16];
+                tc::ld16(lane_base + C::O_COL + c0, ov);
 #pragma unroll
-                for (int c = 0; c < 16; c += 4) {
-                    const float4 v = ok ? make_float4(ov[c] * inv, ov[c + 1] * inv, ov[c + 2] * inv, ov[c + 3] * inv)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (p.num_splits == 1) {
-                        store_out(p.out, orow * D + c0 + c, v.x, p.out_bf16);
-                        store_out(p.out, orow * D + c0 + c + 1, v.y, p.out_bf16);
-                        store_out(p.out, orow * D + c0 + c + 2, v.z, p.out_bf16);
-                        store_out(p.out, orow * D + c0 + c + 3, v.w, p.out_bf16);
-                    } else {
-                        *reinterpret_cast<float4 *>(p.part_o + (orow * p.num_splits + split) * D + c0 + c) = v;
-                    }
+                for (int c = 0; c < 16; ++c) ov[c] *= inv;
+                if (bf) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) w[c] = pack_bf16(ov[2 * c], ov[2 * c + 1]);
+                    *reinterpret_cast<uint4 *>(srow + 2 * c0) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(srow + 2 * c0 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; c += 4)
+                        *reinterpret_cast<float4 *>(srow + 4 * (c0 + c)) = make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
                 }
             }
+            if (live) {
+                tc::fence_async_smem();  // the staged row is read by the copy engine
+                uint8_t *dst = direct ? static_cast<uint8_t *>(p.out) + orow * D * (bf ? 2 : 4)
+                                      : reinterpret_cast<uint8_t *>(p.part_o + (orow * p.num_splits + split) * D);
+                bulk_store_s2g(dst, srow, bf ? D * 2 : D * 4);
+                bulk_commit();
+                bulk_wait_read();  // the row has left shared memory before the CTA ends
+            }
+        } else if (live) {
+            // a wait was abandoned (copies may still land in the rings): zero the row with plain stores
+#pragma unroll 1
+            for (int c = 0; c < D; ++c) {
+                if (direct)
+                    store_out(p.out, orow * D + c, 0.f, p.out_bf16);
+                else
+                    p.part_o[(orow * p.num_splits + split) * D + c] = 0.f;
+            }
         }
-        if (live && p.num_splits > 1)
+        if (live && !direct)
             p.part_ml[orow * p.num_splits + split] = make_float2(m_ref, poisoned ? -1.f : l_sum);
     }
 

@@ -222,6 +222,8 @@ def test_noalloc_rejects_on_the_host(lib):
     vp = ctypes.c_void_p
     fn.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(pa.AttnDesc), vp, vp, vp]
     verify_shaped = hybrid_desc(q_len=16)
+    # its verify plan alone would be larger than the scratch; q_len is still what decides
+    assert pa.workspace_bytes(verify_shaped) > pa.PA_NOALLOC_SCRATCH_BYTES
     assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(verify_shaped), FAKE, None, None) == pa.PA_ERR_INVALID_ARG
     bad = hybrid_desc(num_q_heads=25)
     assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(bad), FAKE, None, None) == pa.PA_ERR_INVALID_ARG
