@@ -58,6 +58,16 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
         reinterpret_cast<float *>(out)[idx] = v;
 }
 
+// Four consecutive outputs from element idx (a multiple of 4): one 16-byte
+// (fp32) or 8-byte (bf16) store.
+__device__ __forceinline__ void store_out4(void *out, size_t idx, float4 v, int out_bf16) {
+    if (out_bf16)
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + idx) =
+            make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+    else
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + idx) = v;
+}
+
 // ---------------------------------------------------------------------------
 // Partition reduce: out[row, h, :] = sum_i w_i o_i / sum_i w_i with
 // w_i = l_i 2^(m_i - max_j m_j) over the non-empty splits of the row's sequence
@@ -156,7 +166,9 @@ __global__ void __launch_bounds__(128) pa_split_reduce_kernel(const ReduceParams
 }
 
 // The same merge for few splits (S <= 8: verify, batched decode).  A warp
-// merges PPW (row, head) pairs, a lane owning D/32 consecutive dims of each;
+// merges PPW (row, head) pairs, a lane owning the 4-dim columns lane,
+// lane + 32, ... of each (so a warp's load of one column set is 512
+// contiguous bytes, and its stores are 16-byte vectors);
 // every load of a warp is issued at once, so the kernel makes one dependent
 // round trip and needs no shared-memory exchange.  Its CTAs reserve more than
 // half of an SM's shared memory (kReduceSmallSmem, unused), so an SM holds at
@@ -183,13 +195,13 @@ __global__ void __launch_bounds__(256, 1) pa_split_reduce_small_kernel(const Red
     for (int j = 0; j < PPW; ++j) {  // all loads first, none behind a branch
         const int pair = min(pair0 + j, pairs - 1);
         const float2 *ml = p.part_ml + (size_t)pair * S;
-        const float *po = p.part_o + (size_t)pair * S * D + lane * E;
+        const float *po = p.part_o + (size_t)pair * S * D + 4 * lane;
 #pragma unroll
         for (int u = 0; u < NSL; ++u) {
             const int i = min(u, S - 1);
             v[j][u] = ml[i];
 #pragma unroll
-            for (int e = 0; e < E / 4; ++e) o[j][u][e] = *reinterpret_cast<const float4 *>(po + (size_t)i * D + 4 * e);
+            for (int e = 0; e < E / 4; ++e) o[j][u][e] = *reinterpret_cast<const float4 *>(po + (size_t)i * D + 128 * e);
         }
     }
 #pragma unroll
@@ -218,14 +230,11 @@ __global__ void __launch_bounds__(256, 1) pa_split_reduce_small_kernel(const Red
             M = Mn;
         }
         const float inv = (bad || !(W > 0.f)) ? 0.f : 1.f / W;
-        const size_t base = (size_t)(pair0 + j) * D + lane * E;
+        const size_t base = (size_t)(pair0 + j) * D + 4 * lane;
 #pragma unroll
-        for (int e = 0; e < E / 4; ++e) {
-            store_out(p.out, base + 4 * e + 0, a[e].x * inv, p.out_bf16);
-            store_out(p.out, base + 4 * e + 1, a[e].y * inv, p.out_bf16);
-            store_out(p.out, base + 4 * e + 2, a[e].z * inv, p.out_bf16);
-            store_out(p.out, base + 4 * e + 3, a[e].w * inv, p.out_bf16);
-        }
+        for (int e = 0; e < E / 4; ++e)
+            store_out4(p.out, base + 128 * e, make_float4(a[e].x * inv, a[e].y * inv, a[e].z * inv, a[e].w * inv),
+                       p.out_bf16);
     }
 }
 

@@ -818,21 +818,29 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
             const bool bf = direct && p.out_bf16;
             uint8_t *srow = smem + threadIdx.x * C::SROW;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 16) {
-                float ov[16];
-                tc::ld16(lane_base + C::O_COL + c0, ov);
+            for (int c1 = 0; c1 < D; c1 += 64) {
+                uint32_t r[4][16];  // 64 columns: four loads in flight, one wait
 #pragma unroll
-                for (int c = 0; c < 16; ++c) ov[c] *= inv;
-                if (bf) {
-                    uint32_t w[8];
+                for (int k = 0; k < 4; ++k) tc::ld16_nowait(lane_base + C::O_COL + c1 + 16 * k, r[k]);
+                tc::wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) w[c] = pack_bf16(ov[2 * c], ov[2 * c + 1]);
-                    *reinterpret_cast<uint4 *>(srow + 2 * c0) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4 *>(srow + 2 * c0 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-                } else {
+                for (int k = 0; k < 4; ++k) {
+                    const int c0 = c1 + 16 * k;
+                    float ov[16];
 #pragma unroll
-                    for (int c = 0; c < 16; c += 4)
-                        *reinterpret_cast<float4 *>(srow + 4 * (c0 + c)) = make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
+                    for (int c = 0; c < 16; ++c) ov[c] = __uint_as_float(r[k][c]) * inv;
+                    if (bf) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) w[c] = pack_bf16(ov[2 * c], ov[2 * c + 1]);
+                        *reinterpret_cast<uint4 *>(srow + 2 * c0) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4 *>(srow + 2 * c0 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 16; c += 4)
+                            *reinterpret_cast<float4 *>(srow + 4 * (c0 + c)) =
+                                make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
+                    }
                 }
             }
             if (live) {
