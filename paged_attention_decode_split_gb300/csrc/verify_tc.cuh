@@ -443,32 +443,43 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
         pdl_wait_primary();
     }
 
+    // Q rows: each softmax thread loads its row (D / 8 16-byte words, one
+    // round of loads) right after the dependency wait, so the loads are in
+    // flight while tensor memory is allocated.
+    constexpr int NQ = D / 8;
+    uint4 qv[NQ];
+    if (warp < 4) {
+        const bool qlive = (int)threadIdx.x < R;
+#pragma unroll
+        for (int v = 0; v < NQ; ++v)
+            qv[v] = qlive ? *reinterpret_cast<const uint4 *>(qrow + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+    }
     if (warp == 4) {
         tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
         tc::tmem_relinquish();
     }
     tc::fence_before();
-    __syncthreads();
+    // The tensor-memory address reaches the softmax and MMA warps (0-4).  With
+    // early_kv the other warps synchronised ahead of the wait (barriers, page
+    // table) and go on streaming; without it this is their synchronisation.
+    if (p.early_kv) {
+        if (warp < 5) named_bar_sync(2, 160);
+    } else {
+        __syncthreads();
+    }
     tc::fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = *tmem_slot;  // (read by warps 0-4 only on the early_kv path)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's tensor-memory lanes
 
     // Q block -> tensor memory, the A operand of S = Q K^T: row rho in lane
-    // rho, dims packed two per column; padding rows are zero.  The softmax
-    // warps store it while the producer already streams K and V; only the
-    // MMA warp waits for it (named barrier 1: warps 0-4).  Over an fp8 cache
-    // the products run in f16, and each row enters scaled by q_pre, the power
-    // of two that brings its largest element into [2^14, 2^15) (f16_prescale).
+    // rho, dims packed two per column (column c holds elements 2c and 2c + 1);
+    // padding rows are zero.  The softmax warps store it while the producer
+    // already streams K and V; only the MMA warp waits for it (named barrier
+    // 1: warps 0-4).  Over an fp8 cache the products run in f16, and each row
+    // enters scaled by q_pre, the power of two that brings its largest element
+    // into [2^14, 2^15) (f16_prescale).
     float q_pre = 1.f;
     if (warp < 4) {
-        // the whole row in one round of loads (D / 8 16-byte words), then
-        // tensor memory: column c holds elements 2c and 2c + 1
-        constexpr int NQ = D / 8;
-        uint4 qv[NQ];
-        const bool qlive = (int)threadIdx.x < R;
-#pragma unroll
-        for (int v = 0; v < NQ; ++v)
-            qv[v] = qlive ? *reinterpret_cast<const uint4 *>(qrow + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
         if constexpr (F8) {  // the products run in f16: Q too
             uint32_t amax = 0;
 #pragma unroll
