@@ -289,7 +289,11 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
 
     const int split = blockIdx.x, b = blockIdx.z;
     const int kvh = blockIdx.y % p.num_kv_heads;
-    const int row0 = (blockIdx.y / p.num_kv_heads) * C::M;  // first row (rho = r G + g) of this block
+    // Row blocks launch last-first: later blocks see more keys (causal), so the
+    // longest CTAs go out in the first wave and a partial last wave holds the
+    // shortest ones.
+    const int n_blocks = gridDim.y / p.num_kv_heads;
+    const int row0 = (n_blocks - 1 - (int)(blockIdx.y / p.num_kv_heads)) * C::M;  // first row (rho = r G + g)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group, R = min(C::M, p.q_len * G - row0);  // rows of this block
 
