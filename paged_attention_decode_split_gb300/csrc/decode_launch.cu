@@ -43,8 +43,13 @@ cudaError_t launch_reduce_small_t(cudaLaunchConfig_t cfg, const ReduceParams &p,
 template <int D, int NSL>
 cudaError_t launch_reduce_small_n(cudaLaunchConfig_t cfg, const ReduceParams &p, int pairs, int ppw, int slot) {
     if (ppw <= 1) return launch_reduce_small_t<D, NSL, 1>(cfg, p, pairs, slot);
-    if (ppw <= 2 || NSL * 4 > 16) return launch_reduce_small_t<D, NSL, 2>(cfg, p, pairs, slot + 1);
-    return launch_reduce_small_t<D, NSL, (NSL * 4 <= 16 ? 4 : 2)>(cfg, p, pairs, slot + 2);
+    if constexpr (NSL * 3 > 16) {  // 8 slots: at most 2 pairs per warp in registers
+        return launch_reduce_small_t<D, NSL, 2>(cfg, p, pairs, slot + 1);
+    } else {
+        if (ppw <= 2) return launch_reduce_small_t<D, NSL, 2>(cfg, p, pairs, slot + 1);
+        if (ppw <= 3) return launch_reduce_small_t<D, NSL, 3>(cfg, p, pairs, slot + 2);
+        return launch_reduce_small_t<D, NSL, 4>(cfg, p, pairs, slot + 3);
+    }
 }
 
 }  // namespace
@@ -63,16 +68,16 @@ cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, int num
         const int pairs = rows * p.num_q_heads;
         const int sms = num_sms > 0 ? num_sms : 1;
         const int ppw = (pairs + 8 * sms - 1) / (8 * sms);
-        // kernel slots 110..127 for the 18 (head_dim, slots, pairs per warp) variants
+        // kernel slots 110..133: four per (head_dim, split slots)
         if (head_dim == 256) {
             if (p.num_splits <= 2) return launch_reduce_small_n<256, 2>(cfg, p, pairs, ppw, 110);
-            if (p.num_splits <= 4) return launch_reduce_small_n<256, 4>(cfg, p, pairs, ppw, 113);
-            return launch_reduce_small_n<256, 8>(cfg, p, pairs, ppw, 116);
+            if (p.num_splits <= 4) return launch_reduce_small_n<256, 4>(cfg, p, pairs, ppw, 114);
+            return launch_reduce_small_n<256, 8>(cfg, p, pairs, ppw, 118);
         }
         if (head_dim == 128) {
-            if (p.num_splits <= 2) return launch_reduce_small_n<128, 2>(cfg, p, pairs, ppw, 119);
-            if (p.num_splits <= 4) return launch_reduce_small_n<128, 4>(cfg, p, pairs, ppw, 122);
-            return launch_reduce_small_n<128, 8>(cfg, p, pairs, ppw, 125);
+            if (p.num_splits <= 2) return launch_reduce_small_n<128, 2>(cfg, p, pairs, ppw, 122);
+            if (p.num_splits <= 4) return launch_reduce_small_n<128, 4>(cfg, p, pairs, ppw, 126);
+            return launch_reduce_small_n<128, 8>(cfg, p, pairs, ppw, 130);
         }
         return cudaErrorInvalidValue;
     }

@@ -25,7 +25,7 @@ namespace {
 constexpr int kMinChunksPerSplit = 2;   // 32 tokens
 constexpr int kMaxChunksPerSplit = 256; // 4096 tokens: bounds the longest CTA for load balance
 constexpr int kMaxDevices = 64;
-constexpr int kKernelSlots = 128;
+constexpr int kKernelSlots = 160;
 
 thread_local pa_plan_info g_last_plan;
 thread_local bool g_have_plan = false;
