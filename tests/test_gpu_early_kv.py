@@ -43,8 +43,13 @@ def call(prob, tensors, flags, num_splits=0):
     out = torch.full((prob.num_seqs * prob.q_len, prob.num_q_heads, prob.head_dim), float("nan"),
                      dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fn = pa.paged_attention_decode if prob.q_len == 1 else pa.paged_attention_verify
-    fn(q, kc, vc, bt, sl, desc, out, ws, status)
+    if prob.kv_fp8:
+        ks, vs = prob.k_scale[0].cuda(), prob.v_scale[0].cuda()
+        fn = pa.paged_attention_decode_fp8 if prob.q_len == 1 else pa.paged_attention_verify_fp8
+        fn(q, kc, vc, ks, vs, bt, sl, desc, out, ws, status)
+    else:
+        fn = pa.paged_attention_decode if prob.q_len == 1 else pa.paged_attention_verify
+        fn(q, kc, vc, bt, sl, desc, out, ws, status)
     return out, status
 
 
@@ -74,6 +79,21 @@ def test_verify_early_equals_default_bitwise(q_len, lens, bs):
     ref, _ = call(prob, t, 0)
     got, _ = call(prob, t, EARLY)
     torch.cuda.synchronize()
+    assert torch.equal(got.cpu(), ref.cpu())
+
+
+# Several 128-row blocks per KV head (40 rows x 6 heads = 240), one and three
+# splits, the bf16 and the fp8 cache: with early K/V reads only the softmax and
+# MMA warps synchronise on the tensor-memory address, the other warps stream on.
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_verify_row_blocks_early_equals_default_bitwise(fp8, splits):
+    prob = hybrid(321 + splits, [40, 900, 2100], 784, q_len=40, poison_unused=True, kv_fp8=fp8)
+    t = to_dev(prob)
+    ref, st0 = call(prob, t, 0, splits)
+    got, st1 = call(prob, t, EARLY, splits)
+    torch.cuda.synchronize()
+    assert st0.item() == 0 and st1.item() == 0
     assert torch.equal(got.cpu(), ref.cpu())
 
 
