@@ -58,9 +58,9 @@ def test_workspace_plan_hybrid_32k(lib):
 def test_workspace_plan_rules(lib):
     assert pa.workspace_bytes(hybrid_desc(num_splits=1)) == 0
     assert pa.workspace_bytes(hybrid_desc(num_splits=5)) == 24 * 5 * 256 * 4 + 24 * 5 * 8
-    # a 512-token context never splits below 2 chunks per split
+    # a 512-token context (32 chunks) never splits below 4 chunks per split: 8 splits
     small = hybrid_desc(block_size=16, max_pages_per_seq=32, max_seq_len=512, num_pages=64)
-    assert pa.workspace_bytes(small) == 24 * 16 * 256 * 4 + 24 * 16 * 8
+    assert pa.workspace_bytes(small) == 24 * 8 * 256 * 4 + 24 * 8 * 8
     # the plan depends only on the description
     assert pa.workspace_bytes(hybrid_desc()) == pa.workspace_bytes(hybrid_desc())
     # empty context / empty batch: nothing to split
