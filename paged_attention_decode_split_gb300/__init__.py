@@ -2,8 +2,10 @@
 
 A thin ctypes layer over ``libpagedattn.so`` (the C ABI of
 ``include/pagedattn.h``).  It only marshals arguments: torch tensors supply
-device pointers and the current CUDA stream; every step of the computation runs
-in the library's CUDA kernels.  If the library is missing or cannot be loaded,
+device pointers and the current CUDA stream (after their element types and
+shapes are checked against the attention description, since the C ABI cannot
+see a buffer's size); every step of the computation runs in the library's CUDA
+kernels.  If the library is missing or cannot be loaded,
 every call raises -- there is no fallback.
 
 Names follow the C ABI: ``reshape_and_cache``, ``paged_attention_decode``,
@@ -180,9 +182,65 @@ def _check(status: int, what: str) -> None:
         raise PagedAttnError(status, what)
 
 
+# The C ABI takes bare pointers and cannot tell a buffer's size or element
+# type, so a tensor of the wrong type or shape would be read or written past
+# its end.  The binding checks every tensor against the description before the
+# call (raw integer pointers pass through unchecked).
+def _expect(t, name: str, dtypes, shape=None) -> None:
+    if t is None or isinstance(t, int):
+        return
+    dts = dtypes if isinstance(dtypes, tuple) else (dtypes,)
+    if t.dtype not in dts:
+        raise ValueError(f"{name}: dtype {t.dtype}; expected {' or '.join(str(d) for d in dts)}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}; expected {tuple(shape)}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: a CUDA tensor is required (got {t.device})")
+
+
+def _fp8_cache_dtypes():
+    import torch
+    return (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def _check_attention(desc: AttnDesc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status,
+                     fp8: bool, k_scale=None, v_scale=None, k_new=None, v_new=None) -> None:
+    import torch
+    rows = desc.num_seqs * desc.q_len
+    cache = (desc.num_pages, desc.block_size, desc.num_kv_heads, desc.head_dim)
+    cache_dt = _fp8_cache_dtypes() if fp8 else torch.bfloat16
+    _expect(q, "q", torch.bfloat16, (rows, desc.num_q_heads, desc.head_dim))
+    _expect(k_cache, "k_cache", cache_dt, cache)
+    _expect(v_cache, "v_cache", cache_dt, cache)
+    _expect(block_table, "block_table", torch.int32, (desc.num_seqs, desc.max_pages_per_seq))
+    _expect(seq_lens, "seq_lens", torch.int32, (desc.num_seqs,))
+    _expect(out, "out", torch.bfloat16 if desc.out_dtype == PA_OUT_BF16 else torch.float32,
+            (rows, desc.num_q_heads, desc.head_dim))
+    if workspace is not None and not isinstance(workspace, int) and workspace.device.type != "cuda":
+        raise ValueError("workspace: a CUDA tensor is required")
+    _expect(status, "status", torch.int32)
+    _expect(k_scale, "k_scale", torch.float32, (desc.num_kv_heads,))
+    _expect(v_scale, "v_scale", torch.float32, (desc.num_kv_heads,))
+    _expect(k_new, "k_new", torch.bfloat16, (desc.num_seqs, desc.num_kv_heads, desc.head_dim))
+    _expect(v_new, "v_new", torch.bfloat16, (desc.num_seqs, desc.num_kv_heads, desc.head_dim))
+
+
+def _check_reshape(k_new, v_new, k_cache, v_cache, slot_mapping, status, fp8: bool) -> None:
+    import torch
+    n = int(slot_mapping.shape[0])
+    _, _, hkv, d = k_cache.shape
+    _expect(k_cache, "k_cache", _fp8_cache_dtypes() if fp8 else torch.bfloat16)
+    _expect(v_cache, "v_cache", _fp8_cache_dtypes() if fp8 else torch.bfloat16, tuple(k_cache.shape))
+    _expect(k_new, "k_new", torch.bfloat16, (n, hkv, d))
+    _expect(v_new, "v_new", torch.bfloat16, (n, hkv, d))
+    _expect(slot_mapping, "slot_mapping", torch.int64, (n,))
+    _expect(status, "status", torch.int32)
+
+
 def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, status=None, stream=None) -> None:
     """Write new K/V rows ([N, Hkv, D] bf16) into cache slots (int64 [N])."""
     num_pages, block_size, num_kv_heads, head_dim = k_cache.shape
+    _check_reshape(k_new, v_new, k_cache, v_cache, slot_mapping, status, fp8=False)
     rc = load_library().pa_reshape_and_cache(
         _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), int(slot_mapping.shape[0]),
         num_kv_heads, head_dim, block_size, num_pages, _ptr(status), _stream(stream))
@@ -192,6 +250,7 @@ def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, status=None,
 def paged_attention_decode(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, workspace=None,
                            status=None, stream=None) -> None:
     """out[b, h, :] = softmax(scale q K^T) V through the block table (q_len 1)."""
+    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=False)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().pa_paged_attention_decode(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
@@ -204,6 +263,8 @@ def paged_attention_decode_append(q, k_new, v_new, k_cache, v_cache, block_table
     """reshape_and_cache of each sequence's new token (rows k_new, v_new
     [B, Hkv, D] bf16 into the slot of token seq_lens[b] - 1) fused with the
     decode that reads it: one kernel, the same result as the two calls."""
+    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=False,
+                     k_new=k_new, v_new=v_new)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().pa_paged_attention_decode_append(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
@@ -215,6 +276,8 @@ def paged_attention_decode_append_fp8(q, k_new, v_new, k_cache, v_cache, k_scale
                                       desc: AttnDesc, out, workspace=None, status=None, stream=None) -> None:
     """The fused append and decode over an e4m3 cache (the new rows quantised
     as reshape_and_cache_fp8 does)."""
+    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=True,
+                     k_scale=k_scale, v_scale=v_scale, k_new=k_new, v_new=v_new)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().pa_paged_attention_decode_append_fp8(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
@@ -227,6 +290,7 @@ def paged_attention_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, d
                                    stream=None) -> None:
     """Decode without a workspace argument (split partials in the library's
     device scratch array; calls that overlap on the GPU must be ordered)."""
+    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, None, status, fp8=False)
     rc = load_library().pa_paged_attention_decode_noalloc(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
         _ptr(status), _stream(stream))
@@ -236,6 +300,7 @@ def paged_attention_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, d
 def paged_attention_verify(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, workspace=None,
                            status=None, stream=None) -> None:
     """q_len > 1 rows per sequence, causal among them; q/out are [B*q_len, Hq, D]."""
+    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=False)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().pa_paged_attention_verify(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
@@ -247,7 +312,11 @@ def reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale,
                           stream=None) -> None:
     """Quantise new K/V rows ([N, Hkv, D] bf16) into e4m3 cache slots (uint8
     caches [P, BS, Hkv, D]; float32 scales [Hkv])."""
+    import torch
     num_pages, block_size, num_kv_heads, head_dim = k_cache.shape
+    _check_reshape(k_new, v_new, k_cache, v_cache, slot_mapping, status, fp8=True)
+    _expect(k_scale, "k_scale", torch.float32, (num_kv_heads,))
+    _expect(v_scale, "v_scale", torch.float32, (num_kv_heads,))
     rc = load_library().pa_reshape_and_cache_fp8(
         _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), _ptr(k_scale), _ptr(v_scale),
         int(slot_mapping.shape[0]), num_kv_heads, head_dim, block_size, num_pages, _ptr(status), _stream(stream))
@@ -257,6 +326,8 @@ def reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale,
 def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, desc: AttnDesc, out,
                                workspace=None, status=None, stream=None) -> None:
     """Decode over an e4m3 cache: K = code x k_scale[kv head], V likewise."""
+    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=True,
+                     k_scale=k_scale, v_scale=v_scale)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().pa_paged_attention_decode_fp8(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
@@ -267,6 +338,8 @@ def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tabl
 def paged_attention_verify_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, desc: AttnDesc, out,
                                workspace=None, status=None, stream=None) -> None:
     """Verify (q_len > 1) over an e4m3 cache: K = code x k_scale[kv head], V likewise."""
+    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=True,
+                     k_scale=k_scale, v_scale=v_scale)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().pa_paged_attention_verify_fp8(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),

@@ -232,3 +232,44 @@ def test_noalloc_rejects_on_the_host(lib):
                        num_sms=152)
     assert pa.workspace_bytes(big) > pa.PA_NOALLOC_SCRATCH_BYTES
     assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(big), FAKE, None, None) == pa.PA_ERR_WORKSPACE
+
+
+def test_binding_checks_tensors_before_calling(lib):
+    """The C ABI cannot see a buffer's size, so the binding checks element
+    types and shapes against the description first: a uint8 (e4m3) cache handed
+    to a bf16 entry point, a cache of another geometry, or a host tensor is
+    refused with ValueError before anything is launched."""
+    import torch
+    desc = hybrid_desc(block_size=16, max_pages_per_seq=4, max_seq_len=64, num_pages=8)
+    q = torch.zeros((1, 24, 256), dtype=torch.bfloat16)
+    cache = torch.zeros((8, 16, 4, 256), dtype=torch.bfloat16)
+    codes = torch.zeros((8, 16, 4, 256), dtype=torch.uint8)
+    bt = torch.zeros((1, 4), dtype=torch.int32)
+    sl = torch.zeros((1,), dtype=torch.int32)
+    out = torch.zeros((1, 24, 256), dtype=torch.float32)
+    cases = [
+        dict(k_cache=codes, v_cache=codes),                       # fp8 codes in a bf16 call
+        dict(k_cache=torch.zeros((8, 16, 4, 128), dtype=torch.bfloat16)),  # another head_dim
+        dict(q=torch.zeros((2, 24, 256), dtype=torch.bfloat16)),  # more rows than the description
+        dict(out=torch.zeros((1, 24, 256), dtype=torch.bfloat16)),  # bf16 out for an fp32 description
+        dict(block_table=torch.zeros((1, 4), dtype=torch.int64)),
+        dict(seq_lens=torch.zeros((2,), dtype=torch.int32)),
+        dict(),                                                   # right types and shapes, but host tensors
+    ]
+    for bad in cases:
+        args = dict(q=q, k_cache=cache, v_cache=cache, block_table=bt, seq_lens=sl, out=out)
+        args.update(bad)
+        with pytest.raises(ValueError):
+            pa.paged_attention_decode(args["q"], args["k_cache"], args["v_cache"], args["block_table"],
+                                      args["seq_lens"], desc, args["out"])
+    # the fp8 entry point refuses a bf16 cache and wrongly shaped scales
+    scales = torch.ones((4,), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        pa.paged_attention_decode_fp8(q, cache, cache, scales, scales, bt, sl, desc, out)
+    with pytest.raises(ValueError):
+        pa.paged_attention_decode_fp8(q, codes, codes, torch.ones((3,)), scales, bt, sl, desc, out)
+    # reshape_and_cache: the new rows must match the cache's heads and dims
+    slots = torch.zeros((2,), dtype=torch.int64)
+    with pytest.raises(ValueError):
+        pa.reshape_and_cache(torch.zeros((2, 4, 128), dtype=torch.bfloat16),
+                             torch.zeros((2, 4, 128), dtype=torch.bfloat16), cache, cache, slots)
