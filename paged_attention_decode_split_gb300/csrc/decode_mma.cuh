@@ -52,6 +52,8 @@
 //    subnormal range 2^-38 below its largest element.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_split.cuh"
 
 namespace pa {
@@ -564,50 +566,65 @@ __global__ void __launch_bounds__((NST * DS + 1) * 32, 1)
         // A lane's V^T fragment holds tokens 2c, 2c + 1 (regs 0, 1) and 8 + 2c,
         // 9 + 2c (regs 2, 3); rows past the sequence end may hold anything
         // (NaN included) and are zeroed in a partial chunk.
-        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-        if (partial) {
-            mlo = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
-            mhi = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
-        }
-        if constexpr (!F8) {
-#pragma unroll
-            for (int mt = 0; mt < MTW; ++mt) {
-                const int gt = ds * MTW + mt;  // global m16 tile: dims 16 gt .. 16 gt + 15 = units 2 gt, 2 gt + 1
-                uint32_t a[4];
-                mm::ldsm_x4_t(a, vb + (gt >> 2) * C::BLOCK_BYTES + offB[gt & 3]);
-                a[0] &= mlo;
-                a[1] &= mlo;
-                a[2] &= mhi;
-                a[3] &= mhi;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    mm::mma<false>(oacc[mt][nt], a[0], a[1], a[2], a[3], bh[nt][0], bh[nt][1]);
-                    mm::mma<false>(oacc[mt][nt], a[0], a[1], a[2], a[3], bl[nt][0], bl[nt][1]);
-                }
+        // Over an fp8 cache, full chunks (all but a sequence's last and a
+        // window's first) skip the masking: two copies of the product, chosen
+        // once per chunk (fp8 32K call 16.55 -> 15.24 us; bf16 measured 1 %
+        // slower that way and keeps the single masked loop).
+        auto pv = [&](auto masked) {
+            constexpr bool MASK = decltype(masked)::value;
+            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+            if (MASK && partial) {
+                mlo = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
+                mhi = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
             }
-        } else {
+            if constexpr (!F8) {
 #pragma unroll
-            for (int mt = 0; mt < MTW; mt += 2) {
-                const int gt = ds * MTW + mt;  // unit gt = m16 tile gt (dims 16 gt ..), and gt + 1
-                uint32_t w[4];
-                mm::ldsm_x4_t(w, vb + (gt >> 3) * C::BLOCK_BYTES + offA[(gt & 7) >> 1]);
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    uint32_t a0, a2, a4, a6;
-                    mm::e4m3x4_f16(mm::prmt(w[2 * u], 0x3120u), a0, a2);      // tokens 2c, 2c+1: dims 2r, 2r+1
-                    mm::e4m3x4_f16(mm::prmt(w[2 * u + 1], 0x3120u), a4, a6);  // tokens 8+2c, 9+2c
-                    a0 &= mlo;
-                    a2 &= mlo;
-                    a4 &= mhi;
-                    a6 &= mhi;
+                for (int mt = 0; mt < MTW; ++mt) {
+                    const int gt = ds * MTW + mt;  // global m16 tile: dims 16 gt .. 16 gt + 15 = units 2 gt, 2 gt + 1
+                    uint32_t a[4];
+                    mm::ldsm_x4_t(a, vb + (gt >> 2) * C::BLOCK_BYTES + offB[gt & 3]);
+                    if constexpr (MASK) {
+                        a[0] &= mlo;
+                        a[1] &= mlo;
+                        a[2] &= mhi;
+                        a[3] &= mhi;
+                    }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        mm::mma<true>(oacc[mt + u][nt], a0, a2, a4, a6, bh[nt][0], bh[nt][1]);
-                        mm::mma<true>(oacc[mt + u][nt], a0, a2, a4, a6, bl[nt][0], bl[nt][1]);
+                        mm::mma<false>(oacc[mt][nt], a[0], a[1], a[2], a[3], bh[nt][0], bh[nt][1]);
+                        mm::mma<false>(oacc[mt][nt], a[0], a[1], a[2], a[3], bl[nt][0], bl[nt][1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < MTW; mt += 2) {
+                    const int gt = ds * MTW + mt;  // unit gt = m16 tile gt (dims 16 gt ..), and gt + 1
+                    uint32_t w[4];
+                    mm::ldsm_x4_t(w, vb + (gt >> 3) * C::BLOCK_BYTES + offA[(gt & 7) >> 1]);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        uint32_t a0, a2, a4, a6;
+                        mm::e4m3x4_f16(mm::prmt(w[2 * u], 0x3120u), a0, a2);      // tokens 2c, 2c+1: dims 2r, 2r+1
+                        mm::e4m3x4_f16(mm::prmt(w[2 * u + 1], 0x3120u), a4, a6);  // tokens 8+2c, 9+2c
+                        if constexpr (MASK) {
+                            a0 &= mlo;
+                            a2 &= mlo;
+                            a4 &= mhi;
+                            a6 &= mhi;
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mm::mma<true>(oacc[mt + u][nt], a0, a2, a4, a6, bh[nt][0], bh[nt][1]);
+                            mm::mma<true>(oacc[mt + u][nt], a0, a2, a4, a6, bl[nt][0], bl[nt][1]);
+                        }
                     }
                 }
             }
-        }
+        };
+        if (!F8 || partial)
+            pv(std::true_type{});
+        else
+            pv(std::false_type{});
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
