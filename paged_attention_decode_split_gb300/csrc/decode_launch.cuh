@@ -50,10 +50,12 @@ cudaError_t launch_decode_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, co
 //    per 0.3 us, which stages under 16 KiB feel): 23.7 us against 24.7 with
 //    8 x 3 and one warp per chunk; 12 and 16 heads: 8 x 3, one warp.
 //  * fp8, D = 256: 8 KiB stages; 4 streams x 6 stages, one warp per chunk, a
-//    lane per stream (17.0 us against 17.2 with 8 x 3, 20.0 with 2 x 12).
-//    12 and 16 heads: 3 streams x 8 stages with 2 warps per chunk, so that
-//    7 warps leave each warp the registers of 16 heads' Q fragments and
-//    accumulators.
+//    lane per stream (17.0 us against 17.2 with 8 x 3, 20.0 with 2 x 12;
+//    with the unmasked P.V of full chunks 15.25 us against 15.85 with 3 x 8,
+//    16.25 with 6 x 4, 17.4 with 8 x 3).  12 and 16 heads take the same layout
+//    (22.1 / 22.5 us against 23.2 / 23.1 with 3 x 8 x 2 and 27.1 / 28.5 with
+//    4 x 6 x 2), although their accumulators and Q fragments spill 20 / 76
+//    bytes at 255 registers.
 //  * fp8, D = 128: 4 KiB stages; 12 streams x 4 stages, a lane per stream;
 //    12 and 16 heads: 6 x 8, one warp per chunk (registers, as above).
 template <bool WIN, bool F8>
@@ -78,7 +80,7 @@ cudaError_t launch_decode_cfg(int head_dim, int group, const CUtensorMap &tk, co
     return cudaErrorInvalidValue;
     if constexpr (F8) {
         if (head_dim == 256) {
-            PA_DECODE_CASES(256, 4, 6, 1, true, 3, 8, 2, slot0)
+            PA_DECODE_CASES(256, 4, 6, 1, true, 4, 6, 1, slot0)
         } else if (head_dim == 128) {
             PA_DECODE_CASES(128, 12, 4, 1, true, 6, 8, 1, slot0 + 10)
         }
