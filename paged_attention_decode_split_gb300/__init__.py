@@ -1,12 +1,14 @@
 """Paged-attention split-KV decode for GB300 (sm_103a): Python binding.
 
-A thin ctypes layer over ``libpagedattn.so`` (the C ABI of
-``include/pagedattn.h``).  It only marshals arguments: torch tensors supply
-device pointers and the current CUDA stream (after their element types and
-shapes are checked against the attention description, since the C ABI cannot
-see a buffer's size); every step of the computation runs in the library's CUDA
-kernels.  If the library is missing or cannot be loaded,
-every call raises -- there is no fallback.
+A thin layer over ``libpagedattn.so`` (the C ABI of ``include/pagedattn.h``).
+It only marshals arguments; every step of the computation runs in the
+library's CUDA kernels.  The library is loaded with ctypes (descriptions, plan
+queries and the raw entry points); the tensor calls go through a small
+compiled module (``binding/pa_binding.cpp``) that checks each tensor's element
+type, shape, device and layout against the attention description -- the C ABI
+cannot see a buffer's size -- and passes its device pointer and the current
+CUDA stream to the C entry point.  If the library or the compiled module is
+missing or cannot be loaded, every call raises -- there is no fallback.
 
 Names follow the C ABI: ``reshape_and_cache``, ``paged_attention_decode``,
 ``paged_attention_decode_append``, ``paged_attention_verify``,
@@ -68,12 +70,40 @@ class PagedAttnError(RuntimeError):
 
 _lock = threading.Lock()
 _lib = None
+_bind = None
 _vp = ctypes.c_void_p
+
+# the C entry points the compiled module calls (it takes their addresses from
+# the library loaded here, so the process holds one copy of the library)
+_BOUND_ENTRIES = ("pa_paged_attention_decode", "pa_paged_attention_verify", "pa_paged_attention_decode_fp8",
+                  "pa_paged_attention_verify_fp8", "pa_paged_attention_decode_append",
+                  "pa_paged_attention_decode_append_fp8", "pa_paged_attention_decode_noalloc", "pa_reshape_and_cache",
+                  "pa_reshape_and_cache_fp8")
+
+
+def _load_binding(lib):
+    """Import the compiled tensor binding built beside the library and hand it
+    the library's entry points."""
+    import importlib.util
+    import sysconfig
+
+    import torch  # noqa: F401  (the module links against torch's libraries)
+    path = os.path.join(_PKG, "_build", "_pa_binding" + sysconfig.get_config_var("EXT_SUFFIX"))
+    if not os.path.exists(path):
+        raise RuntimeError(f"compiled binding not found at {path}; build it with "
+                           "`python -m paged_attention_decode_split_gb300._build`")
+    spec = importlib.util.spec_from_file_location("_pa_binding", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    for name in _BOUND_ENTRIES:
+        mod.set_entry(name, ctypes.cast(getattr(lib, name), ctypes.c_void_p).value)
+    return mod
 
 
 def load_library(path: str | None = None):
-    """Load libpagedattn.so (built by ``_build.build()``); raises if absent."""
-    global _lib
+    """Load libpagedattn.so and the compiled tensor binding (both built by
+    ``_build.build()``); raises if either is absent."""
+    global _lib, _bind
     if _lib is not None and path is None:
         return _lib
     with _lock:
@@ -118,6 +148,7 @@ def load_library(path: str | None = None):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(AttnDesc), _vp, _vp, ctypes.c_size_t, _vp, _vp]
+        _bind = _load_binding(lib)
         _lib = lib
         return lib
 
@@ -149,29 +180,11 @@ def hybrid_page_tokens(state_page_bytes: int, attn_bytes_per_token: int, alignme
     return int(n)
 
 
-def _ptr(t) -> int | None:
-    if t is None:
-        return None
-    if isinstance(t, int):
-        return t
-    assert t.is_contiguous(), "tensors passed to the library must be contiguous"
-    return t.data_ptr()
-
-
-def _current_stream_handle() -> int:
-    """The current CUDA stream of the current device as a raw handle.  The raw
-    query avoids building a torch.cuda.Stream object on every call (about 5 us
-    of host time); the public path is the fallback."""
-    import torch
-    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
-    if raw is not None:
-        return raw(torch.cuda.current_device())
-    return torch.cuda.current_stream().cuda_stream
-
-
-def _stream(stream) -> int | None:
+def _stream(stream) -> int:
+    """The stream handle the binding takes: -1 for the current CUDA stream
+    (read in C++), else the raw handle."""
     if stream is None:
-        return _current_stream_handle()
+        return -1
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
@@ -182,80 +195,26 @@ def _check(status: int, what: str) -> None:
         raise PagedAttnError(status, what)
 
 
-# The C ABI takes bare pointers and cannot tell a buffer's size or element
-# type, so a tensor of the wrong type or shape would be read or written past
-# its end.  The binding checks every tensor against the description before the
-# call (raw integer pointers pass through unchecked).
-def _expect(t, name: str, dtypes, shape=None) -> None:
-    if t is None or isinstance(t, int):
-        return
-    dts = dtypes if isinstance(dtypes, tuple) else (dtypes,)
-    if t.dtype not in dts:
-        raise ValueError(f"{name}: dtype {t.dtype}; expected {' or '.join(str(d) for d in dts)}")
-    if shape is not None and tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name}: shape {tuple(t.shape)}; expected {tuple(shape)}")
-    if t.device.type != "cuda":
-        raise ValueError(f"{name}: a CUDA tensor is required (got {t.device})")
+# Call kinds of the compiled binding's attention(); each maps to one C entry point.
+_DECODE, _DECODE_APPEND, _VERIFY, _DECODE_FP8, _DECODE_APPEND_FP8, _VERIFY_FP8, _DECODE_NOALLOC = range(7)
 
 
-def _fp8_cache_dtypes():
-    import torch
-    return (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
-
-
-def _check_attention(desc: AttnDesc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status,
-                     fp8: bool, k_scale=None, v_scale=None, k_new=None, v_new=None) -> None:
-    import torch
-    rows = desc.num_seqs * desc.q_len
-    cache = (desc.num_pages, desc.block_size, desc.num_kv_heads, desc.head_dim)
-    cache_dt = _fp8_cache_dtypes() if fp8 else torch.bfloat16
-    _expect(q, "q", torch.bfloat16, (rows, desc.num_q_heads, desc.head_dim))
-    _expect(k_cache, "k_cache", cache_dt, cache)
-    _expect(v_cache, "v_cache", cache_dt, cache)
-    _expect(block_table, "block_table", torch.int32, (desc.num_seqs, desc.max_pages_per_seq))
-    _expect(seq_lens, "seq_lens", torch.int32, (desc.num_seqs,))
-    _expect(out, "out", torch.bfloat16 if desc.out_dtype == PA_OUT_BF16 else torch.float32,
-            (rows, desc.num_q_heads, desc.head_dim))
-    if workspace is not None and not isinstance(workspace, int) and workspace.device.type != "cuda":
-        raise ValueError("workspace: a CUDA tensor is required")
-    _expect(status, "status", torch.int32)
-    _expect(k_scale, "k_scale", torch.float32, (desc.num_kv_heads,))
-    _expect(v_scale, "v_scale", torch.float32, (desc.num_kv_heads,))
-    _expect(k_new, "k_new", torch.bfloat16, (desc.num_seqs, desc.num_kv_heads, desc.head_dim))
-    _expect(v_new, "v_new", torch.bfloat16, (desc.num_seqs, desc.num_kv_heads, desc.head_dim))
-
-
-def _check_reshape(k_new, v_new, k_cache, v_cache, slot_mapping, status, fp8: bool) -> None:
-    import torch
-    n = int(slot_mapping.shape[0])
-    _, _, hkv, d = k_cache.shape
-    _expect(k_cache, "k_cache", _fp8_cache_dtypes() if fp8 else torch.bfloat16)
-    _expect(v_cache, "v_cache", _fp8_cache_dtypes() if fp8 else torch.bfloat16, tuple(k_cache.shape))
-    _expect(k_new, "k_new", torch.bfloat16, (n, hkv, d))
-    _expect(v_new, "v_new", torch.bfloat16, (n, hkv, d))
-    _expect(slot_mapping, "slot_mapping", torch.int64, (n,))
-    _expect(status, "status", torch.int32)
+def _bound():
+    return _bind if _bind is not None else (load_library(), _bind)[1]
 
 
 def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, status=None, stream=None) -> None:
     """Write new K/V rows ([N, Hkv, D] bf16) into cache slots (int64 [N])."""
-    num_pages, block_size, num_kv_heads, head_dim = k_cache.shape
-    _check_reshape(k_new, v_new, k_cache, v_cache, slot_mapping, status, fp8=False)
-    rc = load_library().pa_reshape_and_cache(
-        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), int(slot_mapping.shape[0]),
-        num_kv_heads, head_dim, block_size, num_pages, _ptr(status), _stream(stream))
-    _check(rc, "pa_reshape_and_cache")
+    _check(_bound().reshape(False, k_new, v_new, k_cache, v_cache, slot_mapping, None, None, status,
+                            _stream(stream)), "pa_reshape_and_cache")
 
 
 def paged_attention_decode(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, workspace=None,
                            status=None, stream=None) -> None:
     """out[b, h, :] = softmax(scale q K^T) V through the block table (q_len 1)."""
-    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=False)
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load_library().pa_paged_attention_decode(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
-        _ptr(workspace), ws, _ptr(status), _stream(stream))
-    _check(rc, "pa_paged_attention_decode")
+    _check(_bound().attention(_DECODE, q, k_cache, v_cache, None, None, None, None, block_table, seq_lens,
+                              ctypes.addressof(desc), out, workspace, status, _stream(stream)),
+           "pa_paged_attention_decode")
 
 
 def paged_attention_decode_append(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out,
@@ -263,88 +222,59 @@ def paged_attention_decode_append(q, k_new, v_new, k_cache, v_cache, block_table
     """reshape_and_cache of each sequence's new token (rows k_new, v_new
     [B, Hkv, D] bf16 into the slot of token seq_lens[b] - 1) fused with the
     decode that reads it: one kernel, the same result as the two calls."""
-    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=False,
-                     k_new=k_new, v_new=v_new)
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load_library().pa_paged_attention_decode_append(
-        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
-        ctypes.byref(desc), _ptr(out), _ptr(workspace), ws, _ptr(status), _stream(stream))
-    _check(rc, "pa_paged_attention_decode_append")
+    _check(_bound().attention(_DECODE_APPEND, q, k_cache, v_cache, None, None, k_new, v_new, block_table, seq_lens,
+                              ctypes.addressof(desc), out, workspace, status, _stream(stream)),
+           "pa_paged_attention_decode_append")
 
 
 def paged_attention_decode_append_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                                       desc: AttnDesc, out, workspace=None, status=None, stream=None) -> None:
     """The fused append and decode over an e4m3 cache (the new rows quantised
     as reshape_and_cache_fp8 does)."""
-    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=True,
-                     k_scale=k_scale, v_scale=v_scale, k_new=k_new, v_new=v_new)
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load_library().pa_paged_attention_decode_append_fp8(
-        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-        _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out), _ptr(workspace), ws, _ptr(status),
-        _stream(stream))
-    _check(rc, "pa_paged_attention_decode_append_fp8")
+    _check(_bound().attention(_DECODE_APPEND_FP8, q, k_cache, v_cache, k_scale, v_scale, k_new, v_new, block_table,
+                              seq_lens, ctypes.addressof(desc), out, workspace, status, _stream(stream)),
+           "pa_paged_attention_decode_append_fp8")
 
 
 def paged_attention_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, status=None,
                                    stream=None) -> None:
     """Decode without a workspace argument (split partials in the library's
     device scratch array; calls that overlap on the GPU must be ordered)."""
-    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, None, status, fp8=False)
-    rc = load_library().pa_paged_attention_decode_noalloc(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
-        _ptr(status), _stream(stream))
-    _check(rc, "pa_paged_attention_decode_noalloc")
+    _check(_bound().attention(_DECODE_NOALLOC, q, k_cache, v_cache, None, None, None, None, block_table, seq_lens,
+                              ctypes.addressof(desc), out, None, status, _stream(stream)),
+           "pa_paged_attention_decode_noalloc")
 
 
 def paged_attention_verify(q, k_cache, v_cache, block_table, seq_lens, desc: AttnDesc, out, workspace=None,
                            status=None, stream=None) -> None:
     """q_len > 1 rows per sequence, causal among them; q/out are [B*q_len, Hq, D]."""
-    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=False)
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load_library().pa_paged_attention_verify(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(desc), _ptr(out),
-        _ptr(workspace), ws, _ptr(status), _stream(stream))
-    _check(rc, "pa_paged_attention_verify")
+    _check(_bound().attention(_VERIFY, q, k_cache, v_cache, None, None, None, None, block_table, seq_lens,
+                              ctypes.addressof(desc), out, workspace, status, _stream(stream)),
+           "pa_paged_attention_verify")
 
 
 def reshape_and_cache_fp8(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale, v_scale, status=None,
                           stream=None) -> None:
     """Quantise new K/V rows ([N, Hkv, D] bf16) into e4m3 cache slots (uint8
     caches [P, BS, Hkv, D]; float32 scales [Hkv])."""
-    import torch
-    num_pages, block_size, num_kv_heads, head_dim = k_cache.shape
-    _check_reshape(k_new, v_new, k_cache, v_cache, slot_mapping, status, fp8=True)
-    _expect(k_scale, "k_scale", torch.float32, (num_kv_heads,))
-    _expect(v_scale, "v_scale", torch.float32, (num_kv_heads,))
-    rc = load_library().pa_reshape_and_cache_fp8(
-        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), _ptr(k_scale), _ptr(v_scale),
-        int(slot_mapping.shape[0]), num_kv_heads, head_dim, block_size, num_pages, _ptr(status), _stream(stream))
-    _check(rc, "pa_reshape_and_cache_fp8")
+    _check(_bound().reshape(True, k_new, v_new, k_cache, v_cache, slot_mapping, k_scale, v_scale, status,
+                            _stream(stream)), "pa_reshape_and_cache_fp8")
 
 
 def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, desc: AttnDesc, out,
                                workspace=None, status=None, stream=None) -> None:
     """Decode over an e4m3 cache: K = code x k_scale[kv head], V likewise."""
-    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=True,
-                     k_scale=k_scale, v_scale=v_scale)
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load_library().pa_paged_attention_decode_fp8(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
-        ctypes.byref(desc), _ptr(out), _ptr(workspace), ws, _ptr(status), _stream(stream))
-    _check(rc, "pa_paged_attention_decode_fp8")
+    _check(_bound().attention(_DECODE_FP8, q, k_cache, v_cache, k_scale, v_scale, None, None, block_table, seq_lens,
+                              ctypes.addressof(desc), out, workspace, status, _stream(stream)),
+           "pa_paged_attention_decode_fp8")
 
 
 def paged_attention_verify_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, desc: AttnDesc, out,
                                workspace=None, status=None, stream=None) -> None:
     """Verify (q_len > 1) over an e4m3 cache: K = code x k_scale[kv head], V likewise."""
-    _check_attention(desc, q, k_cache, v_cache, block_table, seq_lens, out, workspace, status, fp8=True,
-                     k_scale=k_scale, v_scale=v_scale)
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load_library().pa_paged_attention_verify_fp8(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
-        ctypes.byref(desc), _ptr(out), _ptr(workspace), ws, _ptr(status), _stream(stream))
-    _check(rc, "pa_paged_attention_verify_fp8")
+    _check(_bound().attention(_VERIFY_FP8, q, k_cache, v_cache, k_scale, v_scale, None, None, block_table, seq_lens,
+                              ctypes.addressof(desc), out, workspace, status, _stream(stream)),
+           "pa_paged_attention_verify_fp8")
 
 
 def last_plan() -> dict:

@@ -248,28 +248,48 @@ def test_binding_checks_tensors_before_calling(lib):
     sl = torch.zeros((1,), dtype=torch.int32)
     out = torch.zeros((1, 24, 256), dtype=torch.float32)
     cases = [
-        dict(k_cache=codes, v_cache=codes),                       # fp8 codes in a bf16 call
-        dict(k_cache=torch.zeros((8, 16, 4, 128), dtype=torch.bfloat16)),  # another head_dim
-        dict(q=torch.zeros((2, 24, 256), dtype=torch.bfloat16)),  # more rows than the description
-        dict(out=torch.zeros((1, 24, 256), dtype=torch.bfloat16)),  # bf16 out for an fp32 description
-        dict(block_table=torch.zeros((1, 4), dtype=torch.int64)),
-        dict(seq_lens=torch.zeros((2,), dtype=torch.int32)),
-        dict(),                                                   # right types and shapes, but host tensors
+        (dict(k_cache=codes, v_cache=codes), "k_cache: dtype"),  # fp8 codes in a bf16 call
+        (dict(k_cache=torch.zeros((8, 16, 4, 128), dtype=torch.bfloat16)), "k_cache: shape"),  # another head_dim
+        (dict(q=torch.zeros((2, 24, 256), dtype=torch.bfloat16)), "q: shape"),  # more rows than the description
+        (dict(out=torch.zeros((1, 24, 256), dtype=torch.bfloat16)), "out: dtype"),  # bf16 out, fp32 description
+        (dict(block_table=torch.zeros((1, 4), dtype=torch.int64)), "block_table: dtype"),
+        (dict(seq_lens=torch.zeros((2,), dtype=torch.int32)), "seq_lens: shape"),
+        (dict(status=torch.zeros((1,), dtype=torch.int64)), "status: dtype"),
+        (dict(), "q: a CUDA tensor is required"),  # right types and shapes, but host tensors
     ]
-    for bad in cases:
-        args = dict(q=q, k_cache=cache, v_cache=cache, block_table=bt, seq_lens=sl, out=out)
+    for bad, msg in cases:
+        args = dict(q=q, k_cache=cache, v_cache=cache, block_table=bt, seq_lens=sl, out=out, status=None)
         args.update(bad)
-        with pytest.raises(ValueError):
+        with pytest.raises(ValueError, match=msg):
             pa.paged_attention_decode(args["q"], args["k_cache"], args["v_cache"], args["block_table"],
-                                      args["seq_lens"], desc, args["out"])
-    # the fp8 entry point refuses a bf16 cache and wrongly shaped scales
+                                      args["seq_lens"], desc, args["out"], status=args["status"])
+    # every entry point checks before it calls
+    k_new = torch.zeros((1, 4, 256), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="k_new: shape"):
+        pa.paged_attention_decode_append(q, k_new[:, :2], k_new, cache, cache, bt, sl, desc, out)
+    with pytest.raises(ValueError, match="v_cache: dtype"):
+        pa.paged_attention_verify(q, cache, codes, bt, sl, desc, out)
+    with pytest.raises(ValueError, match="out: shape"):
+        pa.paged_attention_decode_noalloc(q, cache, cache, bt, sl, desc, out[:, :12])
+    # the fp8 entry points refuse a bf16 cache and wrongly shaped or missing scales
     scales = torch.ones((4,), dtype=torch.float32)
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="k_cache: dtype"):
         pa.paged_attention_decode_fp8(q, cache, cache, scales, scales, bt, sl, desc, out)
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="k_scale: shape"):
         pa.paged_attention_decode_fp8(q, codes, codes, torch.ones((3,)), scales, bt, sl, desc, out)
+    with pytest.raises(ValueError, match="v_scale"):
+        pa.paged_attention_verify_fp8(q, codes, codes, scales, None, bt, sl, desc, out)
+    with pytest.raises(ValueError, match="k_new: dtype"):
+        pa.paged_attention_decode_append_fp8(q, k_new.float(), k_new, codes, codes, scales, scales, bt, sl, desc, out)
     # reshape_and_cache: the new rows must match the cache's heads and dims
     slots = torch.zeros((2,), dtype=torch.int64)
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="k_new: shape"):
         pa.reshape_and_cache(torch.zeros((2, 4, 128), dtype=torch.bfloat16),
                              torch.zeros((2, 4, 128), dtype=torch.bfloat16), cache, cache, slots)
+    rows = torch.zeros((2, 4, 256), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="slot_mapping: dtype"):
+        pa.reshape_and_cache(rows, rows, cache, cache, slots.int())
+    with pytest.raises(ValueError, match="k_cache: dtype"):
+        pa.reshape_and_cache_fp8(rows, rows, cache, cache, slots, scales, scales)
+    with pytest.raises(ValueError, match="k_new: a CUDA tensor is required"):
+        pa.reshape_and_cache_fp8(rows, rows, codes, codes, slots, scales, scales)

@@ -5,6 +5,7 @@ likewise) within the bf16-path tolerance.  Edge cases: ties and saturation in
 the quantiser, NaN-poisoned unused slots, ragged tails, forced splits, every
 compiled group size, a sliding window, bf16 output, the early-K/V flag and the
 chain reshape_and_cache -> decode on one stream."""
+import ctypes
 import math
 
 import numpy as np
@@ -217,8 +218,13 @@ def test_decode_fp8_rejects_missing_scales():
     q, kc, vc, bt, sl = to_dev(prob)
     desc = desc_for(prob)
     out = torch.empty((1, 24, 256), device="cuda")
-    with pytest.raises(pa.PagedAttnError):
+    with pytest.raises(ValueError, match="k_scale, v_scale"):  # the binding refuses before the call
         pa.paged_attention_decode_fp8(q, kc, vc, None, None, bt, sl, desc, out)
+    ws = torch.empty(max(1, pa.workspace_bytes(desc)), dtype=torch.uint8, device="cuda")
+    rc = pa.load_library().pa_paged_attention_decode_fp8(  # and so does the C entry point
+        q.data_ptr(), kc.data_ptr(), vc.data_ptr(), None, None, bt.data_ptr(), sl.data_ptr(), ctypes.byref(desc),
+        out.data_ptr(), ws.data_ptr(), ws.numel(), None, torch.cuda.current_stream().cuda_stream)
+    assert rc == pa.PA_ERR_INVALID_ARG
 
 
 # -- verify over the fp8 cache (tcgen05, f16 products) --------------------------------
