@@ -22,9 +22,12 @@ cudaError_t launch_decode(int head_dim, int group, const CUtensorMap &tk, const 
 cudaError_t launch_decode_fp8(int head_dim, int group, const CUtensorMap &tk, const CUtensorMap &tv,
                               const DecodeParams &p, dim3 grid, cudaStream_t stream);
 cudaError_t launch_reduce(int head_dim, const ReduceParams &p, int rows, int num_sms, cudaStream_t stream);
+// Whether a bf16 verify of this shape runs 128-key score tiles (it then reads
+// K through tk128, whole 128-token tiles of one page).
+bool verify_wide_score_tiles(int head_dim, int rows);
 cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const CUtensorMap &tk64, const CUtensorMap &tv64, const VerifyParams &p, dim3 grid,
-                          cudaStream_t stream);
+                          const CUtensorMap &tk64, const CUtensorMap &tv64, const CUtensorMap &tk128,
+                          const VerifyParams &p, dim3 grid, cudaStream_t stream);
 
 cudaError_t launch_verify_fp8(int head_dim, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tk64,
                               const CUtensorMap &tv64, const VerifyParams &p, dim3 grid, cudaStream_t stream);

@@ -647,8 +647,13 @@ pa_status verify_call(const void *q, const void *k_cache, const void *v_cache, c
         tk64 = tk;  // never used: no 64-token tile fits in a smaller page
         tv64 = tv;
     }
-
     const int group = desc->num_q_heads / desc->num_kv_heads;
+    // 128-token K tiles of one page, for the verify shapes that run 128-key score tiles
+    CUtensorMap tk128 = tk64;
+    if (!fp8 && desc->block_size >= 128 && verify_wide_score_tiles(desc->head_dim, desc->q_len * group) &&
+        !encode_cache_map_blocks(&tk128, k_cache, desc, false, 128))
+        return PA_ERR_CUDA;
+
     VerifyParams p;
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.block_table = block_table;
@@ -678,7 +683,8 @@ pa_status verify_call(const void *q, const void *k_cache, const void *v_cache, c
     const int row_blocks = (desc->q_len * group + 127) / 128;
     const dim3 grid(pl.num_splits, desc->num_kv_heads * row_blocks, desc->num_seqs);
     const cudaError_t e = fp8 ? launch_verify_fp8(desc->head_dim, tk, tv, tk64, tv64, p, grid, s)
-                              : launch_verify(desc->head_dim, desc->q_len * group, tk, tv, tk64, tv64, p, grid, s);
+                              : launch_verify(desc->head_dim, desc->q_len * group, tk, tv, tk64, tv64, tk128, p,
+                                              grid, s);
     if (e != cudaSuccess) return PA_ERR_CUDA;
     if (pl.num_splits > 1) {
         ReduceParams r;

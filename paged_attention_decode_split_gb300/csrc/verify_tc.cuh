@@ -220,52 +220,70 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
 }  // namespace tc
 
 // NSB: S/P tensor-memory buffers (the Q K^T products run up to NSB tiles ahead
-// of P V).
-template <int D, int NK, int NV, int NSG = 0, int NSB = 2>
+// of P V).  TK: keys per score tile, 64 or 128.  With 128 the score product
+// S = Q K^T is M = 128 x N = 128: half as many MMA instructions per key as with
+// N = 64, whose instruction rate bounds the tile when the tiles come from L2
+// (many row blocks per KV head, chunked prefill).  Two 128-column S/P buffers
+// and O fill tensor memory, so Q moves to shared memory as the product's A
+// operand (QSM), the K ring holds one 128-key tile and P V runs over two
+// 64-key V tiles per score tile.
+template <int D, int NK, int NV, int NSG = 0, int NSB = 2, int TK = 64>
 struct VerifyTcCfg {
     static constexpr bool F8 = NSG > 0;                // fp8 cache: e4m3 staging ring of NSG slots per tensor
+    static constexpr bool QSM = TK == 128;             // Q in shared memory
     static constexpr int M = 128;                      // MMA rows (query rows, zero padded)
-    static constexpr int TT = 64;                      // tokens per tile (4 TMA chunks)
-    static constexpr int CPT = TT / kChunk;            // chunks per tile
+    static constexpr int TT = 64;                      // tokens per V tile (4 TMA chunks)
+    static constexpr int CPT = TT / kChunk;            // chunks per V tile
+    static constexpr int CPK = TK / kChunk;            // chunks per K (score) tile
+    static constexpr int VPK = TK / TT;                // V tiles per score tile
     static constexpr int DB = D / 64;                  // 128-byte column blocks
-    static constexpr int TILE_BYTES = TT * D * 2;      // K or V of one tile (bf16 or f16)
+    static constexpr int TILE_BYTES = TT * D * 2;      // V of one tile (bf16 or f16)
+    static constexpr int KTILE_BYTES = TK * D * 2;     // K of one score tile
     static constexpr int KVB = F8 ? 1 : 2;             // bytes per cached element
     static constexpr int CHUNK_BYTES = kChunk * D * KVB;  // one TMA chunk as copied
     static constexpr int STG_BYTES = TT * D;           // one e4m3 tile, [D/128][64 tokens][128 B] swizzled
-    static constexpr int OFF_V = NK * TILE_BYTES;       // K ring, then V ring
+    static constexpr int OFF_V = NK * KTILE_BYTES;      // K ring, then V ring
     static constexpr int OFF_STG = OFF_V + NV * TILE_BYTES;  // K staging, then V staging
-    static constexpr int OFF_BAR = OFF_STG + 2 * NSG * STG_BYTES;
+    static constexpr int OFF_Q = OFF_STG + 2 * NSG * STG_BYTES;  // QSM: Q as [D/64][M rows][128 B], swizzled
+    static constexpr int Q_BYTES = QSM ? M * D * 2 : 0;
+    static constexpr int OFF_BAR = OFF_Q + Q_BYTES;
     // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[NSB], p_full[NSB], o_done[NSB], mma_fin,
     // then (fp8) kst_full[NSG], kst_empty[NSG], vst_full[NSG], vst_empty[NSG]
     static constexpr int OFF_TMEM = OFF_BAR + (2 * NK + 2 * NV + 3 * NSB + 1 + 4 * NSG) * 8;
     static constexpr int OFF_FLAGS = OFF_TMEM + 16;
     static constexpr int OFF_PT = OFF_FLAGS + 16;                    // the split's block-table entries
     static constexpr int SMEM_BYTES = OFF_PT + kVerifyPageTab * 4 + 1024;
-    // tensor-memory columns: O (fp32, D), NSB S/P buffers (64 each), Q (bf16 pairs, D / 2)
+    // tensor-memory columns: O (fp32, D), NSB S/P buffers (TK each), Q (bf16
+    // pairs, D / 2; not with QSM).  P of a score tile is written over its S
+    // buffer, per 64-key half: a bf16 head in 32 columns, then the residual in 32.
     static constexpr int TMEM_COLS = 512;
     static constexpr int O_COL = 0;
     static constexpr int S_COL = D;
-    static constexpr int Q_COL = D + NSB * TT;
+    static constexpr int Q_COL = D + NSB * TK;
+    static constexpr int Q_TCOLS = QSM ? 0 : D / 2;
+    static constexpr int SBUF(int j) { return S_COL + j * TK; }
     static constexpr int CW = 2;                       // fp8: widening warps per tensor
     static constexpr int SROW = D * 4 + 16;            // epilogue: output rows staged in the K/V rings
     static_assert(M * SROW <= OFF_STG, "the staged output rows fit in the K/V rings");
     static constexpr int THREADS = (F8 ? 6 + 2 * CW : 6) * 32;
     static_assert(D == 256 || D == 128, "head_dim 256 or 128");
-    static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor-memory columns");
+    static_assert(Q_COL + Q_TCOLS <= TMEM_COLS, "tensor-memory columns");
+    static_assert(TK == 64 || (TK == 128 && !F8), "128-key score tiles: bf16 cache only");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
 // NSG > 0: fp8 cache (tm_k / tm_v: e4m3 boxes of 128 codes x 16 tokens,
 // tm_k64 / tm_v64: 5-D boxes of a whole 64-token tile, both with the 128-byte
 // swizzle).
-template <int D, int NK, int NV, int NSG, int NSB>
-__global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
+// tm_k64: 5-D boxes of a whole K tile of TK keys (64, or 128 with TK = 128).
+template <int D, int NK, int NV, int NSG, int NSB, int TK = 64>
+__global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB, TK>::THREADS, 1)
     pa_verify_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
                         const VerifyParams p) {
-    using C = VerifyTcCfg<D, NK, NV, NSG, NSB>;
-    constexpr bool F8 = C::F8;
-    constexpr int TT = C::TT, CPT = C::CPT;
+    using C = VerifyTcCfg<D, NK, NV, NSG, NSB, TK>;
+    constexpr bool F8 = C::F8, QSM = C::QSM;
+    constexpr int TT = C::TT, CPT = C::CPT, CPK = C::CPK, VPK = C::VPK;
     constexpr float kLazy = 8.f;  // raise the reference max only when it grows by more than 2^8
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -380,7 +398,8 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
         }
         return;
     }
-    const int n_tiles = (n_my + CPT - 1) / CPT;
+    const int n_tiles = (n_my + CPK - 1) / CPK;   // score tiles (K tiles)
+    const int n_vtiles = (n_my + CPT - 1) / CPT;  // V tiles (VPK per score tile)
 
     // The split's block-table entries, staged in shared memory by all threads
     // (visible to the producer after the next __syncthreads); splits spanning
@@ -392,11 +411,11 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
     if (staged)
         for (int j = threadIdx.x; j < n_pt; j += C::THREADS) page_tab[j] = bt[lp_first + j];
 
-    // TMA copies of one tile (4 chunks) of K or of V, issued by the whole
-    // producer warp: lane 0 arms the barrier; a tile inside one page is one
-    // 5-D box (lane 0), otherwise lane c * NB + b copies column block b of
-    // chunk c, so a tile over 16-token pages (16 boxes per tensor for D = 256)
-    // costs no more issue time than one box.
+    // TMA copies of one tile of K (CPK chunks) or of V (CPT chunks), issued by
+    // the whole producer warp: lane 0 arms the barrier; a tile inside one page
+    // is one 5-D box (lane 0), otherwise lane c * NB + b copies column block b
+    // of chunk c, so a tile over 16-token pages (16 boxes per tensor for
+    // D = 256) costs no more issue time than one box.
     int issued_k = 0, issued_v = 0;
     auto issue_tile = [&](int i, int tensor, uint64_t policy) {
         constexpr int NB = F8 ? D / 128 : C::DB;  // boxes per 16-token chunk (128-byte columns)
@@ -404,10 +423,11 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
         const int s = F8 ? i % (NSG > 0 ? NSG : 1) : (tensor == 0 ? i % NK : i % NV);
         uint64_t *bar = F8 ? (tensor == 0 ? &kst_full[s] : &vst_full[s]) : (tensor == 0 ? &k_full[s] : &v_full[s]);
         uint8_t *dst0 = F8 ? smem + C::OFF_STG + (tensor * NSG + s) * C::STG_BYTES
-                           : smem + (tensor == 0 ? s * C::TILE_BYTES : C::OFF_V + s * C::TILE_BYTES);
+                           : smem + (tensor == 0 ? s * C::KTILE_BYTES : C::OFF_V + s * C::TILE_BYTES);
         const CUtensorMap *m4 = tensor == 0 ? &tm_k : &tm_v;
         const CUtensorMap *m5 = tensor == 0 ? &tm_k64 : &tm_v64;
-        const int nc = min(CPT, n_my - i * CPT);  // chunks in this tile
+        const int cpt = tensor == 0 ? CPK : CPT, tt = cpt * kChunk;  // chunks and tokens per tile
+        const int nc = min(cpt, n_my - i * cpt);  // chunks in this tile
         if (lane == 0) mbar_arrive_expect_tx(bar, nc * C::CHUNK_BYTES);
         __syncwarp();
         auto page_of = [&](int lp) {
@@ -418,22 +438,23 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
             }
             return page;
         };
-        const int t00 = (c_begin + i * CPT) * kChunk;
+        const int t00 = (c_begin + i * cpt) * kChunk;
         const int lp0 = t00 / p.block_size, off0 = t00 - lp0 * p.block_size;
-        if (nc == CPT && off0 + TT <= p.block_size) {
-            // the whole tile lies in one page: one copy lands it as [blocks][64 tokens][128 B]
+        if (nc == cpt && off0 + tt <= p.block_size) {
+            // the whole tile lies in one page: one copy lands it as [blocks][tt tokens][128 B]
             if (lane == 0) tma_load_5d(dst0, m5, bar, 0, off0, 0, kvh, page_of(lp0), policy);
         } else if (lane < nc * NB) {
             const int c = lane / NB, db = lane % NB;
             const int t0 = t00 + c * kChunk, lp = t0 / p.block_size;
-            tma_load_4d(dst0 + db * TT * 128 + c * kChunk * 128, m4, bar, db * BW, kvh, t0 - lp * p.block_size,
+            tma_load_4d(dst0 + db * tt * 128 + c * kChunk * 128, m4, bar, db * BW, kvh, t0 - lp * p.block_size,
                         page_of(lp), policy);
         }
         __syncwarp();
     };
+    static_assert(CPK * (F8 ? D / 128 : C::DB) <= 32, "a lane per box of a tile");
     // tiles that end before the new rows (early_kv reads only those before the wait)
-    auto before_new_rows = [&](int i) {
-        return (c_begin + i * CPT + min(CPT, n_my - i * CPT)) * kChunk <= L - p.q_len;
+    auto before_new_rows = [&](int i, int cpt) {
+        return (c_begin + i * cpt + min(cpt, n_my - i * cpt)) * kChunk <= L - p.q_len;
     };
     if (p.early_kv) {
         __syncthreads();  // barrier initialisation and the page table are visible to the producer warp
@@ -441,8 +462,8 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
             // first use of each slot: tiles that end before the new rows
             const uint64_t policy = l2_policy_evict_first();
             constexpr int FK = F8 ? NSG : NK, FV = F8 ? NSG : NV;  // slots the copies land in
-            while (issued_k < min(FK, n_tiles) && before_new_rows(issued_k)) issue_tile(issued_k++, 0, policy);
-            while (issued_v < min(FV, n_tiles) && before_new_rows(issued_v)) issue_tile(issued_v++, 1, policy);
+            while (issued_k < min(FK, n_tiles) && before_new_rows(issued_k, CPK)) issue_tile(issued_k++, 0, policy);
+            while (issued_v < min(FV, n_vtiles) && before_new_rows(issued_v, CPT)) issue_tile(issued_v++, 1, policy);
         }
         pdl_wait_primary();
     }
@@ -496,19 +517,30 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
                 qv[v] = make_uint4(bf16x2_to_f16x2_scaled(qv[v].x, q_pre), bf16x2_to_f16x2_scaled(qv[v].y, q_pre),
                                    bf16x2_to_f16x2_scaled(qv[v].z, q_pre), bf16x2_to_f16x2_scaled(qv[v].w, q_pre));
         }
+        if constexpr (QSM) {
+            // row rho of the block at [D/64 column blocks][M rows][128 B], 16-byte unit u of a
+            // row stored at unit u ^ (row % 8): the K-major operand layout with the 128-byte swizzle
+            const int r = threadIdx.x;
 #pragma unroll
-        for (int c = 0; c < NQ / 8; ++c) {
-            uint32_t r[32];
+            for (int v = 0; v < NQ; ++v)
+                *reinterpret_cast<uint4 *>(smem + C::OFF_Q + (v / 8) * (C::M * 128) + r * 128 +
+                                           (((v % 8) ^ (r % 8)) << 4)) = qv[v];
+            tc::fence_async_smem();  // the rows are read by the tensor core
+        } else {
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                r[4 * v] = qv[8 * c + v].x;
-                r[4 * v + 1] = qv[8 * c + v].y;
-                r[4 * v + 2] = qv[8 * c + v].z;
-                r[4 * v + 3] = qv[8 * c + v].w;
+            for (int c = 0; c < NQ / 8; ++c) {
+                uint32_t r[32];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    r[4 * v] = qv[8 * c + v].x;
+                    r[4 * v + 1] = qv[8 * c + v].y;
+                    r[4 * v + 2] = qv[8 * c + v].z;
+                    r[4 * v + 3] = qv[8 * c + v].w;
+                }
+                tc::st32(lane_base + C::Q_COL + 32 * c, r);
             }
-            tc::st32(lane_base + C::Q_COL + 32 * c, r);
+            tc::wait_st();
         }
-        tc::wait_st();
         tc::fence_before();
         asm volatile("bar.arrive 1, 160;" ::: "memory");
     } else if (warp == 4) {
@@ -528,12 +560,12 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
         constexpr int FK = F8 ? NSG : NK, FV = F8 ? NSG : NV;
         uint64_t *ke = F8 ? kst_empty : k_empty;
         uint64_t *ve = F8 ? vst_empty : v_empty;
-        while (issued_k < n_tiles || issued_v < n_tiles) {
+        while (issued_k < n_tiles || issued_v < n_vtiles) {
             bool go_k = false, go_v = false;
             if (lane == 0) {
                 go_k = issued_k < n_tiles &&
                        (issued_k < FK || mbar_test_wait(&ke[issued_k % FK], ((issued_k / FK) - 1) & 1));
-                go_v = issued_v < n_tiles &&
+                go_v = issued_v < n_vtiles &&
                        (issued_v < FV || mbar_test_wait(&ve[issued_v % FV], ((issued_v / FV) - 1) & 1));
             }
             go_k = __shfl_sync(0xffffffffu, go_k, 0);
@@ -565,7 +597,7 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
     } else if (warp == 4) {
         // ---------------- MMA issue: one lane ----------------
         if (lane == 0) {
-            constexpr uint32_t kIdQK = tc::idesc_bf16(128, TT, 0, F8);
+            constexpr uint32_t kIdQK = tc::idesc_bf16(128, TK, 0, F8);
             constexpr uint32_t kIdPV = tc::idesc_bf16(128, D, 1, F8);
             // Event loop: each product is issued as soon as its own inputs are
             // ready -- O += P_i V_i when the softmax warps have written P_i,
@@ -578,23 +610,42 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
             bool ok = true;
             while (next_pv < n_tiles) {
                 bool progress = false;
-                if (next_pv < next_qk && mbar_test_wait(&p_full[next_pv % NSB], (next_pv / NSB) & 1) &&
-                    mbar_test_wait(&v_full[next_pv % NV], (next_pv / NV) & 1)) {
-                    const int i = next_pv, j = i % NSB;
-                    tc::fence_after();
-                    const uint32_t v_addr = smem_addr(smem + C::OFF_V + (i % NV) * C::TILE_BYTES);
-#pragma unroll
-                    for (int ks = 0; ks < TT / 16; ++ks) {
-                        // V: MN-major; 64-dim blocks TT x 128 B apart (LBO), 8-token groups 1 KiB apart (SBO)
-                        const uint64_t bdesc = tc::sdesc(v_addr + ks * 16 * 128, TT * 128, 1024, 2);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            // P (head, then residual): 16 tokens = 8 columns per step
-                            const uint32_t a_tm = tmem + C::S_COL + j * TT + h * (TT / 2) + ks * 8;
-                            tc::mma_bf16_ta(tmem + C::O_COL, a_tm, bdesc, kIdPV, (i > 0 || ks > 0 || h > 0) ? 1u : 0u);
+                // the V tiles of score tile next_pv (VPK, fewer at a split's end) have landed
+                auto v_ready = [&](int i) {
+                    if constexpr (VPK == 1) {
+                        return mbar_test_wait(&v_full[i % NV], (i / NV) & 1);
+                    } else {
+                        const int nvt = min(VPK, n_vtiles - i * VPK);
+                        for (int h2 = 0; h2 < nvt; ++h2) {
+                            const int vt = i * VPK + h2;
+                            if (!mbar_test_wait(&v_full[vt % NV], (vt / NV) & 1)) return false;
                         }
+                        return true;
                     }
-                    tc::commit(&v_empty[i % NV]);
+                };
+                if (next_pv < next_qk && mbar_test_wait(&p_full[next_pv % NSB], (next_pv / NSB) & 1) &&
+                    v_ready(next_pv)) {
+                    const int i = next_pv, j = i % NSB;
+                    const int nvt = VPK == 1 ? 1 : min(VPK, n_vtiles - i * VPK);
+                    tc::fence_after();
+#pragma unroll 1
+                    for (int h2 = 0; h2 < nvt; ++h2) {
+                        const int vt = i * VPK + h2;
+                        const uint32_t v_addr = smem_addr(smem + C::OFF_V + (vt % NV) * C::TILE_BYTES);
+#pragma unroll
+                        for (int ks = 0; ks < TT / 16; ++ks) {
+                            // V: MN-major; 64-dim blocks TT x 128 B apart (LBO), 8-token groups 1 KiB apart (SBO)
+                            const uint64_t bdesc = tc::sdesc(v_addr + ks * 16 * 128, TT * 128, 1024, 2);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                // P (head, then residual) of this 64-key half: 16 tokens = 8 columns per step
+                                const uint32_t a_tm = tmem + C::SBUF(j) + h2 * TT + h * (TT / 2) + ks * 8;
+                                tc::mma_bf16_ta(tmem + C::O_COL, a_tm, bdesc, kIdPV,
+                                                (i > 0 || h2 > 0 || ks > 0 || h > 0) ? 1u : 0u);
+                            }
+                        }
+                        tc::commit(&v_empty[vt % NV]);
+                    }
                     tc::commit(&o_done[j]);
                     ++next_pv;
                     progress = true;
@@ -603,13 +654,19 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
                     const int i = next_qk, s = i % NK, j = i % NSB;
                     if (mbar_test_wait(&k_full[s], (i / NK) & 1)) {
                         tc::fence_after();
-                        const uint32_t k_addr = smem_addr(smem + s * C::TILE_BYTES);
+                        const uint32_t k_addr = smem_addr(smem + s * C::KTILE_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             // 16-element k steps: +32 B inside a 128-byte swizzle row, next 64-dim block further on
-                            const uint32_t koff = (kk >> 2) * (TT * 128) + (kk & 3) * 32;
-                            tc::mma_bf16_ta(tmem + C::S_COL + j * TT, tmem + C::Q_COL + kk * 8,
-                                            tc::sdesc(k_addr + koff, 16, 1024, 2), kIdQK, kk > 0 ? 1u : 0u);
+                            const uint32_t koff = (kk >> 2) * (TK * 128) + (kk & 3) * 32;
+                            if constexpr (QSM) {  // Q from shared memory, laid out like K with M rows
+                                const uint32_t qoff = (kk >> 2) * (C::M * 128) + (kk & 3) * 32;
+                                tc::mma_bf16(tmem + C::SBUF(j), tc::sdesc(smem_addr(smem + C::OFF_Q) + qoff, 16, 1024, 2),
+                                             tc::sdesc(k_addr + koff, 16, 1024, 2), kIdQK, kk > 0 ? 1u : 0u);
+                            } else {
+                                tc::mma_bf16_ta(tmem + C::SBUF(j), tmem + C::Q_COL + kk * 8,
+                                                tc::sdesc(k_addr + koff, 16, 1024, 2), kIdQK, kk > 0 ? 1u : 0u);
+                            }
                         }
                         tc::commit(&k_empty[s]);
                         tc::commit(&s_full[j]);
@@ -718,101 +775,223 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB>::THREADS, 1)
                 ok = false;
                 break;
             }
-            tc::fence_after();
-            float sv[TT];
-            {
-                uint32_t r[TT / 16][16];  // the tile's scores: all loads in flight, one wait
-#pragma unroll
-                for (int c0 = 0; c0 < TT / 16; ++c0) tc::ld16_nowait(lane_base + C::S_COL + j * TT + 16 * c0, r[c0]);
-                tc::wait_ld();
-#pragma unroll
-                for (int c = 0; c < TT; ++c) sv[c] = __uint_as_float(r[c / 16][c % 16]);
-            }
-            if (i >= NSB && !wait_pv(i - NSB)) {
-                ok = false;
-                break;
-            }
-
-            const int t0 = (c_begin + i * CPT) * kChunk;
-            float mx = -INFINITY;
-            // the exponent is 2^(sv * mul - m): raw scores with mul = scale when
-            // every key of the tile is visible to this row (no mask, and the
-            // max of the scaled scores is the scaled max for scale > 0), else
-            // scaled and masked scores with mul = 1
-            float mul = 1.f;
-            if (sl > 0.f && t0 + TT - 1 <= lim && t0 >= lo) {
-                float mr = sv[0];
-#pragma unroll
-                for (int c = 1; c + 1 < TT; c += 2) mr = fmax3(mr, sv[c], sv[c + 1]);
-                mr = fmaxf(mr, sv[TT - 1]);
-                mx = mr * sl;
-                mul = sl;
-            } else {
-#pragma unroll
-                for (int c = 0; c < TT; ++c) sv[c] = (t0 + c <= lim && t0 + c >= lo) ? sv[c] * sl : -INFINITY;
-#pragma unroll
-                for (int c = 0; c < TT; c += 2) mx = fmax3(mx, sv[c], sv[c + 1]);
-            }
-            // lazy rescale: only when the max grows by more than 2^kLazy, and
-            // then only after the previous tile's P.V product has finished
-            const bool raise = mx > m_ref + kLazy;
-            const bool need_rescale = raise && m_ref != -INFINITY;
-            if (__any_sync(0xffffffffu, need_rescale)) {
-                if (!wait_pv(i - 1)) {
-                    ok = false;
-                    break;
-                }
+            if constexpr (VPK == 1) {
                 tc::fence_after();
-                const float alpha = need_rescale ? fast_exp2(m_ref - mx) : 1.f;
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 16) {
-                    float ov[16];
-                    tc::ld16(lane_base + C::O_COL + c0, ov);
+                float sv[TT];
+                {
+                    uint32_t r[TT / 16][16];  // the tile's scores: all loads in flight, one wait
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) ov[c] *= alpha;
-                    tc::st16(lane_base + C::O_COL + c0, ov);
+                    for (int c0 = 0; c0 < TT / 16; ++c0) tc::ld16_nowait(lane_base + C::SBUF(j) + 16 * c0, r[c0]);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int c = 0; c < TT; ++c) sv[c] = __uint_as_float(r[c / 16][c % 16]);
                 }
-                if (need_rescale) l_sum *= alpha;
-            }
-            if (raise) m_ref = mx;
-            // The tile may be short or end in a partial chunk: V rows past the
-            // end hold stale data (even NaN), and 0 * NaN would reach O through
-            // the tensor core, so zero them before the P.V product reads them.
-            const int nv = min(TT, t_end - t0);
-            if (!F8 && nv < TT) {  // (fp8: the widening warp writes those rows as zeros)
-                if (!__all_sync(0xffffffffu, mbar_wait(&v_full[i % NV], (i / NV) & 1, &flags[0]))) {
+                if (i >= NSB && !wait_pv(i - NSB)) {
                     ok = false;
                     break;
                 }
-                uint8_t *vst = smem + C::OFF_V + (i % NV) * C::TILE_BYTES;
-                for (int idx = threadIdx.x; idx < (TT - nv) * C::DB * 8; idx += 128) {
-                    const int t = nv + idx / (C::DB * 8), rem = idx % (C::DB * 8);
-                    *reinterpret_cast<uint4 *>(vst + (rem >> 3) * (TT * 128) + t * 128 + (rem & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                tc::fence_async_smem();  // zeroed V rows are read by the tensor core
-            }
-            // P = 2^(s - m) as a bf16 head and a bf16 residual, written over S_i
-            // (tokens packed two per column: head in the first 32 columns)
-            // with no visible key yet (m = -inf) every p is 0: 2^(x - inf)
-            const float m_use = m_ref == -INFINITY ? INFINITY : m_ref;
-            float2 ps2 = make_float2(0.f, 0.f);
-            uint32_t hw[TT / 2], lw[TT / 2];
+
+                const int t0 = (c_begin + i * CPT) * kChunk;
+                float mx = -INFINITY;
+                // the exponent is 2^(sv * mul - m): raw scores with mul = scale when
+                // every key of the tile is visible to this row (no mask, and the
+                // max of the scaled scores is the scaled max for scale > 0), else
+                // scaled and masked scores with mul = 1
+                float mul = 1.f;
+                if (sl > 0.f && t0 + TT - 1 <= lim && t0 >= lo) {
+                    float mr = sv[0];
 #pragma unroll
-            for (int c = 0; c < TT / 2; ++c) {
-                const float p0 = fast_exp2(fmaf(sv[2 * c], mul, -m_use));
-                const float p1 = fast_exp2(fmaf(sv[2 * c + 1], mul, -m_use));
-                ps2 = __fadd2_rn(ps2, make_float2(p0, p1));
-                if constexpr (F8)
-                    split_f16(p0, p1, hw[c], lw[c]);
-                else
-                    split_bf16(p0, p1, hw[c], lw[c]);
+                    for (int c = 1; c + 1 < TT; c += 2) mr = fmax3(mr, sv[c], sv[c + 1]);
+                    mr = fmaxf(mr, sv[TT - 1]);
+                    mx = mr * sl;
+                    mul = sl;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < TT; ++c) sv[c] = (t0 + c <= lim && t0 + c >= lo) ? sv[c] * sl : -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < TT; c += 2) mx = fmax3(mx, sv[c], sv[c + 1]);
+                }
+                // lazy rescale: only when the max grows by more than 2^kLazy, and
+                // then only after the previous tile's P.V product has finished
+                const bool raise = mx > m_ref + kLazy;
+                const bool need_rescale = raise && m_ref != -INFINITY;
+                if (__any_sync(0xffffffffu, need_rescale)) {
+                    if (!wait_pv(i - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const float alpha = need_rescale ? fast_exp2(m_ref - mx) : 1.f;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 16) {
+                        float ov[16];
+                        tc::ld16(lane_base + C::O_COL + c0, ov);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) ov[c] *= alpha;
+                        tc::st16(lane_base + C::O_COL + c0, ov);
+                    }
+                    if (need_rescale) l_sum *= alpha;
+                }
+                if (raise) m_ref = mx;
+                // The tile may be short or end in a partial chunk: V rows past the
+                // end hold stale data (even NaN), and 0 * NaN would reach O through
+                // the tensor core, so zero them before the P.V product reads them.
+                const int nv = min(TT, t_end - t0);
+                if (!F8 && nv < TT) {  // (fp8: the widening warp writes those rows as zeros)
+                    if (!__all_sync(0xffffffffu, mbar_wait(&v_full[i % NV], (i / NV) & 1, &flags[0]))) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *vst = smem + C::OFF_V + (i % NV) * C::TILE_BYTES;
+                    for (int idx = threadIdx.x; idx < (TT - nv) * C::DB * 8; idx += 128) {
+                        const int t = nv + idx / (C::DB * 8), rem = idx % (C::DB * 8);
+                        *reinterpret_cast<uint4 *>(vst + (rem >> 3) * (TT * 128) + t * 128 + (rem & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    tc::fence_async_smem();  // zeroed V rows are read by the tensor core
+                }
+                // P = 2^(s - m) as a bf16 head and a bf16 residual, written over S_i
+                // (tokens packed two per column: head in the first 32 columns)
+                // with no visible key yet (m = -inf) every p is 0: 2^(x - inf)
+                const float m_use = m_ref == -INFINITY ? INFINITY : m_ref;
+                float2 ps2 = make_float2(0.f, 0.f);
+                uint32_t hw[TT / 2], lw[TT / 2];
+#pragma unroll
+                for (int c = 0; c < TT / 2; ++c) {
+                    const float p0 = fast_exp2(fmaf(sv[2 * c], mul, -m_use));
+                    const float p1 = fast_exp2(fmaf(sv[2 * c + 1], mul, -m_use));
+                    ps2 = __fadd2_rn(ps2, make_float2(p0, p1));
+                    if constexpr (F8)
+                        split_f16(p0, p1, hw[c], lw[c]);
+                    else
+                        split_bf16(p0, p1, hw[c], lw[c]);
+                }
+                l_sum += ps2.x + ps2.y;
+                tc::st32(lane_base + C::SBUF(j), hw);
+                tc::st32(lane_base + C::SBUF(j) + TT / 2, lw);
+                tc::wait_st();
+                tc::fence_before();
+            } else {
+                tc::fence_after();
+                const int t0 = (c_begin + i * CPK) * kChunk;        // first key of the score tile
+                const int nvt = min(VPK, n_vtiles - i * VPK);       // its 64-key halves with keys of this split
+                // The exponent is 2^(sv * mul - m): raw scores with mul = scale when
+                // every key of the tile is visible to this row (no mask, and the
+                // max of the scaled scores is the scaled max for scale > 0), else
+                // scaled and masked scores with mul = 1.
+                const bool all_visible = sl > 0.f && t0 + TK - 1 <= lim && t0 >= lo;
+                const float mul = all_visible ? sl : 1.f;
+                // 64 scores of half h2 (all loads in flight, one wait), masked and scaled unless all_visible
+                float sv[TT];
+                auto load_half = [&](int h2) {
+                    uint32_t r[TT / 16][16];
+#pragma unroll
+                    for (int c0 = 0; c0 < TT / 16; ++c0)
+                        tc::ld16_nowait(lane_base + C::SBUF(j) + h2 * TT + 16 * c0, r[c0]);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int c = 0; c < TT; ++c) sv[c] = __uint_as_float(r[c / 16][c % 16]);
+                    if (!all_visible) {
+                        const int th = t0 + h2 * TT;
+#pragma unroll
+                        for (int c = 0; c < TT; ++c) sv[c] = (th + c <= lim && th + c >= lo) ? sv[c] * sl : -INFINITY;
+                    }
+                };
+                auto half_max = [&]() {
+                    float mh;
+                    if (all_visible) {
+                        mh = sv[0];
+#pragma unroll
+                        for (int c = 1; c + 1 < TT; c += 2) mh = fmax3(mh, sv[c], sv[c + 1]);
+                        mh = fmaxf(mh, sv[TT - 1]) * sl;
+                    } else {
+                        mh = -INFINITY;
+#pragma unroll
+                        for (int c = 0; c < TT; c += 2) mh = fmax3(mh, sv[c], sv[c + 1]);
+                    }
+                    return mh;
+                };
+                float mx = -INFINITY;
+                for (int h2 = 0; h2 < nvt; ++h2) {  // the tile's max, over every half
+                    load_half(h2);
+                    mx = fmaxf(mx, half_max());
+                }
+                if (i >= NSB && !wait_pv(i - NSB)) {
+                    ok = false;
+                    break;
+                }
+                // lazy rescale: only when the max grows by more than 2^kLazy, and
+                // then only after the previous tile's P.V product has finished
+                const bool raise = mx > m_ref + kLazy;
+                const bool need_rescale = raise && m_ref != -INFINITY;
+                if (__any_sync(0xffffffffu, need_rescale)) {
+                    if (!wait_pv(i - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const float alpha = need_rescale ? fast_exp2(m_ref - mx) : 1.f;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 16) {
+                        float ov[16];
+                        tc::ld16(lane_base + C::O_COL + c0, ov);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) ov[c] *= alpha;
+                        tc::st16(lane_base + C::O_COL + c0, ov);
+                    }
+                    if (need_rescale) l_sum *= alpha;
+                }
+                if (raise) m_ref = mx;
+                // A V tile may be short or end in a partial chunk: V rows past the
+                // end hold stale data (even NaN), and 0 * NaN would reach O through
+                // the tensor core, so zero them before the P.V product reads them.
+                bool zero_ok = true;
+                for (int h2 = 0; h2 < nvt && !F8; ++h2) {  // (fp8: the widening warp writes those rows as zeros)
+                    const int vt = i * VPK + h2;
+                    const int nv = min(TT, t_end - (t0 + h2 * TT));
+                    if (nv >= TT) continue;
+                    if (!__all_sync(0xffffffffu, mbar_wait(&v_full[vt % NV], (vt / NV) & 1, &flags[0]))) {
+                        zero_ok = false;
+                        break;
+                    }
+                    uint8_t *vst = smem + C::OFF_V + (vt % NV) * C::TILE_BYTES;
+                    for (int idx = threadIdx.x; idx < (TT - nv) * C::DB * 8; idx += 128) {
+                        const int t = nv + idx / (C::DB * 8), rem = idx % (C::DB * 8);
+                        *reinterpret_cast<uint4 *>(vst + (rem >> 3) * (TT * 128) + t * 128 + (rem & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    tc::fence_async_smem();  // zeroed V rows are read by the tensor core
+                }
+                if (!zero_ok) {
+                    ok = false;
+                    break;
+                }
+                // P = 2^(s - m) per 64-key half as a bf16 head and a bf16 residual,
+                // written over that half's S columns (tokens packed two per column:
+                // head in the first 32 columns); with no visible key yet (m = -inf)
+                // every p is 0: 2^(x - inf)
+                const float m_use = m_ref == -INFINITY ? INFINITY : m_ref;
+                for (int h2 = 0; h2 < nvt; ++h2) {
+                    if (VPK > 1) load_half(h2);  // (one half: its scores are still in sv)
+                    float2 ps2 = make_float2(0.f, 0.f);
+                    uint32_t hw[TT / 2], lw[TT / 2];
+#pragma unroll
+                    for (int c = 0; c < TT / 2; ++c) {
+                        const float p0 = fast_exp2(fmaf(sv[2 * c], mul, -m_use));
+                        const float p1 = fast_exp2(fmaf(sv[2 * c + 1], mul, -m_use));
+                        ps2 = __fadd2_rn(ps2, make_float2(p0, p1));
+                        if constexpr (F8)
+                            split_f16(p0, p1, hw[c], lw[c]);
+                        else
+                            split_bf16(p0, p1, hw[c], lw[c]);
+                    }
+                    l_sum += ps2.x + ps2.y;
+                    tc::st32(lane_base + C::SBUF(j) + h2 * TT, hw);
+                    tc::st32(lane_base + C::SBUF(j) + h2 * TT + TT / 2, lw);
+                }
+                tc::wait_st();
+                tc::fence_before();
             }
-            l_sum += ps2.x + ps2.y;
-            tc::st32(lane_base + C::S_COL + j * TT, hw);
-            tc::st32(lane_base + C::S_COL + j * TT + TT / 2, lw);
-            tc::wait_st();
-            tc::fence_before();
             mbar_arrive(&p_full[j]);
         }
         // Epilogue: wait for the last P.V MMA, normalise and write this row.
