@@ -222,6 +222,32 @@ def test_verify_rescale_window(oracle_mod):
     assert_parity(out, oracle_out(oracle_mod, prob, window=2048), rel_l2=REL_L2_VERIFY, what="verify window saw")
 
 
+@pytest.mark.parametrize("pattern", ["saw", "rise", "spike", "step"])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_verify_rescale_row_blocks(oracle_mod, pattern, splits):
+    """24 rows x 6 heads = 144 rows per KV head: two row blocks, the shape
+    that runs 128-key score tiles, where a tile's max is taken over both of
+    its 64-key halves before any of its P is written.  (With 48 rows the
+    steepest ramps reach a rel-L2 of 1.35e-4 from the fp32 scores alone, the
+    same with 64-key tiles.)"""
+    prob = ramp_problem(381, [3000, 1700], 832, pattern, q_len=24)
+    write_ramp_rows(oracle_mod, prob, 11)
+    out, status, plan = run_attention(prob, num_splits=splits)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05 and plan["num_splits"] == splits
+    assert split_raises(oracle_mod, prob, plan, row=23) >= 1
+    assert_parity(out, oracle_out(oracle_mod, prob), rel_l2=REL_L2_VERIFY,
+                  what=f"verify row blocks {pattern} splits={splits}")
+
+
+def test_verify_rescale_row_blocks_window(oracle_mod):
+    prob = ramp_problem(391, [4000], 784, "saw", q_len=24)
+    write_ramp_rows(oracle_mod, prob, 13)
+    out, status, plan = run_attention(prob, window=2048)
+    assert status == 0
+    assert_parity(out, oracle_out(oracle_mod, prob, window=2048), rel_l2=REL_L2_VERIFY,
+                  what="verify row blocks window saw")
+
+
 def test_verify_rescale_fp8(oracle_mod):
     """The fp8 verify over the sawtooth (the cache is built directly; no new
     rows are written)."""
