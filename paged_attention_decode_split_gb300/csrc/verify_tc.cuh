@@ -612,12 +612,7 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB, TK>::THREADS,
                 bool progress = false;
                 // the V tiles of score tile next_pv (VPK, fewer at a split's end) have landed
                 auto v_ready = [&](int i) {
-                    // A 64-key tile keeps its scores in registers from the max to the
-            // exponentials (one load); a 128-key tile takes its max over both
-            // halves first and loads each half again for P (the one-load form
-            // for 128 keys would not fit the registers, and the two-pass form
-            // makes the fp8 variants spill).
-            if constexpr (VPK == 1) {
+                    if constexpr (VPK == 1) {
                         return mbar_test_wait(&v_full[i % NV], (i / NV) & 1);
                     } else {
                         const int nvt = min(VPK, n_vtiles - i * VPK);
@@ -780,6 +775,11 @@ __global__ void __launch_bounds__(VerifyTcCfg<D, NK, NV, NSG, NSB, TK>::THREADS,
                 ok = false;
                 break;
             }
+            // A 64-key tile keeps its scores in registers from the max to the
+            // exponentials (one load); a 128-key tile takes its max over both
+            // halves first and loads each half again for P (the one-load form
+            // for 128 keys would not fit the registers, and the two-pass form
+            // makes the fp8 variants spill).
             if constexpr (VPK == 1) {
                 tc::fence_after();
                 float sv[TT];
