@@ -293,3 +293,12 @@ def test_binding_checks_tensors_before_calling(lib):
         pa.reshape_and_cache_fp8(rows, rows, cache, cache, slots, scales, scales)
     with pytest.raises(ValueError, match="k_new: a CUDA tensor is required"):
         pa.reshape_and_cache_fp8(rows, rows, codes, codes, slots, scales, scales)
+
+
+def test_compiled_binding_knows_its_entry_points(lib):
+    """The compiled module takes the C entry points by name from the loaded
+    library; an unknown name is refused."""
+    import paged_attention_decode_split_gb300 as pkg
+    assert pkg._bind is not None
+    with pytest.raises(ValueError):
+        pkg._bind.set_entry("pa_no_such_entry", 0)
