@@ -14,6 +14,7 @@
 // library and its host-side state (last plan, tensor-map cache).
 #include <torch/extension.h>
 
+#include <c10/cuda/CUDAFunctions.h>
 #include <c10/cuda/CUDAStream.h>
 
 #include <array>
@@ -81,10 +82,14 @@ void expect(const Tensor &t, const char *name, bool type_ok, const char *want, c
     if (check_shape) TORCH_CHECK_VALUE(t.sizes().equals(shape), name, ": shape ", t.sizes(), "; expected ", shape);
 }
 
+// The library launches on the current device, so every tensor must live there.
 void placed(std::initializer_list<std::pair<const Tensor *, const char *>> ts) {
+    int dev = -1;
     for (const auto &[t, name] : ts) {
         if (t == nullptr) continue;
         TORCH_CHECK_VALUE(t->is_cuda(), name, ": a CUDA tensor is required (got ", t->device(), ")");
+        if (dev < 0) dev = c10::cuda::current_device();
+        TORCH_CHECK_VALUE(t->get_device() == dev, name, ": on ", t->device(), ", but the current device is cuda:", dev);
         TORCH_CHECK_VALUE(t->is_contiguous(), name, ": the tensor must be contiguous");
     }
 }
