@@ -434,6 +434,32 @@ def test_verify_maximum_rows_sampled(oracle_mod):
                   what="verify 32768 rows (sampled)")
 
 
+
+def test_verify_maximum_rows_sampled_d256(oracle_mod):
+    """q_len x G = 4096 x 8 = 32768 rows per KV head at head_dim 256: the
+    largest block set of the 128-key score tiles (256 row blocks x 4 KV
+    heads), sampled against the oracle, the rest checked finite."""
+    q_len = 4096
+    prob = make_problem(191, num_seqs=1, seq_lens=[q_len + 700], num_q_heads=32, num_kv_heads=4, head_dim=256,
+                        block_size=832, q_len=q_len, scale=1 / 16, poison_unused=True)
+    write_new_rows(prob, 31)
+    out, status, plan = run_attention(prob)
+    assert status == 0 and plan["path_id"] == pa.PA_PATH_VERIFY_TCGEN05
+    assert torch.isfinite(out).all()
+    g = torch.Generator().manual_seed(5)
+    rows = [0, 1, 15, 16, 2047, q_len - 1] + torch.randint(0, q_len, (10,), generator=g).tolist()
+    heads = [0, 7, 8, 31]
+    q, kc, vc = bits(prob.q[0]), bits(prob.k_cache[0]), bits(prob.v_cache[0])
+    got, ref = [], []
+    for r in rows:
+        for h in heads:
+            o, _, _ = oracle_mod.attention_partial(q, kc, vc, prob.block_table.numpy(), prob.seq_lens.numpy(),
+                                                   prob.scale, r, h, 0, 1 << 40, q_len=q_len)
+            got.append(out[r, h])
+            ref.append(o)
+    assert_parity(torch.stack(got)[:, None, :], np.stack(ref)[:, None, :], rel_l2=REL_L2_VERIFY,
+                  what="verify 32768 rows d256 (sampled)")
+
 # -- the other benchmarked workloads at full size, in their benchmark launch ---------
 
 def test_decode_window2048_l32768_bs784_workload(oracle_mod):
