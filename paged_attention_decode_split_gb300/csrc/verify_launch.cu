@@ -36,20 +36,24 @@ bool verify_supported(int head_dim, int rows) {
     return (head_dim == 256 || head_dim == 128) && rows >= 1 && rows <= 32768;
 }
 
-bool verify_wide_score_tiles(int head_dim, int rows) { return head_dim == 256 && rows > 128; }
+bool verify_wide_score_tiles(int head_dim, int rows) { return (head_dim == 256 || head_dim == 128) && rows > 128; }
 
 // Each CTA runs one M = 128 block of rows.  With several blocks per KV head
-// (D = 256) the blocks read their tiles mostly from L2 and the score
-// product's instruction rate bounds the tile: 128-key score tiles, Q in
-// shared memory, one K slot of 128 keys and three V slots of 64.  A single
-// block streams from HBM and keeps the 64-key tiles and deeper rings.
+// the blocks read their tiles mostly from L2 and the score product's
+// instruction rate bounds the tile: 128-key score tiles (D = 256: Q in shared
+// memory, one K slot of 128 keys and three V slots of 64; D = 128: Q in tensor
+// memory, three K slots and six V slots).  A single block streams from HBM and
+// keeps the 64-key tiles and deeper rings.
 cudaError_t launch_verify(int head_dim, int rows, const CUtensorMap &tk, const CUtensorMap &tv,
                           const CUtensorMap &tk64, const CUtensorMap &tv64, const CUtensorMap &tk128,
                           const VerifyParams &p, dim3 grid, cudaStream_t stream) {
-    if (verify_wide_score_tiles(head_dim, rows))  // K's whole-tile boxes are 128 tokens
-        return launch_verify_tc<256, 1, 3, 0, 2, 128>(tk, tv, tk128, tv64, p, grid, stream, 104);
-    if (head_dim == 256) return launch_verify_tc<256, 4, 3, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 100);
-    if (head_dim == 128) return launch_verify_tc<128, 6, 6, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 101);
+    const bool wide = verify_wide_score_tiles(head_dim, rows);  // (K's whole-tile boxes are then 128 tokens)
+    if (head_dim == 256)
+        return wide ? launch_verify_tc<256, 1, 3, 0, 2, 128>(tk, tv, tk128, tv64, p, grid, stream, 104)
+                    : launch_verify_tc<256, 4, 3, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 100);
+    if (head_dim == 128)
+        return wide ? launch_verify_tc<128, 3, 6, 0, 2, 128>(tk, tv, tk128, tv64, p, grid, stream, 105)
+                    : launch_verify_tc<128, 6, 6, 0, 2>(tk, tv, tk64, tv64, p, grid, stream, 101);
     return cudaErrorInvalidValue;
 }
 

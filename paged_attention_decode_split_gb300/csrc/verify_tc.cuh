@@ -223,14 +223,14 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
 // of P V).  TK: keys per score tile, 64 or 128.  With 128 the score product
 // S = Q K^T is M = 128 x N = 128: half as many MMA instructions per key as with
 // N = 64, whose instruction rate bounds the tile when the tiles come from L2
-// (many row blocks per KV head, chunked prefill).  Two 128-column S/P buffers
-// and O fill tensor memory, so Q moves to shared memory as the product's A
-// operand (QSM), the K ring holds one 128-key tile and P V runs over two
-// 64-key V tiles per score tile.
+// (many row blocks per KV head, chunked prefill), and P V runs over two 64-key
+// V tiles per score tile.  At D = 256 two 128-column S/P buffers and O fill
+// tensor memory, so Q moves to shared memory as the product's A operand (QSM)
+// and the K ring holds one 128-key tile; at D = 128 Q stays in tensor memory.
 template <int D, int NK, int NV, int NSG = 0, int NSB = 2, int TK = 64>
 struct VerifyTcCfg {
     static constexpr bool F8 = NSG > 0;                // fp8 cache: e4m3 staging ring of NSG slots per tensor
-    static constexpr bool QSM = TK == 128;             // Q in shared memory
+    static constexpr bool QSM = TK == 128 && D == 256;  // Q in shared memory
     static constexpr int M = 128;                      // MMA rows (query rows, zero padded)
     static constexpr int TT = 64;                      // tokens per V tile (4 TMA chunks)
     static constexpr int CPT = TT / kChunk;            // chunks per V tile
