@@ -461,7 +461,7 @@ def bench_gpu(args, world, rank, local):
                      "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "nominal_peak": NOMINAL_HBM_GBS},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "Python binding, eager calls on an explicit stream; the step's inputs copied in from one pinned host buffer and its outputs copied out every step"},
+                "how": "the Python API (its compiled tensor binding checks every tensor), eager calls on an explicit stream; the step's inputs copied in from one pinned host buffer and its outputs copied out every step"},
         "gpu_launches": launches_per_step * args.steps,
         "device_status": st,
         "clocks": clocks.result,
