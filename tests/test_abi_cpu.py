@@ -34,6 +34,32 @@ def test_header_symbols_exported(lib):
         assert hasattr(lib, name), f"{name} declared in pagedattn.h but not exported"
 
 
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """The header compiles as C99 with warnings as errors, and a C program that
+    takes the address of every declared entry point links against the library
+    and runs (no entry point is called)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "abi.c"
+    src.write_text('#include "pagedattn.h"\n#include <stdio.h>\n'
+                   "int main(void) {\n"
+                   "    void (*const fns[])(void) = {" + ", ".join(f"(void (*)(void)){n}" for n in names) + "};\n"
+                   '    printf("%d\\n", (int)(sizeof(fns) / sizeof(fns[0])));\n'
+                   "    return 0;\n}\n")
+    exe = tmp_path / "abi"
+    build_dir = os.path.dirname(_build.LIB)
+    res = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.dirname(HEADER), str(src),
+                          "-L", build_dir, "-lpagedattn", f"-Wl,-rpath,{build_dir}", "-o", str(exe)],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0 and run.stdout.strip() == str(len(names)), run.stderr
+
+
 def test_status_strings(lib):
     for code in range(5):
         assert pa.status_string(code).startswith("PA_")
